@@ -1,0 +1,205 @@
+/*
+ * rowops.h - C ABI of librowops, the GB300 (sm_103a) row-wise
+ * normalise-and-reduce ops of a transformer training step.
+ *
+ * Every op works on row-major fp32 matrices of `rows` x `cols` with row stride
+ * `cols` and launches hand-written CUDA kernels on the caller's stream.
+ *
+ * Common contract (applies to every entry point below):
+ *   - Pointers are DEVICE pointers on the current CUDA device.  The caller owns
+ *     every buffer (inputs, outputs and workspace); the library never allocates
+ *     device memory and keeps no per-call state, so calls are reentrant.
+ *   - Calls are asynchronous: they validate the arguments on the host, queue
+ *     the kernel(s) on `stream` and return.  No call synchronises the device.
+ *   - A NULL `stream` is the legacy default stream.
+ *   - Return value: ROWOPS_OK, or the first error found.  Nothing is launched
+ *     when an error is returned, except ROWOPS_ERR_CUDA, which reports a failed
+ *     launch (the CUDA runtime's error after the launch).
+ *   - rows == 0 is a successful no-op for every op.  Negative sizes, and
+ *     rows * cols that does not fit in int64, are ROWOPS_ERR_SHAPE.
+ *   - A pointer may be NULL only when the buffer it names is empty.
+ *   - Buffers must not overlap unless the entry point says so
+ *     (ROWOPS_ERR_ALIAS); overlap is checked by address range.
+ *   - Any alignment is accepted.  16-byte aligned buffers with cols % 4 == 0
+ *     take the 128-bit vector path; others take a scalar path with the same
+ *     results up to fp32 rounding order.
+ *   - Reductions use a fixed order: repeated calls on the same inputs give
+ *     bit-identical outputs.
+ *
+ * The definitions follow four API-documentation pages:
+ *   [P1] pulsatrix HIPBackend class reference
+ *   [P2] MicroGPT CuBLASBackend API page
+ *   [P3] TorchLean NN.Runtime.Autograd.Engine.LibTorch.Kernels (CUDA buffer kernels FFI)
+ *   [P4] oxicuda-backend ComputeBackend trait
+ */
+#ifndef ROWOPS_H
+#define ROWOPS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ROWOPS_OK = 0,
+    ROWOPS_ERR_NULL = 1,      /* a required pointer is NULL */
+    ROWOPS_ERR_SHAPE = 2,     /* bad size, k, seq_len, scale, eps or grad_scale */
+    ROWOPS_ERR_ALIAS = 3,     /* buffers overlap where the op forbids it */
+    ROWOPS_ERR_WORKSPACE = 4, /* workspace missing, misaligned or too small */
+    ROWOPS_ERR_CUDA = 5       /* the CUDA runtime reported an error at launch */
+} rowops_status;
+
+/* Same object as cudaStream_t. */
+typedef struct CUstream_st *rowops_stream;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *rowops_status_string(int status);
+
+/* Number of kernels this library has queued since it was loaded (all devices,
+ * all threads).  Diagnostic counter for benchmarks. */
+uint64_t rowops_kernel_launches(void);
+
+/*
+ * Row softmax, max-subtracted.  [P1] softmax_rows(in, out, rows, cols); [P2]
+ * softmax_rows(x); [P4] softmax(..., axis) on the last axis.
+ *   y_ij = exp(x_ij - m_i) / sum_k exp(x_ik - m_i),  m_i = max_k x_ik.
+ * x, y: rows x cols.  y may be exactly x (in place, as [P1] allows); any other
+ * overlap is ROWOPS_ERR_ALIAS.  cols == 0 is a no-op ([P3] softmax "including
+ * empty tensors").
+ */
+int rowops_softmax_fwd(const float *x, float *y, int64_t rows, int64_t cols,
+                       rowops_stream stream);
+
+/*
+ * Softmax backward from the output.  [P1] softmax_rows_backward(y, dy, dx, ...);
+ * [P2] softmax_backward(s, ds).
+ *   dx_ij = y_ij * (dy_ij - sum_k y_ik * dy_ik).
+ * y, dy, dx: rows x cols.  dx must not overlap y or dy ([P1]).  cols == 0 is a
+ * no-op.
+ */
+int rowops_softmax_bwd(const float *y, const float *dy, float *dx, int64_t rows, int64_t cols,
+                       rowops_stream stream);
+
+/*
+ * Scaled causal attention softmax.  [P2] fused_attn_softmax(scores, scale) on the
+ * stacked (batch*heads*seq_len, seq_len) score rows of
+ * causal_mask_batched(scores, seq_len): row r is query i = r mod seq_len and
+ *   p_rj = exp(scale*s_rj - m_r) / sum_{k<=i} exp(scale*s_rk - m_r)  for j <= i,
+ *   p_rj = 0 (exactly +0.0)                                       for j > i,
+ * with m_r = max_{k<=i} scale*s_rk.  Only the entries j <= i of `scores` are
+ * read.  Requires seq_len >= 1, cols == seq_len, rows % seq_len == 0 and
+ * 0 < scale < inf (else ROWOPS_ERR_SHAPE).  p must not overlap scores.
+ */
+int rowops_attn_softmax_fwd(const float *scores, float *p, int64_t rows, int64_t cols,
+                            int64_t seq_len, float scale, rowops_stream stream);
+
+/*
+ * Backward of rowops_attn_softmax_fwd with respect to the raw scores, from its
+ * output p.  [P2] fused_attn_softmax_backward(s, ds, scale).
+ *   c_r = sum_{k<=i} p_rk dp_rk,  ds_rj = scale * p_rj * (dp_rj - c_r) for j <= i,
+ *   ds_rj = 0 (exactly +0.0) for j > i.
+ * Only the entries j <= i of p and dp are read.  Same shape rules as the
+ * forward.  ds must not overlap p or dp.
+ */
+int rowops_attn_softmax_bwd(const float *p, const float *dp, float *ds, int64_t rows,
+                            int64_t cols, int64_t seq_len, float scale, rowops_stream stream);
+
+/*
+ * Hard-masked row softmax.  [P3] stable row-wise hard-masked softmax.
+ *   A_i = { j : mask_ij != 0 },  y_ij = exp(x_ij - max_{A_i} x) / sum_{A_i} exp(.)
+ *   for j in A_i;  y_ij = +0.0 for j not in A_i;  a row with empty A_i is all +0.0.
+ * x, y: rows x cols fp32; mask: rows x cols bytes, any nonzero byte allows.  y may
+ * be exactly x; any other overlap (with x or mask) is ROWOPS_ERR_ALIAS.  cols == 0
+ * is a no-op.
+ */
+int rowops_masked_softmax(const float *x, const uint8_t *mask, float *y, int64_t rows,
+                          int64_t cols, rowops_stream stream);
+
+/*
+ * Per-row log-sum-exp, max-subtracted.  [P1] logsumexp_rows(in, out, rows, cols).
+ *   lse_i = m_i + log sum_j exp(x_ij - m_i).
+ * x: rows x cols; lse: rows.  cols == 0 writes -inf (log of an empty sum); a row
+ * whose maximum is +-inf gets that maximum.  lse must not overlap x.
+ */
+int rowops_logsumexp(const float *x, float *lse, int64_t rows, int64_t cols,
+                     rowops_stream stream);
+
+/*
+ * Fused softmax cross-entropy loss and logits gradient for integer targets.
+ * [P2] fused_softmax_ce_grad(logits, targets) -> (Float64 loss, grad).
+ *   loss_i = lse_i - x_{i,t_i}
+ *   grad_ij = grad_scale * (softmax(x_i)_j - [j == t_i])
+ *   *mean_loss = (1/rows) * sum_i loss_i   (double, fixed summation order)
+ * logits, grad: rows x cols fp32; targets: rows int32; row_loss: rows fp32
+ * (written, then reduced into the mean); mean_loss: ONE double in device memory.
+ * grad_scale = 1/rows gives the gradient of the mean loss.  A target outside
+ * [0, cols) cannot be checked without a device sync, so it is defined instead:
+ * that row's row_loss is NaN (hence *mean_loss is NaN) and its gradient row is
+ * grad_scale * softmax with no one-hot term.  cols == 0 and a non-finite
+ * grad_scale are ROWOPS_ERR_SHAPE.  No output may overlap another buffer.
+ */
+int rowops_softmax_ce(const float *logits, const int32_t *targets, float *grad,
+                      float *row_loss, double *mean_loss, int64_t rows, int64_t cols,
+                      float grad_scale, rowops_stream stream);
+
+/*
+ * LayerNorm forward over the columns.  [P1] layer_norm_forward(); [P2]
+ * layer_norm_forward(x, gamma, beta); [P3] layer normalisation returning
+ * (output, normalized, invStd).
+ *   mu_i = mean_j x_ij,  v_i = mean_j (x_ij - mu_i)^2 (population variance),
+ *   inv_std_i = 1/sqrt(v_i + eps),  xhat_ij = (x_ij - mu_i) * inv_std_i,
+ *   out_ij = gamma_j * xhat_ij + beta_j.
+ * x, out, xhat: rows x cols; gamma, beta: cols; inv_std: rows.  cols == 0,
+ * eps < 0 or non-finite eps are ROWOPS_ERR_SHAPE.  No output may overlap another
+ * buffer.
+ */
+int rowops_layernorm_fwd(const float *x, const float *gamma, const float *beta, float *out,
+                         float *xhat, float *inv_std, int64_t rows, int64_t cols, float eps,
+                         rowops_stream stream);
+
+/* Bytes of device workspace rowops_layernorm_bwd needs for this shape (a pure
+ * function of rows and cols; 0 when rows or cols is 0 or negative). */
+size_t rowops_layernorm_bwd_workspace(int64_t rows, int64_t cols);
+
+/*
+ * LayerNorm backward.  [P3] layer-normalisation VJP returning (dX, dGamma,
+ * dBeta); [P2] layer_norm_backward(grad, norm, std_inv, gamma); [P1]
+ * layer_norm_backward() for dX and column_sums() for the parameter sums.
+ *   g'_ij = dy_ij * gamma_j
+ *   dx_ij = inv_std_i * (g'_ij - mean_k g'_ik - xhat_ij * mean_k (g'_ik xhat_ik))
+ *   dgamma_j = sum_i dy_ij * xhat_ij,   dbeta_j = sum_i dy_ij   (overwritten)
+ * dy, xhat, dx: rows x cols; gamma, dgamma, dbeta: cols; inv_std: rows.  The
+ * column sums are deterministic: fixed blocks of rows write partial sums into
+ * `workspace` (at least rowops_layernorm_bwd_workspace(rows, cols) bytes of
+ * 16-byte aligned device memory; its contents need not be initialised and are
+ * garbage afterwards), then a second kernel adds the partials in a fixed order.
+ * Concurrent calls need separate workspaces.  cols == 0 is ROWOPS_ERR_SHAPE; a
+ * short, NULL or misaligned workspace is ROWOPS_ERR_WORKSPACE.  No output may
+ * overlap another buffer.
+ */
+int rowops_layernorm_bwd(const float *dy, const float *gamma, const float *xhat,
+                         const float *inv_std, float *dx, float *dgamma, float *dbeta,
+                         int64_t rows, int64_t cols, void *workspace, size_t workspace_bytes,
+                         rowops_stream stream);
+
+/*
+ * Top-k kept mask.  [P3] kept mask (Spec.MoE.kept): entry i of a row is kept
+ * when fewer than k entries of the row beat it; entry j beats entry i when
+ * x_j > x_i, or when neither is larger and j < i.
+ *   kept_ij = 1.0f if #{ j' : j' beats j } < k, else 0.0f.
+ * The result is exact (comparisons and counts only) and equals the literal
+ * compare-and-count for every input, NaN included (a NaN is neither larger nor
+ * smaller than anything, so it ties).  x, kept: rows x cols fp32.  Requires
+ * 1 <= k <= cols ([P1] top_k_rows precondition), else ROWOPS_ERR_SHAPE.  kept
+ * must not overlap x.
+ */
+int rowops_topk_kept(const float *x, float *kept, int64_t rows, int64_t cols, int64_t k,
+                     rowops_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ROWOPS_H */
