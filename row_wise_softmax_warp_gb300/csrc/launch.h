@@ -1,0 +1,103 @@
+// launch.h - host-side glue between the C ABI (abi.cu) and the kernels.
+//
+// Each launch_* function queues the kernel(s) of one op on `stream` for
+// arguments that abi.cu has already validated, and returns the CUDA error of
+// the launch.  `vec4` says that every row-major matrix argument is 16-byte
+// aligned with cols % 4 == 0 (and byte masks 4-byte aligned), which enables the
+// 128-bit path.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace rowops {
+
+// ------------------------------------------------------------ bookkeeping
+
+void note_launches(int n);  // counts kernels queued (rowops_kernel_launches)
+
+template <int L, int N, int V>
+struct Geom {
+    static constexpr int LANES = L;
+    static constexpr int NV = N;
+    static constexpr int VEC = V;
+};
+
+// Calls f(Geom<LANES, NV, VEC>{}) with the group geometry for rows of `cols`
+// floats (see common.cuh), or returns false when a row is longer than one
+// warp can hold in registers (1024 floats vectorised, 256 scalar).
+template <typename F>
+bool with_geometry(bool vec4, int64_t cols, F&& f) {
+    if (vec4) {
+        const int64_t nc = cols / 4;
+        if (nc <= 4) f(Geom<4, 1, 4>{});
+        else if (nc <= 8) f(Geom<4, 2, 4>{});
+        else if (nc <= 16) f(Geom<8, 2, 4>{});
+        else if (nc <= 32) f(Geom<16, 2, 4>{});
+        else if (nc <= 64) f(Geom<32, 2, 4>{});
+        else if (nc <= 128) f(Geom<32, 4, 4>{});
+        else if (nc <= 192) f(Geom<32, 6, 4>{});
+        else if (nc <= 256) f(Geom<32, 8, 4>{});
+        else return false;
+    } else {
+        if (cols <= 4) f(Geom<4, 1, 1>{});
+        else if (cols <= 8) f(Geom<8, 1, 1>{});
+        else if (cols <= 16) f(Geom<8, 2, 1>{});
+        else if (cols <= 32) f(Geom<16, 2, 1>{});
+        else if (cols <= 64) f(Geom<32, 2, 1>{});
+        else if (cols <= 128) f(Geom<32, 4, 1>{});
+        else if (cols <= 256) f(Geom<32, 8, 1>{});
+        else return false;
+    }
+    return true;
+}
+
+// Blocks of 256 threads for a group kernel over `rows` rows (grid-stride
+// beyond the cap).
+inline unsigned group_grid(int64_t rows, int lanes) {
+    const int64_t groups_per_block = 256 / lanes;
+    int64_t b = (rows + groups_per_block - 1) / groups_per_block;
+    if (b > (1 << 20)) b = 1 << 20;
+    return static_cast<unsigned>(b < 1 ? 1 : b);
+}
+
+// Blocks for a one-row-per-block (or per-cluster) kernel.
+inline unsigned row_grid(int64_t rows, int per_row = 1) {
+    int64_t b = rows;
+    const int64_t cap = (int64_t(1) << 20);
+    if (b > cap) b = cap;
+    return static_cast<unsigned>((b < 1 ? 1 : b) * per_row);
+}
+
+// ----------------------------------------------------------------- ops
+
+cudaError_t launch_softmax_fwd(const float* x, float* y, int64_t rows, int64_t cols, bool vec4,
+                               cudaStream_t stream);
+cudaError_t launch_softmax_bwd(const float* y, const float* dy, float* dx, int64_t rows,
+                               int64_t cols, bool vec4, cudaStream_t stream);
+cudaError_t launch_attn_fwd(const float* s, float* p, int64_t rows, int64_t cols, int64_t seq_len,
+                            float scale, bool vec4, cudaStream_t stream);
+cudaError_t launch_attn_bwd(const float* p, const float* dp, float* ds, int64_t rows,
+                            int64_t cols, int64_t seq_len, float scale, bool vec4,
+                            cudaStream_t stream);
+cudaError_t launch_masked_softmax(const float* x, const uint8_t* mask, float* y, int64_t rows,
+                                  int64_t cols, bool vec4, cudaStream_t stream);
+cudaError_t launch_logsumexp(const float* x, float* lse, int64_t rows, int64_t cols, bool vec4,
+                             cudaStream_t stream);
+cudaError_t launch_softmax_ce(const float* logits, const int32_t* targets, float* grad,
+                              float* row_loss, double* mean_loss, int64_t rows, int64_t cols,
+                              float grad_scale, bool vec4, cudaStream_t stream);
+cudaError_t launch_layernorm_fwd(const float* x, const float* gamma, const float* beta,
+                                 float* out, float* xhat, float* inv_std, int64_t rows,
+                                 int64_t cols, float eps, bool vec4, cudaStream_t stream);
+size_t layernorm_bwd_workspace(int64_t rows, int64_t cols);
+cudaError_t launch_layernorm_bwd(const float* dy, const float* gamma, const float* xhat,
+                                 const float* inv_std, float* dx, float* dgamma, float* dbeta,
+                                 int64_t rows, int64_t cols, float* workspace, bool vec4,
+                                 cudaStream_t stream);
+cudaError_t launch_topk_kept(const float* x, float* kept, int64_t rows, int64_t cols, int64_t k,
+                             bool vec4, cudaStream_t stream);
+
+}  // namespace rowops

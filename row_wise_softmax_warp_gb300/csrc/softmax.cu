@@ -1,0 +1,560 @@
+// softmax.cu - softmax forward/backward, scaled causal attention softmax
+// forward/backward and hard-masked softmax.
+//
+// Two kernel shapes per op:
+//   *_group    : rows of up to 1024 floats (256 unaligned) held in registers by
+//                a group of LANES lanes (geometry in common.cuh); one HBM read
+//                and one HBM write per element.
+//   *_rowblock : any row length and alignment; one 256-thread block per row,
+//                streaming the row from global memory once per pass.
+#include "common.cuh"
+#include "launch.h"
+
+namespace rowops {
+namespace {
+
+// ------------------------------------------------------------ softmax fwd
+// pulsatrix HIPBackend::softmax_rows: y = exp(x - max) / sum exp(x - max).
+
+template <int LANES, int NV, int VEC>
+__global__ void __launch_bounds__(kBlockThreads)
+softmax_fwd_group(const float* x, float* y, int64_t rows, int cols) {
+    constexpr int GPB = kBlockThreads / LANES;
+    const int g = threadIdx.x % LANES;
+    const int grp = threadIdx.x / LANES;
+    const int nch = cols / VEC;
+    for (int64_t base = int64_t(blockIdx.x) * GPB; base < rows; base += int64_t(gridDim.x) * GPB) {
+        const int64_t row = base + grp;
+        const bool live = row < rows;
+        const int64_t off = (live ? row : 0) * int64_t(cols);
+        float v[NV][VEC];
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c = g + k * LANES;
+            if (live && c < nch) {
+                ld_chunk_coherent<VEC>(x + off + c * VEC, v[k]);  // y may be x
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) v[k][e] = -INFINITY;
+            }
+        }
+        float m = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) m = fmaxf(m, v[k][e]);
+        m = group_max<LANES>(m);
+        float s = 0.f;
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                v[k][e] = expf(v[k][e] - m);
+                s += v[k][e];
+            }
+        s = group_sum<LANES>(s);
+        const float inv = 1.0f / s;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c = g + k * LANES;
+            if (live && c < nch) {
+                float o[VEC];
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) o[e] = v[k][e] * inv;
+                st_chunk<VEC>(y + off + c * VEC, o);
+            }
+        }
+    }
+}
+
+template <int VEC>
+__global__ void __launch_bounds__(kBlockThreads)
+softmax_fwd_rowblock(const float* x, float* y, int64_t rows, int64_t cols) {
+    __shared__ float scratch[2 * kBlockThreads / 32];
+    const int64_t nch = cols / VEC;
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const float* xr = x + row * cols;
+        float* yr = y + row * cols;
+        MaxSum a{-INFINITY, 0.f};
+        for (int64_t c = threadIdx.x; c < nch; c += kBlockThreads) {
+            float v[VEC];
+            ld_chunk_coherent<VEC>(xr + c * VEC, v);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) a = ms_push(a, v[e]);
+        }
+        a = block_maxsum<kBlockThreads>(a, scratch);
+        const float inv = 1.0f / a.s;
+        for (int64_t c = threadIdx.x; c < nch; c += kBlockThreads) {
+            float v[VEC];
+            ld_chunk_coherent<VEC>(xr + c * VEC, v);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) v[e] = expf(v[e] - a.m) * inv;
+            st_chunk<VEC>(yr + c * VEC, v);
+        }
+    }
+}
+
+// ------------------------------------------------------------ softmax bwd
+// pulsatrix HIPBackend::softmax_rows_backward: dx = y * (dy - sum_k y_k dy_k).
+
+template <int LANES, int NV, int VEC>
+__global__ void __launch_bounds__(kBlockThreads)
+softmax_bwd_group(const float* __restrict__ y, const float* __restrict__ dy,
+                  float* __restrict__ dx, int64_t rows, int cols) {
+    constexpr int GPB = kBlockThreads / LANES;
+    const int g = threadIdx.x % LANES;
+    const int grp = threadIdx.x / LANES;
+    const int nch = cols / VEC;
+    for (int64_t base = int64_t(blockIdx.x) * GPB; base < rows; base += int64_t(gridDim.x) * GPB) {
+        const int64_t row = base + grp;
+        const bool live = row < rows;
+        const int64_t off = (live ? row : 0) * int64_t(cols);
+        float a[NV][VEC], b[NV][VEC];
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c = g + k * LANES;
+            if (live && c < nch) {
+                ld_chunk<VEC>(y + off + c * VEC, a[k]);
+                ld_chunk<VEC>(dy + off + c * VEC, b[k]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) a[k][e] = b[k][e] = 0.f;
+            }
+        }
+        float dot = 0.f;
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) dot = fmaf(a[k][e], b[k][e], dot);
+        dot = group_sum<LANES>(dot);
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c = g + k * LANES;
+            if (live && c < nch) {
+                float o[VEC];
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) o[e] = a[k][e] * (b[k][e] - dot);
+                st_chunk<VEC>(dx + off + c * VEC, o);
+            }
+        }
+    }
+}
+
+template <int VEC>
+__global__ void __launch_bounds__(kBlockThreads)
+softmax_bwd_rowblock(const float* __restrict__ y, const float* __restrict__ dy,
+                     float* __restrict__ dx, int64_t rows, int64_t cols) {
+    __shared__ float scratch[kBlockThreads / 32];
+    const int64_t nch = cols / VEC;
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const int64_t off = row * cols;
+        float dot = 0.f;
+        for (int64_t c = threadIdx.x; c < nch; c += kBlockThreads) {
+            float a[VEC], b[VEC];
+            ld_chunk<VEC>(y + off + c * VEC, a);
+            ld_chunk<VEC>(dy + off + c * VEC, b);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) dot = fmaf(a[e], b[e], dot);
+        }
+        dot = block_sum<kBlockThreads>(dot, scratch);
+        for (int64_t c = threadIdx.x; c < nch; c += kBlockThreads) {
+            float a[VEC], b[VEC];
+            ld_chunk<VEC>(y + off + c * VEC, a);
+            ld_chunk<VEC>(dy + off + c * VEC, b);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) a[e] = a[e] * (b[e] - dot);
+            st_chunk<VEC>(dx + off + c * VEC, a);
+        }
+    }
+}
+
+// --------------------------------------------------- causal attention fwd
+// MicroGPT CuBLASBackend::fused_attn_softmax with causal_mask_batched: row r is
+// query q = r mod seq_len; keys j <= q keep scale*s_j, keys j > q get p = +0.
+// Only the visible prefix of each row is read.
+
+template <int LANES, int NV, int VEC>
+__global__ void __launch_bounds__(kBlockThreads)
+attn_fwd_group(const float* __restrict__ s, float* __restrict__ p, int64_t rows, int cols,
+               int64_t seq_len, float scale) {
+    constexpr int GPB = kBlockThreads / LANES;
+    const int g = threadIdx.x % LANES;
+    const int grp = threadIdx.x / LANES;
+    const int nch = cols / VEC;
+    for (int64_t base = int64_t(blockIdx.x) * GPB; base < rows; base += int64_t(gridDim.x) * GPB) {
+        const int64_t row = base + grp;
+        const bool live = row < rows;
+        const int64_t off = (live ? row : 0) * int64_t(cols);
+        const int q = live ? int(row % seq_len) : 0;
+        const int nvis = q + 1 < cols ? q + 1 : cols;  // visible keys 0..q
+        float v[NV][VEC];
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c0 = (g + k * LANES) * VEC;
+            if (live && c0 < nvis) {
+                ld_chunk<VEC>(s + off + c0, v[k]);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) v[k][e] = (c0 + e < nvis) ? scale * v[k][e] : -INFINITY;
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) v[k][e] = -INFINITY;
+            }
+        }
+        float m = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) m = fmaxf(m, v[k][e]);
+        m = group_max<LANES>(m);
+        float sum = 0.f;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c0 = (g + k * LANES) * VEC;
+            if (c0 < nvis) {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    v[k][e] = (c0 + e < nvis) ? expf(v[k][e] - m) : 0.f;
+                    sum += v[k][e];
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) v[k][e] = 0.f;
+            }
+        }
+        sum = group_sum<LANES>(sum);
+        const float inv = 1.0f / sum;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c = g + k * LANES;
+            if (live && c < nch) {
+                float o[VEC];
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) o[e] = v[k][e] * inv;
+                st_chunk<VEC>(p + off + c * VEC, o);
+            }
+        }
+    }
+}
+
+template <int VEC>
+__global__ void __launch_bounds__(kBlockThreads)
+attn_fwd_rowblock(const float* __restrict__ s, float* __restrict__ p, int64_t rows, int64_t cols,
+                  int64_t seq_len, float scale) {
+    __shared__ float scratch[2 * kBlockThreads / 32];
+    const int64_t nch = cols / VEC;
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const int64_t off = row * cols;
+        const int64_t q = row % seq_len;
+        const int64_t nvis = q + 1 < cols ? q + 1 : cols;
+        MaxSum a{-INFINITY, 0.f};
+        for (int64_t c = threadIdx.x; c * VEC < nvis; c += kBlockThreads) {
+            float v[VEC];
+            ld_chunk<VEC>(s + off + c * VEC, v);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e)
+                if (c * VEC + e < nvis) a = ms_push(a, scale * v[e]);
+        }
+        a = block_maxsum<kBlockThreads>(a, scratch);
+        const float inv = 1.0f / a.s;
+        for (int64_t c = threadIdx.x; c < nch; c += kBlockThreads) {
+            float v[VEC];
+            if (c * VEC < nvis) {
+                ld_chunk<VEC>(s + off + c * VEC, v);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e)
+                    v[e] = (c * VEC + e < nvis) ? expf(scale * v[e] - a.m) * inv : 0.f;
+                st_chunk<VEC>(p + off + c * VEC, v);
+            } else {
+                st_zero_chunk<VEC>(p + off + c * VEC);
+            }
+        }
+    }
+}
+
+// --------------------------------------------------- causal attention bwd
+// MicroGPT CuBLASBackend::fused_attn_softmax_backward: from the output p,
+// ds = scale * p * (dp - sum_{k<=q} p_k dp_k) on the visible keys, +0 beyond.
+
+template <int LANES, int NV, int VEC>
+__global__ void __launch_bounds__(kBlockThreads)
+attn_bwd_group(const float* __restrict__ p, const float* __restrict__ dp, float* __restrict__ ds,
+               int64_t rows, int cols, int64_t seq_len, float scale) {
+    constexpr int GPB = kBlockThreads / LANES;
+    const int g = threadIdx.x % LANES;
+    const int grp = threadIdx.x / LANES;
+    const int nch = cols / VEC;
+    for (int64_t base = int64_t(blockIdx.x) * GPB; base < rows; base += int64_t(gridDim.x) * GPB) {
+        const int64_t row = base + grp;
+        const bool live = row < rows;
+        const int64_t off = (live ? row : 0) * int64_t(cols);
+        const int q = live ? int(row % seq_len) : 0;
+        const int nvis = q + 1 < cols ? q + 1 : cols;
+        float a[NV][VEC], b[NV][VEC];
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c0 = (g + k * LANES) * VEC;
+            if (live && c0 < nvis) {
+                ld_chunk<VEC>(p + off + c0, a[k]);
+                ld_chunk<VEC>(dp + off + c0, b[k]);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e)
+                    if (c0 + e >= nvis) a[k][e] = b[k][e] = 0.f;
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) a[k][e] = b[k][e] = 0.f;
+            }
+        }
+        float dot = 0.f;
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) dot = fmaf(a[k][e], b[k][e], dot);
+        dot = group_sum<LANES>(dot);
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c0 = (g + k * LANES) * VEC;
+            if (live && c0 < nch * VEC) {
+                float o[VEC];
+#pragma unroll
+                for (int e = 0; e < VEC; ++e)
+                    o[e] = (c0 + e < nvis) ? scale * a[k][e] * (b[k][e] - dot) : 0.f;
+                st_chunk<VEC>(ds + off + c0, o);
+            }
+        }
+    }
+}
+
+template <int VEC>
+__global__ void __launch_bounds__(kBlockThreads)
+attn_bwd_rowblock(const float* __restrict__ p, const float* __restrict__ dp,
+                  float* __restrict__ ds, int64_t rows, int64_t cols, int64_t seq_len,
+                  float scale) {
+    __shared__ float scratch[kBlockThreads / 32];
+    const int64_t nch = cols / VEC;
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const int64_t off = row * cols;
+        const int64_t q = row % seq_len;
+        const int64_t nvis = q + 1 < cols ? q + 1 : cols;
+        float dot = 0.f;
+        for (int64_t c = threadIdx.x; c * VEC < nvis; c += kBlockThreads) {
+            float a[VEC], b[VEC];
+            ld_chunk<VEC>(p + off + c * VEC, a);
+            ld_chunk<VEC>(dp + off + c * VEC, b);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e)
+                if (c * VEC + e < nvis) dot = fmaf(a[e], b[e], dot);
+        }
+        dot = block_sum<kBlockThreads>(dot, scratch);
+        for (int64_t c = threadIdx.x; c < nch; c += kBlockThreads) {
+            if (c * VEC < nvis) {
+                float a[VEC], b[VEC];
+                ld_chunk<VEC>(p + off + c * VEC, a);
+                ld_chunk<VEC>(dp + off + c * VEC, b);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e)
+                    a[e] = (c * VEC + e < nvis) ? scale * a[e] * (b[e] - dot) : 0.f;
+                st_chunk<VEC>(ds + off + c * VEC, a);
+            } else {
+                st_zero_chunk<VEC>(ds + off + c * VEC);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------ hard-masked softmax
+// TorchLean hard-masked softmax: max and denominator over allowed entries
+// (mask byte != 0); blocked entries +0; a row with nothing allowed is all +0.
+
+template <int LANES, int NV, int VEC>
+__global__ void __launch_bounds__(kBlockThreads)
+masked_group(const float* x, const uint8_t* __restrict__ mask, float* y, int64_t rows, int cols) {
+    constexpr int GPB = kBlockThreads / LANES;
+    const int g = threadIdx.x % LANES;
+    const int grp = threadIdx.x / LANES;
+    const int nch = cols / VEC;
+    for (int64_t base = int64_t(blockIdx.x) * GPB; base < rows; base += int64_t(gridDim.x) * GPB) {
+        const int64_t row = base + grp;
+        const bool live = row < rows;
+        const int64_t off = (live ? row : 0) * int64_t(cols);
+        float v[NV][VEC];
+        bool al[NV][VEC];
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c = g + k * LANES;
+            if (live && c < nch) {
+                ld_chunk_coherent<VEC>(x + off + c * VEC, v[k]);  // y may be x
+                ld_mask<VEC>(mask + off + c * VEC, al[k]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) al[k][e] = false;
+            }
+        }
+        float m = -INFINITY;
+        int n_allowed = 0;
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e)
+                if (al[k][e]) {
+                    m = fmaxf(m, v[k][e]);
+                    ++n_allowed;
+                }
+        m = group_max<LANES>(m);
+        n_allowed = group_sum_int<LANES>(n_allowed);
+        float s = 0.f;
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                v[k][e] = al[k][e] ? expf(v[k][e] - m) : 0.f;
+                s += v[k][e];
+            }
+        s = group_sum<LANES>(s);
+        const float inv = n_allowed > 0 ? 1.0f / s : 0.f;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c = g + k * LANES;
+            if (live && c < nch) {
+                float o[VEC];
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) o[e] = al[k][e] ? v[k][e] * inv : 0.f;
+                st_chunk<VEC>(y + off + c * VEC, o);
+            }
+        }
+    }
+}
+
+template <int VEC>
+__global__ void __launch_bounds__(kBlockThreads)
+masked_rowblock(const float* x, const uint8_t* __restrict__ mask, float* y, int64_t rows,
+                int64_t cols) {
+    __shared__ float scratch[2 * kBlockThreads / 32];
+    __shared__ int iscratch[kBlockThreads / 32];
+    const int64_t nch = cols / VEC;
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const int64_t off = row * cols;
+        MaxSum a{-INFINITY, 0.f};
+        int n_allowed = 0;
+        for (int64_t c = threadIdx.x; c < nch; c += kBlockThreads) {
+            float v[VEC];
+            bool al[VEC];
+            ld_chunk_coherent<VEC>(x + off + c * VEC, v);
+            ld_mask<VEC>(mask + off + c * VEC, al);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e)
+                if (al[e]) {
+                    a = ms_push(a, v[e]);
+                    ++n_allowed;
+                }
+        }
+        a = block_maxsum<kBlockThreads>(a, scratch);
+        n_allowed = block_sum_int<kBlockThreads>(n_allowed, iscratch);
+        const float inv = n_allowed > 0 ? 1.0f / a.s : 0.f;
+        for (int64_t c = threadIdx.x; c < nch; c += kBlockThreads) {
+            float v[VEC];
+            bool al[VEC];
+            ld_chunk_coherent<VEC>(x + off + c * VEC, v);
+            ld_mask<VEC>(mask + off + c * VEC, al);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) v[e] = al[e] ? expf(v[e] - a.m) * inv : 0.f;
+            st_chunk<VEC>(y + off + c * VEC, v);
+        }
+    }
+}
+
+}  // namespace
+
+// ------------------------------------------------------------ launchers
+
+cudaError_t launch_softmax_fwd(const float* x, float* y, int64_t rows, int64_t cols, bool vec4,
+                               cudaStream_t stream) {
+    const bool done = with_geometry(vec4, cols, [&](auto geo) {
+        using G = decltype(geo);
+        softmax_fwd_group<G::LANES, G::NV, G::VEC>
+            <<<group_grid(rows, G::LANES), kBlockThreads, 0, stream>>>(x, y, rows, int(cols));
+    });
+    if (!done) {
+        if (vec4)
+            softmax_fwd_rowblock<4><<<row_grid(rows), kBlockThreads, 0, stream>>>(x, y, rows, cols);
+        else
+            softmax_fwd_rowblock<1><<<row_grid(rows), kBlockThreads, 0, stream>>>(x, y, rows, cols);
+    }
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_softmax_bwd(const float* y, const float* dy, float* dx, int64_t rows,
+                               int64_t cols, bool vec4, cudaStream_t stream) {
+    const bool done = with_geometry(vec4, cols, [&](auto geo) {
+        using G = decltype(geo);
+        softmax_bwd_group<G::LANES, G::NV, G::VEC>
+            <<<group_grid(rows, G::LANES), kBlockThreads, 0, stream>>>(y, dy, dx, rows, int(cols));
+    });
+    if (!done) {
+        if (vec4)
+            softmax_bwd_rowblock<4><<<row_grid(rows), kBlockThreads, 0, stream>>>(y, dy, dx, rows, cols);
+        else
+            softmax_bwd_rowblock<1><<<row_grid(rows), kBlockThreads, 0, stream>>>(y, dy, dx, rows, cols);
+    }
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_attn_fwd(const float* s, float* p, int64_t rows, int64_t cols, int64_t seq_len,
+                            float scale, bool vec4, cudaStream_t stream) {
+    const bool done = with_geometry(vec4, cols, [&](auto geo) {
+        using G = decltype(geo);
+        attn_fwd_group<G::LANES, G::NV, G::VEC><<<group_grid(rows, G::LANES), kBlockThreads, 0,
+                                                  stream>>>(s, p, rows, int(cols), seq_len, scale);
+    });
+    if (!done) {
+        if (vec4)
+            attn_fwd_rowblock<4><<<row_grid(rows), kBlockThreads, 0, stream>>>(s, p, rows, cols,
+                                                                               seq_len, scale);
+        else
+            attn_fwd_rowblock<1><<<row_grid(rows), kBlockThreads, 0, stream>>>(s, p, rows, cols,
+                                                                               seq_len, scale);
+    }
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_attn_bwd(const float* p, const float* dp, float* ds, int64_t rows,
+                            int64_t cols, int64_t seq_len, float scale, bool vec4,
+                            cudaStream_t stream) {
+    const bool done = with_geometry(vec4, cols, [&](auto geo) {
+        using G = decltype(geo);
+        attn_bwd_group<G::LANES, G::NV, G::VEC><<<group_grid(rows, G::LANES), kBlockThreads, 0,
+                                                  stream>>>(p, dp, ds, rows, int(cols), seq_len,
+                                                            scale);
+    });
+    if (!done) {
+        if (vec4)
+            attn_bwd_rowblock<4><<<row_grid(rows), kBlockThreads, 0, stream>>>(p, dp, ds, rows, cols,
+                                                                               seq_len, scale);
+        else
+            attn_bwd_rowblock<1><<<row_grid(rows), kBlockThreads, 0, stream>>>(p, dp, ds, rows, cols,
+                                                                               seq_len, scale);
+    }
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_masked_softmax(const float* x, const uint8_t* mask, float* y, int64_t rows,
+                                  int64_t cols, bool vec4, cudaStream_t stream) {
+    const bool done = with_geometry(vec4, cols, [&](auto geo) {
+        using G = decltype(geo);
+        masked_group<G::LANES, G::NV, G::VEC>
+            <<<group_grid(rows, G::LANES), kBlockThreads, 0, stream>>>(x, mask, y, rows, int(cols));
+    });
+    if (!done) {
+        if (vec4)
+            masked_rowblock<4><<<row_grid(rows), kBlockThreads, 0, stream>>>(x, mask, y, rows, cols);
+        else
+            masked_rowblock<1><<<row_grid(rows), kBlockThreads, 0, stream>>>(x, mask, y, rows, cols);
+    }
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace rowops
