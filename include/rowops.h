@@ -15,8 +15,9 @@
  *   - Return value: ROWOPS_OK, or the first error found.  Nothing is launched
  *     when an error is returned, except ROWOPS_ERR_CUDA, which reports a failed
  *     launch (the CUDA runtime's error after the launch).
- *   - rows == 0 is a successful no-op for every op.  Negative sizes, and
- *     rows * cols that does not fit in int64, are ROWOPS_ERR_SHAPE.
+ *   - rows == 0 is a successful no-op for every op (after the scalar
+ *     parameters are checked).  Negative sizes, cols >= 2^31, and matrices of
+ *     more than 2^60 elements are ROWOPS_ERR_SHAPE.
  *   - A pointer may be NULL only when the buffer it names is empty.
  *   - Buffers must not overlap unless the entry point says so
  *     (ROWOPS_ERR_ALIAS); overlap is checked by address range.

@@ -1,0 +1,223 @@
+// abi.cu - the extern "C" entry points of librowops (include/rowops.h).
+//
+// Each entry point validates its arguments on the host in a fixed order
+// (sizes, scalar parameters, empty problem, NULL pointers, overlap), decides
+// whether the 128-bit path applies, and hands over to the op's launcher.  No
+// exception crosses this boundary and nothing here allocates or synchronises.
+#include <atomic>
+#include <climits>
+#include <cmath>
+#include <cstdint>
+
+#include "../../include/rowops.h"
+#include "launch.h"
+
+namespace rowops {
+
+static std::atomic<uint64_t> g_launches{0};
+
+void note_launches(int n) { g_launches.fetch_add(uint64_t(n), std::memory_order_relaxed); }
+
+}  // namespace rowops
+
+namespace {
+
+using rowops::launch_attn_bwd;
+
+struct Buf {
+    const void* p;
+    int64_t bytes;
+};
+
+bool overlap(Buf a, Buf b) {
+    if (a.p == nullptr || b.p == nullptr || a.bytes <= 0 || b.bytes <= 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+    return a0 < b0 + uint64_t(b.bytes) && b0 < a0 + uint64_t(a.bytes);
+}
+
+bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) & (n - 1)) == 0; }
+
+// rows, cols >= 0; cols < 2^31; rows*cols*8 bytes fits in int64.
+int check_dims(int64_t rows, int64_t cols) {
+    if (rows < 0 || cols < 0 || cols > INT32_MAX) return ROWOPS_ERR_SHAPE;
+    if (cols > 0 && rows > (INT64_MAX / 8) / cols) return ROWOPS_ERR_SHAPE;
+    return ROWOPS_OK;
+}
+
+int to_status(cudaError_t e) { return e == cudaSuccess ? ROWOPS_OK : ROWOPS_ERR_CUDA; }
+
+cudaStream_t st(rowops_stream s) { return reinterpret_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+extern "C" {
+
+const char* rowops_status_string(int status) {
+    switch (status) {
+        case ROWOPS_OK: return "ROWOPS_OK";
+        case ROWOPS_ERR_NULL: return "ROWOPS_ERR_NULL: a required pointer is NULL";
+        case ROWOPS_ERR_SHAPE: return "ROWOPS_ERR_SHAPE: invalid size or scalar parameter";
+        case ROWOPS_ERR_ALIAS: return "ROWOPS_ERR_ALIAS: buffers overlap where the op forbids it";
+        case ROWOPS_ERR_WORKSPACE: return "ROWOPS_ERR_WORKSPACE: workspace missing, misaligned or too small";
+        case ROWOPS_ERR_CUDA: return "ROWOPS_ERR_CUDA: the CUDA runtime reported a launch error";
+        default: return "ROWOPS: unknown status";
+    }
+}
+
+uint64_t rowops_kernel_launches(void) { return rowops::g_launches.load(std::memory_order_relaxed); }
+
+int rowops_softmax_fwd(const float* x, float* y, int64_t rows, int64_t cols, rowops_stream stream) {
+    if (int e = check_dims(rows, cols)) return e;
+    if (rows == 0 || cols == 0) return ROWOPS_OK;
+    if (!x || !y) return ROWOPS_ERR_NULL;
+    const int64_t n = rows * cols * 4;
+    if (static_cast<const void*>(x) != y && overlap({x, n}, {y, n})) return ROWOPS_ERR_ALIAS;
+    const bool vec4 = cols % 4 == 0 && aligned(x, 16) && aligned(y, 16);
+    return to_status(rowops::launch_softmax_fwd(x, y, rows, cols, vec4, st(stream)));
+}
+
+int rowops_softmax_bwd(const float* y, const float* dy, float* dx, int64_t rows, int64_t cols,
+                       rowops_stream stream) {
+    if (int e = check_dims(rows, cols)) return e;
+    if (rows == 0 || cols == 0) return ROWOPS_OK;
+    if (!y || !dy || !dx) return ROWOPS_ERR_NULL;
+    const int64_t n = rows * cols * 4;
+    if (overlap({dx, n}, {y, n}) || overlap({dx, n}, {dy, n})) return ROWOPS_ERR_ALIAS;
+    const bool vec4 = cols % 4 == 0 && aligned(y, 16) && aligned(dy, 16) && aligned(dx, 16);
+    return to_status(rowops::launch_softmax_bwd(y, dy, dx, rows, cols, vec4, st(stream)));
+}
+
+static int check_attn(int64_t rows, int64_t cols, int64_t seq_len, float scale) {
+    if (int e = check_dims(rows, cols)) return e;
+    if (seq_len < 1 || cols != seq_len || rows % seq_len != 0) return ROWOPS_ERR_SHAPE;
+    if (!(scale > 0.f) || !std::isfinite(scale)) return ROWOPS_ERR_SHAPE;
+    return ROWOPS_OK;
+}
+
+int rowops_attn_softmax_fwd(const float* scores, float* p, int64_t rows, int64_t cols,
+                            int64_t seq_len, float scale, rowops_stream stream) {
+    if (int e = check_attn(rows, cols, seq_len, scale)) return e;
+    if (rows == 0) return ROWOPS_OK;
+    if (!scores || !p) return ROWOPS_ERR_NULL;
+    const int64_t n = rows * cols * 4;
+    if (overlap({scores, n}, {p, n})) return ROWOPS_ERR_ALIAS;
+    const bool vec4 = cols % 4 == 0 && aligned(scores, 16) && aligned(p, 16);
+    return to_status(rowops::launch_attn_fwd(scores, p, rows, cols, seq_len, scale, vec4, st(stream)));
+}
+
+int rowops_attn_softmax_bwd(const float* p, const float* dp, float* ds, int64_t rows, int64_t cols,
+                            int64_t seq_len, float scale, rowops_stream stream) {
+    if (int e = check_attn(rows, cols, seq_len, scale)) return e;
+    if (rows == 0) return ROWOPS_OK;
+    if (!p || !dp || !ds) return ROWOPS_ERR_NULL;
+    const int64_t n = rows * cols * 4;
+    if (overlap({ds, n}, {p, n}) || overlap({ds, n}, {dp, n})) return ROWOPS_ERR_ALIAS;
+    const bool vec4 = cols % 4 == 0 && aligned(p, 16) && aligned(dp, 16) && aligned(ds, 16);
+    return to_status(launch_attn_bwd(p, dp, ds, rows, cols, seq_len, scale, vec4, st(stream)));
+}
+
+int rowops_masked_softmax(const float* x, const uint8_t* mask, float* y, int64_t rows, int64_t cols,
+                          rowops_stream stream) {
+    if (int e = check_dims(rows, cols)) return e;
+    if (rows == 0 || cols == 0) return ROWOPS_OK;
+    if (!x || !mask || !y) return ROWOPS_ERR_NULL;
+    const int64_t n = rows * cols * 4;
+    if (static_cast<const void*>(x) != y && overlap({x, n}, {y, n})) return ROWOPS_ERR_ALIAS;
+    if (overlap({mask, rows * cols}, {y, n}) || overlap({mask, rows * cols}, {x, n}))
+        return ROWOPS_ERR_ALIAS;
+    const bool vec4 = cols % 4 == 0 && aligned(x, 16) && aligned(y, 16) && aligned(mask, 4);
+    return to_status(rowops::launch_masked_softmax(x, mask, y, rows, cols, vec4, st(stream)));
+}
+
+int rowops_logsumexp(const float* x, float* lse, int64_t rows, int64_t cols, rowops_stream stream) {
+    if (int e = check_dims(rows, cols)) return e;
+    if (rows == 0) return ROWOPS_OK;
+    if (!lse || (cols > 0 && !x)) return ROWOPS_ERR_NULL;
+    if (overlap({x, rows * cols * 4}, {lse, rows * 4})) return ROWOPS_ERR_ALIAS;
+    const bool vec4 = cols % 4 == 0 && aligned(x, 16);
+    return to_status(rowops::launch_logsumexp(x, lse, rows, cols, vec4, st(stream)));
+}
+
+int rowops_softmax_ce(const float* logits, const int32_t* targets, float* grad, float* row_loss,
+                      double* mean_loss, int64_t rows, int64_t cols, float grad_scale,
+                      rowops_stream stream) {
+    if (int e = check_dims(rows, cols)) return e;
+    if (cols == 0 || !std::isfinite(grad_scale)) return ROWOPS_ERR_SHAPE;
+    if (rows == 0) return ROWOPS_OK;
+    if (!logits || !targets || !grad || !row_loss || !mean_loss) return ROWOPS_ERR_NULL;
+    const int64_t n = rows * cols * 4;
+    const Buf in[2] = {{logits, n}, {targets, rows * 4}};
+    const Buf out[3] = {{grad, n}, {row_loss, rows * 4}, {mean_loss, 8}};
+    for (const Buf& o : out) {
+        for (const Buf& i : in)
+            if (overlap(o, i)) return ROWOPS_ERR_ALIAS;
+        for (const Buf& o2 : out)
+            if (&o != &o2 && overlap(o, o2)) return ROWOPS_ERR_ALIAS;
+    }
+    const bool vec4 = cols % 4 == 0 && aligned(logits, 16) && aligned(grad, 16);
+    return to_status(rowops::launch_softmax_ce(logits, targets, grad, row_loss, mean_loss, rows, cols,
+                                               grad_scale, vec4, st(stream)));
+}
+
+int rowops_layernorm_fwd(const float* x, const float* gamma, const float* beta, float* out,
+                         float* xhat, float* inv_std, int64_t rows, int64_t cols, float eps,
+                         rowops_stream stream) {
+    if (int e = check_dims(rows, cols)) return e;
+    if (cols == 0 || !std::isfinite(eps) || eps < 0.f) return ROWOPS_ERR_SHAPE;
+    if (rows == 0) return ROWOPS_OK;
+    if (!x || !gamma || !beta || !out || !xhat || !inv_std) return ROWOPS_ERR_NULL;
+    const int64_t n = rows * cols * 4;
+    const Buf in[3] = {{x, n}, {gamma, cols * 4}, {beta, cols * 4}};
+    const Buf o[3] = {{out, n}, {xhat, n}, {inv_std, rows * 4}};
+    for (int a = 0; a < 3; ++a) {
+        for (int b = 0; b < 3; ++b)
+            if (overlap(o[a], in[b]) || (a != b && overlap(o[a], o[b]))) return ROWOPS_ERR_ALIAS;
+    }
+    const bool vec4 = cols % 4 == 0 && aligned(x, 16) && aligned(gamma, 16) && aligned(beta, 16) &&
+                      aligned(out, 16) && aligned(xhat, 16);
+    return to_status(rowops::launch_layernorm_fwd(x, gamma, beta, out, xhat, inv_std, rows, cols, eps,
+                                                  vec4, st(stream)));
+}
+
+size_t rowops_layernorm_bwd_workspace(int64_t rows, int64_t cols) {
+    if (check_dims(rows, cols) != ROWOPS_OK) return 0;
+    return rowops::layernorm_bwd_workspace(rows, cols);
+}
+
+int rowops_layernorm_bwd(const float* dy, const float* gamma, const float* xhat,
+                         const float* inv_std, float* dx, float* dgamma, float* dbeta,
+                         int64_t rows, int64_t cols, void* workspace, size_t workspace_bytes,
+                         rowops_stream stream) {
+    if (int e = check_dims(rows, cols)) return e;
+    if (cols == 0) return ROWOPS_ERR_SHAPE;
+    if (rows == 0) return ROWOPS_OK;
+    if (!dy || !gamma || !xhat || !inv_std || !dx || !dgamma || !dbeta) return ROWOPS_ERR_NULL;
+    const size_t need = rowops::layernorm_bwd_workspace(rows, cols);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return ROWOPS_ERR_WORKSPACE;
+    const int64_t n = rows * cols * 4;
+    const Buf in[4] = {{dy, n}, {gamma, cols * 4}, {xhat, n}, {inv_std, rows * 4}};
+    const Buf o[4] = {{dx, n}, {dgamma, cols * 4}, {dbeta, cols * 4}, {workspace, int64_t(need)}};
+    for (int a = 0; a < 4; ++a) {
+        for (int b = 0; b < 4; ++b)
+            if (overlap(o[a], in[b]) || (a != b && overlap(o[a], o[b]))) return ROWOPS_ERR_ALIAS;
+    }
+    const bool vec4 = cols % 4 == 0 && aligned(dy, 16) && aligned(gamma, 16) && aligned(xhat, 16) &&
+                      aligned(dx, 16);
+    return to_status(rowops::launch_layernorm_bwd(dy, gamma, xhat, inv_std, dx, dgamma, dbeta, rows,
+                                                  cols, static_cast<float*>(workspace), vec4,
+                                                  st(stream)));
+}
+
+int rowops_topk_kept(const float* x, float* kept, int64_t rows, int64_t cols, int64_t k,
+                     rowops_stream stream) {
+    if (int e = check_dims(rows, cols)) return e;
+    if (k < 1 || k > cols) return ROWOPS_ERR_SHAPE;
+    if (rows == 0) return ROWOPS_OK;
+    if (!x || !kept) return ROWOPS_ERR_NULL;
+    const int64_t n = rows * cols * 4;
+    if (overlap({x, n}, {kept, n})) return ROWOPS_ERR_ALIAS;
+    const bool vec4 = cols % 4 == 0 && aligned(x, 16) && aligned(kept, 16);
+    return to_status(rowops::launch_topk_kept(x, kept, rows, cols, k, vec4, st(stream)));
+}
+
+}  // extern "C"

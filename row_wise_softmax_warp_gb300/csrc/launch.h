@@ -75,6 +75,10 @@ inline unsigned row_grid(int64_t rows, int per_row = 1) {
 
 cudaError_t launch_softmax_fwd(const float* x, float* y, int64_t rows, int64_t cols, bool vec4,
                                cudaStream_t stream);
+// Vectorised rows too long for one warp: the cluster kernel of lse_ce.cu.
+// Returns false (nothing launched) when the row exceeds its capacity.
+bool launch_softmax_fwd_long(const float* x, float* y, int64_t rows, int64_t cols,
+                             cudaStream_t stream, cudaError_t* err);
 cudaError_t launch_softmax_bwd(const float* y, const float* dy, float* dx, int64_t rows,
                                int64_t cols, bool vec4, cudaStream_t stream);
 cudaError_t launch_attn_fwd(const float* s, float* p, int64_t rows, int64_t cols, int64_t seq_len,

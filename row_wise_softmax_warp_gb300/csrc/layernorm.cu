@@ -1,0 +1,436 @@
+// layernorm.cu - LayerNorm forward (out, xhat, inv_std) and backward
+// (dx, dgamma, dbeta) over the columns of a row-major matrix.
+//
+// Forward statistics are a two-pass mean/variance of the register-held row.
+// The mean is accumulated around a shift (the row's first entry), so rows whose
+// mean is large next to their spread (mean 5, std 0.1) keep full fp32 accuracy.
+//
+// Backward writes dx per row and the column sums dgamma_j = sum_i dy*xhat,
+// dbeta_j = sum_i dy in two deterministic stages:
+//   stage 1 (ln_bwd_group, clusters of 8 CTAs): each CTA owns a fixed block of
+//     rows; groups accumulate their columns in registers, CTAs add their warps
+//     in warp order through shared memory, and the 8 CTAs of a cluster add their
+//     partials in rank order through distributed shared memory, writing one
+//     partial per cluster to the workspace;
+//   stage 2 (ln_params_reduce): one thread per output column adds the
+//     cluster partials in increasing order.
+#include "common.cuh"
+#include "launch.h"
+
+namespace rowops {
+namespace {
+
+constexpr int kLnClusterCtas = 8;
+
+// -------------------------------------------------------------- forward
+// pulsatrix HIPBackend::layer_norm_forward / TorchLean layer normalisation.
+
+template <int LANES, int NV, int VEC>
+__global__ void __launch_bounds__(kBlockThreads)
+ln_fwd_group(const float* __restrict__ x, const float* __restrict__ gamma,
+             const float* __restrict__ beta, float* __restrict__ out, float* __restrict__ xhat,
+             float* __restrict__ inv_std, int64_t rows, int cols, float eps) {
+    constexpr int GPB = kBlockThreads / LANES;
+    const int g = threadIdx.x % LANES;
+    const int grp = threadIdx.x / LANES;
+    const int lane = threadIdx.x & 31;
+    const int leader = lane - g;  // lane of this group's first lane
+    const int nch = cols / VEC;
+    const float inv_cols = 1.0f / float(cols);
+    for (int64_t base = int64_t(blockIdx.x) * GPB; base < rows; base += int64_t(gridDim.x) * GPB) {
+        const int64_t row = base + grp;
+        const bool live = row < rows;
+        const int64_t off = (live ? row : 0) * int64_t(cols);
+        float v[NV][VEC];
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c = g + k * LANES;
+            if (live && c < nch) {
+                ld_chunk<VEC>(x + off + c * VEC, v[k]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) v[k][e] = 0.f;
+            }
+        }
+        const float shift = __shfl_sync(kFullMask, v[0][0], leader);  // the row's first entry
+        float s = 0.f;
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+            if (g + k * LANES < nch)
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) s += v[k][e] - shift;
+        s = group_sum<LANES>(s);
+        const float mean = shift + s * inv_cols;
+        float q = 0.f;
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+            if (g + k * LANES < nch)
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    v[k][e] -= mean;
+                    q = fmaf(v[k][e], v[k][e], q);
+                }
+        q = group_sum<LANES>(q);
+        const float r = 1.0f / sqrtf(q * inv_cols + eps);
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c = g + k * LANES;
+            if (live && c < nch) {
+                float gm[VEC], bt[VEC], h[VEC], o[VEC];
+                ld_chunk<VEC>(gamma + c * VEC, gm);
+                ld_chunk<VEC>(beta + c * VEC, bt);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    h[e] = v[k][e] * r;
+                    o[e] = fmaf(gm[e], h[e], bt[e]);
+                }
+                st_chunk<VEC>(xhat + off + c * VEC, h);
+                st_chunk<VEC>(out + off + c * VEC, o);
+            }
+        }
+        if (live && g == 0) inv_std[row] = r;
+    }
+}
+
+template <int VEC>
+__global__ void __launch_bounds__(kBlockThreads)
+ln_fwd_rowblock(const float* __restrict__ x, const float* __restrict__ gamma,
+                const float* __restrict__ beta, float* __restrict__ out, float* __restrict__ xhat,
+                float* __restrict__ inv_std, int64_t rows, int64_t cols, float eps) {
+    __shared__ float scratch[kBlockThreads / 32];
+    const int64_t nch = cols / VEC;
+    const float inv_cols = 1.0f / float(cols);
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const float* xr = x + row * cols;
+        const float shift = __ldg(xr);
+        float s = 0.f;
+        for (int64_t c = threadIdx.x; c < nch; c += kBlockThreads) {
+            float v[VEC];
+            ld_chunk<VEC>(xr + c * VEC, v);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) s += v[e] - shift;
+        }
+        const float mean = shift + block_sum<kBlockThreads>(s, scratch) * inv_cols;
+        float q = 0.f;
+        for (int64_t c = threadIdx.x; c < nch; c += kBlockThreads) {
+            float v[VEC];
+            ld_chunk<VEC>(xr + c * VEC, v);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                const float d = v[e] - mean;
+                q = fmaf(d, d, q);
+            }
+        }
+        const float r = 1.0f / sqrtf(block_sum<kBlockThreads>(q, scratch) * inv_cols + eps);
+        for (int64_t c = threadIdx.x; c < nch; c += kBlockThreads) {
+            float v[VEC], gm[VEC], bt[VEC], o[VEC];
+            ld_chunk<VEC>(xr + c * VEC, v);
+            ld_chunk<VEC>(gamma + c * VEC, gm);
+            ld_chunk<VEC>(beta + c * VEC, bt);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                v[e] = (v[e] - mean) * r;
+                o[e] = fmaf(gm[e], v[e], bt[e]);
+            }
+            st_chunk<VEC>(xhat + row * cols + c * VEC, v);
+            st_chunk<VEC>(out + row * cols + c * VEC, o);
+        }
+        if (threadIdx.x == 0) inv_std[row] = r;
+    }
+}
+
+// ------------------------------------------------------------- backward
+// TorchLean layer-normalisation VJP / MicroGPT layer_norm_backward:
+//   g' = dy*gamma, dx = r*(g' - mean(g') - xhat*mean(g'*xhat)),
+//   dgamma_j = sum_i dy*xhat, dbeta_j = sum_i dy.
+
+// Geometry of the stage-1 grid: a pure function of rows.
+inline int64_t ln_bwd_ctas(int64_t rows) {
+    int64_t b = (rows + 7) / 8;
+    if (b > 1024) b = 1024;
+    if (b < 1) b = 1;
+    return (b + kLnClusterCtas - 1) / kLnClusterCtas * kLnClusterCtas;
+}
+inline int64_t ln_bwd_partials(int64_t rows) { return ln_bwd_ctas(rows) / kLnClusterCtas; }
+
+__device__ __forceinline__ void cl_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void cl_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+
+// Dynamic shared memory: red[8 warps][2][MAXC] then bpart[2][MAXC], MAXC = the
+// geometry's largest row.
+template <int LANES, int NV, int VEC>
+__global__ void __launch_bounds__(kBlockThreads)
+ln_bwd_group(const float* __restrict__ dy, const float* __restrict__ gamma,
+             const float* __restrict__ xhat, const float* __restrict__ inv_std,
+             float* __restrict__ dx, float* __restrict__ ws, int64_t rows, int cols,
+             int64_t rows_per_cta) {
+    namespace cg = cooperative_groups;
+    constexpr int MAXC = LANES * NV * VEC;
+    constexpr int GPB = kBlockThreads / LANES;
+    extern __shared__ float smem[];
+    float* red = smem;                      // [8][2][MAXC]
+    float* bpart = smem + 8 * 2 * MAXC;     // [2][MAXC]
+    const int g = threadIdx.x % LANES;
+    const int grp = threadIdx.x / LANES;
+    const int warp = threadIdx.x >> 5;
+    const int nch = cols / VEC;
+    const float inv_cols = 1.0f / float(cols);
+    const int64_t r_begin = int64_t(blockIdx.x) * rows_per_cta;
+    int64_t r_end = r_begin + rows_per_cta;
+    if (r_end > rows) r_end = rows;
+
+    float pg[NV][VEC], pb[NV][VEC];  // this group's column partials (dgamma, dbeta)
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) pg[k][e] = pb[k][e] = 0.f;
+
+    for (int64_t base = r_begin; base < r_end; base += GPB) {  // block-uniform
+        const int64_t row = base + grp;
+        const bool live = row < r_end;
+        const int64_t off = (live ? row : 0) * int64_t(cols);
+        float a[NV][VEC], h[NV][VEC];
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c = g + k * LANES;
+            if (live && c < nch) {
+                ld_chunk<VEC>(dy + off + c * VEC, a[k]);
+                ld_chunk<VEC>(xhat + off + c * VEC, h[k]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) a[k][e] = h[k][e] = 0.f;
+            }
+        }
+        const float r = live ? __ldg(inv_std + row) : 0.f;
+        float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c = g + k * LANES;
+            if (c < nch) {
+                float gm[VEC];
+                ld_chunk<VEC>(gamma + c * VEC, gm);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    pg[k][e] = fmaf(a[k][e], h[k][e], pg[k][e]);
+                    pb[k][e] += a[k][e];
+                    a[k][e] *= gm[e];  // g' = dy * gamma
+                    s1 += a[k][e];
+                    s2 = fmaf(a[k][e], h[k][e], s2);
+                }
+            }
+        }
+        s1 = group_sum<LANES>(s1) * inv_cols;
+        s2 = group_sum<LANES>(s2) * inv_cols;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c = g + k * LANES;
+            if (live && c < nch) {
+                float o[VEC];
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) o[e] = r * (a[k][e] - s1 - h[k][e] * s2);
+                st_chunk<VEC>(dx + off + c * VEC, o);
+            }
+        }
+    }
+
+    // Groups of a warp -> warp partial (identical in every group of the warp).
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+            pg[k][e] = across_groups_sum<LANES>(pg[k][e]);
+            pb[k][e] = across_groups_sum<LANES>(pb[k][e]);
+        }
+    if ((threadIdx.x & 31) < LANES) {
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                const int col = (g + k * LANES) * VEC + e;
+                red[(warp * 2 + 0) * MAXC + col] = pg[k][e];
+                red[(warp * 2 + 1) * MAXC + col] = pb[k][e];
+            }
+    }
+    __syncthreads();
+    // Warps -> CTA partial, warp order.
+    for (int i = threadIdx.x; i < 2 * MAXC; i += kBlockThreads) {
+        float t = red[i];
+#pragma unroll
+        for (int w = 1; w < 8; ++w) t += red[w * 2 * MAXC + i];
+        bpart[i] = t;
+    }
+    // CTAs of the cluster -> cluster partial, rank order.  Rank q adds the
+    // entries q*256 + tid (+ 8*256 ...) of all 8 CTAs.
+    cg::cluster_group cluster = cg::this_cluster();
+    cl_arrive();
+    cl_wait();
+    const int rank = int(cluster.block_rank());
+    const int64_t cl_id = blockIdx.x / kLnClusterCtas;
+    for (int i = rank * kBlockThreads + threadIdx.x; i < 2 * cols;
+         i += kLnClusterCtas * kBlockThreads) {
+        const int half = i >= cols ? 1 : 0;
+        const int col = i - half * cols;
+        float t = 0.f;
+#pragma unroll
+        for (int q = 0; q < kLnClusterCtas; ++q)
+            t += cluster.map_shared_rank(bpart, q)[half * MAXC + col];
+        ws[cl_id * 2 * int64_t(cols) + i] = t;
+    }
+    cl_arrive();
+    cl_wait();  // peers are done with this CTA's bpart
+}
+
+// Any length and alignment: one block per fixed row range accumulates its
+// columns straight into its workspace slot (each column owned by one thread).
+template <int VEC>
+__global__ void __launch_bounds__(kBlockThreads)
+ln_bwd_rowblock(const float* __restrict__ dy, const float* __restrict__ gamma,
+                const float* __restrict__ xhat, const float* __restrict__ inv_std,
+                float* __restrict__ dx, float* __restrict__ ws, int64_t rows, int64_t cols,
+                int64_t rows_per_cta) {
+    __shared__ float scratch[kBlockThreads / 32];
+    const int64_t nch = cols / VEC;
+    const float inv_cols = 1.0f / float(cols);
+    float* wg = ws + int64_t(blockIdx.x) * 2 * cols;
+    float* wb = wg + cols;
+    for (int64_t c = threadIdx.x; c < nch; c += kBlockThreads) {
+        const float z[VEC] = {};
+        st_chunk<VEC>(wg + c * VEC, z);
+        st_chunk<VEC>(wb + c * VEC, z);
+    }
+    const int64_t r_begin = int64_t(blockIdx.x) * rows_per_cta;
+    int64_t r_end = r_begin + rows_per_cta;
+    if (r_end > rows) r_end = rows;
+    for (int64_t row = r_begin; row < r_end; ++row) {
+        const int64_t off = row * cols;
+        float s1 = 0.f, s2 = 0.f;
+        for (int64_t c = threadIdx.x; c < nch; c += kBlockThreads) {
+            float a[VEC], h[VEC], gm[VEC];
+            ld_chunk<VEC>(dy + off + c * VEC, a);
+            ld_chunk<VEC>(xhat + off + c * VEC, h);
+            ld_chunk<VEC>(gamma + c * VEC, gm);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                const float gp = a[e] * gm[e];
+                s1 += gp;
+                s2 = fmaf(gp, h[e], s2);
+            }
+        }
+        s1 = block_sum<kBlockThreads>(s1, scratch) * inv_cols;
+        s2 = block_sum<kBlockThreads>(s2, scratch) * inv_cols;
+        const float r = __ldg(inv_std + row);
+        for (int64_t c = threadIdx.x; c < nch; c += kBlockThreads) {
+            float a[VEC], h[VEC], gm[VEC], o[VEC], pg[VEC], pb[VEC];
+            ld_chunk<VEC>(dy + off + c * VEC, a);
+            ld_chunk<VEC>(xhat + off + c * VEC, h);
+            ld_chunk<VEC>(gamma + c * VEC, gm);
+            ld_chunk_coherent<VEC>(wg + c * VEC, pg);
+            ld_chunk_coherent<VEC>(wb + c * VEC, pb);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                o[e] = r * (a[e] * gm[e] - s1 - h[e] * s2);
+                pg[e] = fmaf(a[e], h[e], pg[e]);
+                pb[e] += a[e];
+            }
+            st_chunk<VEC>(dx + off + c * VEC, o);
+            st_chunk<VEC>(wg + c * VEC, pg);
+            st_chunk<VEC>(wb + c * VEC, pb);
+        }
+    }
+}
+
+// Stage 2: out[i] = sum_p ws[p][i] for i in [0, 2*cols), p increasing.
+__global__ void __launch_bounds__(kBlockThreads)
+ln_params_reduce(const float* __restrict__ ws, int64_t partials, int64_t cols,
+                 float* __restrict__ dgamma, float* __restrict__ dbeta) {
+    const int64_t i = int64_t(blockIdx.x) * kBlockThreads + threadIdx.x;
+    if (i >= 2 * cols) return;
+    float t = 0.f;
+    for (int64_t p = 0; p < partials; ++p) t += ws[p * 2 * cols + i];
+    if (i < cols)
+        dgamma[i] = t;
+    else
+        dbeta[i - cols] = t;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------ launchers
+
+cudaError_t launch_layernorm_fwd(const float* x, const float* gamma, const float* beta,
+                                 float* out, float* xhat, float* inv_std, int64_t rows,
+                                 int64_t cols, float eps, bool vec4, cudaStream_t stream) {
+    const bool done = with_geometry(vec4, cols, [&](auto geo) {
+        using G = decltype(geo);
+        ln_fwd_group<G::LANES, G::NV, G::VEC><<<group_grid(rows, G::LANES), kBlockThreads, 0, stream>>>(
+            x, gamma, beta, out, xhat, inv_std, rows, int(cols), eps);
+    });
+    if (!done) {
+        if (vec4)
+            ln_fwd_rowblock<4><<<row_grid(rows), kBlockThreads, 0, stream>>>(x, gamma, beta, out, xhat,
+                                                                             inv_std, rows, cols, eps);
+        else
+            ln_fwd_rowblock<1><<<row_grid(rows), kBlockThreads, 0, stream>>>(x, gamma, beta, out, xhat,
+                                                                             inv_std, rows, cols, eps);
+    }
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+size_t layernorm_bwd_workspace(int64_t rows, int64_t cols) {
+    if (rows <= 0 || cols <= 0) return 0;
+    return size_t(ln_bwd_partials(rows)) * 2 * size_t(cols) * sizeof(float);
+}
+
+cudaError_t launch_layernorm_bwd(const float* dy, const float* gamma, const float* xhat,
+                                 const float* inv_std, float* dx, float* dgamma, float* dbeta,
+                                 int64_t rows, int64_t cols, float* ws, bool vec4,
+                                 cudaStream_t stream) {
+    const int64_t partials = ln_bwd_partials(rows);
+    cudaError_t err = cudaSuccess;
+    const bool done = with_geometry(vec4, cols, [&](auto geo) {
+        using G = decltype(geo);
+        constexpr int MAXC = G::LANES * G::NV * G::VEC;
+        const size_t smem = size_t(9) * 2 * MAXC * sizeof(float);
+        auto kern = ln_bwd_group<G::LANES, G::NV, G::VEC>;
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (err != cudaSuccess) return;
+        const int64_t ctas = partials * kLnClusterCtas;
+        const int64_t per_cta = (rows + ctas - 1) / ctas;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(unsigned(ctas));
+        cfg.blockDim = dim3(kBlockThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = kLnClusterCtas;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        err = cudaLaunchKernelEx(&cfg, kern, dy, gamma, xhat, inv_std, dx, ws, rows, int(cols),
+                                 per_cta);
+    });
+    if (!done) {
+        const int64_t per_cta = (rows + partials - 1) / partials;
+        if (vec4)
+            ln_bwd_rowblock<4><<<unsigned(partials), kBlockThreads, 0, stream>>>(
+                dy, gamma, xhat, inv_std, dx, ws, rows, cols, per_cta);
+        else
+            ln_bwd_rowblock<1><<<unsigned(partials), kBlockThreads, 0, stream>>>(
+                dy, gamma, xhat, inv_std, dx, ws, rows, cols, per_cta);
+    }
+    if (err == cudaSuccess) err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    const int64_t nb = (2 * cols + kBlockThreads - 1) / kBlockThreads;
+    ln_params_reduce<<<unsigned(nb), kBlockThreads, 0, stream>>>(ws, partials, cols, dgamma, dbeta);
+    note_launches(2);
+    return cudaGetLastError();
+}
+
+}  // namespace rowops

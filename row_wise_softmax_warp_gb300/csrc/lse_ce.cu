@@ -1,0 +1,431 @@
+// lse_ce.cu - per-row logsumexp, fused softmax cross-entropy (loss + logits
+// gradient) and the long-row softmax forward.
+//
+// Kernel shapes:
+//   *_group           : rows of up to 1024 floats in registers (common.cuh).
+//   long_row_cluster  : rows of 1K..128K floats (vectorised).  A thread-block
+//                       cluster of CL CTAs owns one row; each CTA holds a slice
+//                       in registers (NV float4 per thread), reduces its slice
+//                       to (max, sum exp) and the CTAs exchange those pairs
+//                       through distributed shared memory.  The row is read from
+//                       HBM exactly once, and the gradient or probabilities are
+//                       written from registers.
+//   *_rowblock        : any length and alignment, streaming two passes.
+#include "common.cuh"
+#include "launch.h"
+
+namespace rowops {
+namespace {
+
+// MicroGPT CuBLASBackend::fused_softmax_ce_grad / pulsatrix logsumexp_rows.
+
+template <int LANES, int NV, int VEC>
+__global__ void __launch_bounds__(kBlockThreads)
+lse_group(const float* __restrict__ x, float* __restrict__ lse, int64_t rows, int cols) {
+    constexpr int GPB = kBlockThreads / LANES;
+    const int g = threadIdx.x % LANES;
+    const int grp = threadIdx.x / LANES;
+    const int nch = cols / VEC;
+    for (int64_t base = int64_t(blockIdx.x) * GPB; base < rows; base += int64_t(gridDim.x) * GPB) {
+        const int64_t row = base + grp;
+        const bool live = row < rows;
+        const int64_t off = (live ? row : 0) * int64_t(cols);
+        float v[NV][VEC];
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c = g + k * LANES;
+            if (live && c < nch) {
+                ld_chunk<VEC>(x + off + c * VEC, v[k]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) v[k][e] = -INFINITY;
+            }
+        }
+        float m = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) m = fmaxf(m, v[k][e]);
+        m = group_max<LANES>(m);
+        float s = 0.f;
+        if (!isinf(m)) {
+#pragma unroll
+            for (int k = 0; k < NV; ++k)
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) s += expf(v[k][e] - m);
+        }
+        s = group_sum<LANES>(s);
+        if (live && g == 0) lse[row] = isinf(m) ? m : m + logf(s);
+    }
+}
+
+template <int LANES, int NV, int VEC>
+__global__ void __launch_bounds__(kBlockThreads)
+ce_group(const float* __restrict__ x, const int32_t* __restrict__ targets, float* __restrict__ grad,
+         float* __restrict__ row_loss, int64_t rows, int cols, float grad_scale) {
+    constexpr int GPB = kBlockThreads / LANES;
+    const int g = threadIdx.x % LANES;
+    const int grp = threadIdx.x / LANES;
+    const int nch = cols / VEC;
+    for (int64_t base = int64_t(blockIdx.x) * GPB; base < rows; base += int64_t(gridDim.x) * GPB) {
+        const int64_t row = base + grp;
+        const bool live = row < rows;
+        const int64_t off = (live ? row : 0) * int64_t(cols);
+        const int t = live ? __ldg(targets + row) : -1;
+        const bool tvalid = t >= 0 && t < cols;
+        float v[NV][VEC];
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c = g + k * LANES;
+            if (live && c < nch) {
+                ld_chunk<VEC>(x + off + c * VEC, v[k]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) v[k][e] = -INFINITY;
+            }
+        }
+        float m = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) m = fmaxf(m, v[k][e]);
+        m = group_max<LANES>(m);
+        float s = 0.f;
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                v[k][e] = expf(v[k][e] - m);
+                s += v[k][e];
+            }
+        s = group_sum<LANES>(s);
+        const float inv = 1.0f / s;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c = g + k * LANES;
+            if (live && c < nch) {
+                float o[VEC];
+#pragma unroll
+                for (int e = 0; e < VEC; ++e)
+                    o[e] = grad_scale * (v[k][e] * inv - ((tvalid && c * VEC + e == t) ? 1.f : 0.f));
+                st_chunk<VEC>(grad + off + c * VEC, o);
+            }
+        }
+        if (live && g == 0) {
+            const float lse = m + logf(s);
+            row_loss[row] = tvalid ? lse - __ldg(x + off + t) : __int_as_float(0x7fc00000);
+        }
+    }
+}
+
+// ---------------------------------------------------------- long rows
+
+enum class LongOp { kLse, kCe, kSoftmax };
+
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+
+template <LongOp OP, int NV>
+__global__ void __launch_bounds__(kBlockThreads)
+long_row_cluster(const float* x, float* out,  // out may be x (in-place softmax)
+                 const int32_t* __restrict__ targets, float* __restrict__ aux, int64_t rows,
+                 int cols, float grad_scale) {
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int CL = int(cluster.num_blocks());
+    const int rank = int(cluster.block_rank());
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    __shared__ float scratch[kBlockThreads / 32];
+    __shared__ float part[2];   // this CTA's (max, sum) published to the cluster
+    __shared__ float total[2];  // the row's (max, sum)
+    const int nch = cols / 4;
+    const int cpc = (nch + CL - 1) / CL;
+    const int c_begin = rank * cpc;
+    const int c_end = min(nch, c_begin + cpc);
+    const int64_t nclusters = gridDim.x / CL;
+    bool pending_wait = false;
+    for (int64_t row = blockIdx.x / CL; row < rows; row += nclusters) {
+        const int64_t off = row * int64_t(cols);
+        float v[NV][4];
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c = c_begin + tid + k * kBlockThreads;
+            if (c < c_end) {
+                ld_chunk<4>(x + off + c * 4, v[k]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) v[k][e] = -INFINITY;
+            }
+        }
+        float m = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) m = fmaxf(m, v[k][e]);
+        const float mc = block_max<kBlockThreads>(m, scratch);
+        float s = 0.f;
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                v[k][e] = (mc == -INFINITY) ? 0.f : expf(v[k][e] - mc);
+                s += v[k][e];
+            }
+        const float sc = block_sum<kBlockThreads>(s, scratch);
+        // Publish (mc, sc); peers must have finished reading the previous row's.
+        if (pending_wait) cluster_wait();
+        if (tid == 0) {
+            part[0] = mc;
+            part[1] = sc;
+        }
+        cluster_arrive();
+        cluster_wait();
+        if (tid < 32) {
+            float pm = -INFINITY, ps = 0.f;
+            if (lane < CL) {
+                const float* pq = cluster.map_shared_rank(part, lane);
+                pm = pq[0];
+                ps = pq[1];
+            }
+            MaxSum t{-INFINITY, 0.f};
+            for (int q = 0; q < CL; ++q)
+                t = ms_merge(t, MaxSum{__shfl_sync(kFullMask, pm, q), __shfl_sync(kFullMask, ps, q)});
+            if (lane == 0) {
+                total[0] = t.m;
+                total[1] = t.s;
+            }
+        }
+        cluster_arrive();  // done reading the peers' partials
+        pending_wait = true;
+        __syncthreads();
+        const float tm = total[0], ts = total[1];
+        if constexpr (OP == LongOp::kLse) {
+            if (rank == 0 && tid == 0) out[row] = isinf(tm) ? tm : tm + logf(ts);
+        } else {
+            const float alpha = (mc == -INFINITY) ? 0.f : expf(mc - tm) / ts;
+            int t = -1;
+            if constexpr (OP == LongOp::kCe) t = __ldg(targets + row);
+            const bool tvalid = t >= 0 && t < cols;
+#pragma unroll
+            for (int k = 0; k < NV; ++k) {
+                const int c = c_begin + tid + k * kBlockThreads;
+                if (c < c_end) {
+                    float o[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        if constexpr (OP == LongOp::kCe)
+                            o[e] = grad_scale * (v[k][e] * alpha - ((tvalid && c * 4 + e == t) ? 1.f : 0.f));
+                        else
+                            o[e] = v[k][e] * alpha;
+                    }
+                    st_chunk<4>(out + off + c * 4, o);
+                }
+            }
+            if constexpr (OP == LongOp::kCe) {
+                if (rank == 0 && tid == 0)
+                    aux[row] = tvalid ? (tm + logf(ts)) - __ldg(x + off + t) : __int_as_float(0x7fc00000);
+            }
+        }
+    }
+    // Keep this CTA's shared memory alive until every peer has read it.
+    if (pending_wait) cluster_wait();
+}
+
+// Picks (NV, CL) for a vectorised row of nch float4 chunks; false if too long.
+bool long_row_config(int64_t nch, int* nv, int* cl) {
+    const int nvs[3] = {4, 8, 16};
+    for (int i = 0; i < 3; ++i)
+        for (int c = 1; c <= 8; c *= 2)
+            if (int64_t(c) * kBlockThreads * nvs[i] >= nch) {
+                *nv = nvs[i];
+                *cl = c;
+                return true;
+            }
+    return false;
+}
+
+template <LongOp OP, int NV>
+cudaError_t launch_long_nv(int cl, const float* x, float* out, const int32_t* targets, float* aux,
+                           int64_t rows, int cols, float grad_scale, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(row_grid(rows, cl));
+    cfg.blockDim = dim3(kBlockThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, long_row_cluster<OP, NV>, x, out, targets, aux, rows, cols,
+                              grad_scale);
+}
+
+template <LongOp OP>
+cudaError_t launch_long(int nv, int cl, const float* x, float* out, const int32_t* targets,
+                        float* aux, int64_t rows, int cols, float grad_scale, cudaStream_t stream) {
+    switch (nv) {
+        case 4: return launch_long_nv<OP, 4>(cl, x, out, targets, aux, rows, cols, grad_scale, stream);
+        case 8: return launch_long_nv<OP, 8>(cl, x, out, targets, aux, rows, cols, grad_scale, stream);
+        default: return launch_long_nv<OP, 16>(cl, x, out, targets, aux, rows, cols, grad_scale, stream);
+    }
+}
+
+// ------------------------------------------------------------ streaming
+
+template <int VEC>
+__global__ void __launch_bounds__(kBlockThreads)
+lse_rowblock(const float* __restrict__ x, float* __restrict__ lse, int64_t rows, int64_t cols) {
+    __shared__ float scratch[2 * kBlockThreads / 32];
+    const int64_t nch = cols / VEC;
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const float* xr = x + row * cols;
+        MaxSum a{-INFINITY, 0.f};
+        for (int64_t c = threadIdx.x; c < nch; c += kBlockThreads) {
+            float v[VEC];
+            ld_chunk<VEC>(xr + c * VEC, v);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) a = ms_push(a, v[e]);
+        }
+        a = block_maxsum<kBlockThreads>(a, scratch);
+        if (threadIdx.x == 0) lse[row] = isinf(a.m) ? a.m : a.m + logf(a.s);
+    }
+}
+
+template <int VEC>
+__global__ void __launch_bounds__(kBlockThreads)
+ce_rowblock(const float* __restrict__ x, const int32_t* __restrict__ targets,
+            float* __restrict__ grad, float* __restrict__ row_loss, int64_t rows, int64_t cols,
+            float grad_scale) {
+    __shared__ float scratch[2 * kBlockThreads / 32];
+    const int64_t nch = cols / VEC;
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const float* xr = x + row * cols;
+        float* gr = grad + row * cols;
+        MaxSum a{-INFINITY, 0.f};
+        for (int64_t c = threadIdx.x; c < nch; c += kBlockThreads) {
+            float v[VEC];
+            ld_chunk<VEC>(xr + c * VEC, v);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) a = ms_push(a, v[e]);
+        }
+        a = block_maxsum<kBlockThreads>(a, scratch);
+        const int64_t t = __ldg(targets + row);
+        const bool tvalid = t >= 0 && t < cols;
+        const float inv = 1.0f / a.s;
+        for (int64_t c = threadIdx.x; c < nch; c += kBlockThreads) {
+            float v[VEC];
+            ld_chunk<VEC>(xr + c * VEC, v);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e)
+                v[e] = grad_scale * (expf(v[e] - a.m) * inv - ((tvalid && c * VEC + e == t) ? 1.f : 0.f));
+            st_chunk<VEC>(gr + c * VEC, v);
+        }
+        if (threadIdx.x == 0)
+            row_loss[row] = tvalid ? (a.m + logf(a.s)) - __ldg(xr + t) : __int_as_float(0x7fc00000);
+    }
+}
+
+// Mean of the row losses in double: each thread sums a fixed strided subset in
+// order, then a fixed tree; one block, so the order never changes.
+__global__ void __launch_bounds__(1024)
+ce_mean(const float* __restrict__ row_loss, int64_t rows, double* __restrict__ mean) {
+    __shared__ double sh[1024];
+    double s = 0.0;
+    for (int64_t i = threadIdx.x; i < rows; i += 1024) s += double(row_loss[i]);
+    sh[threadIdx.x] = s;
+    __syncthreads();
+    for (int w = 512; w > 0; w >>= 1) {
+        if (threadIdx.x < w) sh[threadIdx.x] += sh[threadIdx.x + w];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) *mean = sh[0] / double(rows);
+}
+
+__global__ void fill_value(float* __restrict__ p, int64_t n, float v) {
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += int64_t(gridDim.x) * blockDim.x)
+        p[i] = v;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------ launchers
+
+cudaError_t launch_logsumexp(const float* x, float* lse, int64_t rows, int64_t cols, bool vec4,
+                             cudaStream_t stream) {
+    if (cols == 0) {
+        const int64_t b = (rows + 255) / 256;
+        fill_value<<<unsigned(b > 4096 ? 4096 : b), 256, 0, stream>>>(lse, rows, -INFINITY);
+        note_launches(1);
+        return cudaGetLastError();
+    }
+    const bool done = with_geometry(vec4, cols, [&](auto geo) {
+        using G = decltype(geo);
+        lse_group<G::LANES, G::NV, G::VEC>
+            <<<group_grid(rows, G::LANES), kBlockThreads, 0, stream>>>(x, lse, rows, int(cols));
+    });
+    int nv = 0, cl = 0;
+    cudaError_t err = cudaSuccess;
+    if (!done) {
+        if (vec4 && long_row_config(cols / 4, &nv, &cl))
+            err = launch_long<LongOp::kLse>(nv, cl, x, lse, nullptr, nullptr, rows, int(cols), 1.f,
+                                            stream);
+        else if (vec4)
+            lse_rowblock<4><<<row_grid(rows), kBlockThreads, 0, stream>>>(x, lse, rows, cols);
+        else
+            lse_rowblock<1><<<row_grid(rows), kBlockThreads, 0, stream>>>(x, lse, rows, cols);
+    }
+    note_launches(1);
+    const cudaError_t last = cudaGetLastError();
+    return err != cudaSuccess ? err : last;
+}
+
+cudaError_t launch_softmax_ce(const float* logits, const int32_t* targets, float* grad,
+                              float* row_loss, double* mean_loss, int64_t rows, int64_t cols,
+                              float grad_scale, bool vec4, cudaStream_t stream) {
+    const bool done = with_geometry(vec4, cols, [&](auto geo) {
+        using G = decltype(geo);
+        ce_group<G::LANES, G::NV, G::VEC><<<group_grid(rows, G::LANES), kBlockThreads, 0, stream>>>(
+            logits, targets, grad, row_loss, rows, int(cols), grad_scale);
+    });
+    int nv = 0, cl = 0;
+    cudaError_t err = cudaSuccess;
+    if (!done) {
+        if (vec4 && long_row_config(cols / 4, &nv, &cl))
+            err = launch_long<LongOp::kCe>(nv, cl, logits, grad, targets, row_loss, rows, int(cols),
+                                           grad_scale, stream);
+        else if (vec4)
+            ce_rowblock<4><<<row_grid(rows), kBlockThreads, 0, stream>>>(logits, targets, grad,
+                                                                         row_loss, rows, cols,
+                                                                         grad_scale);
+        else
+            ce_rowblock<1><<<row_grid(rows), kBlockThreads, 0, stream>>>(logits, targets, grad,
+                                                                         row_loss, rows, cols,
+                                                                         grad_scale);
+    }
+    if (err == cudaSuccess) err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    ce_mean<<<1, 1024, 0, stream>>>(row_loss, rows, mean_loss);
+    note_launches(2);
+    return cudaGetLastError();
+}
+
+// Long vectorised rows of softmax_fwd use the cluster kernel; called from
+// softmax.cu's dispatcher through this hook.
+bool launch_softmax_fwd_long(const float* x, float* y, int64_t rows, int64_t cols,
+                             cudaStream_t stream, cudaError_t* err) {
+    int nv = 0, cl = 0;
+    if (!long_row_config(cols / 4, &nv, &cl)) return false;
+    *err = launch_long<LongOp::kSoftmax>(nv, cl, x, y, nullptr, nullptr, rows, int(cols), 1.f, stream);
+    return true;
+}
+
+}  // namespace rowops

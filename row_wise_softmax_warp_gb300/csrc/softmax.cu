@@ -473,14 +473,18 @@ cudaError_t launch_softmax_fwd(const float* x, float* y, int64_t rows, int64_t c
         softmax_fwd_group<G::LANES, G::NV, G::VEC>
             <<<group_grid(rows, G::LANES), kBlockThreads, 0, stream>>>(x, y, rows, int(cols));
     });
+    cudaError_t err = cudaSuccess;
     if (!done) {
-        if (vec4)
+        if (vec4 && launch_softmax_fwd_long(x, y, rows, cols, stream, &err)) {
+        } else if (vec4) {
             softmax_fwd_rowblock<4><<<row_grid(rows), kBlockThreads, 0, stream>>>(x, y, rows, cols);
-        else
+        } else {
             softmax_fwd_rowblock<1><<<row_grid(rows), kBlockThreads, 0, stream>>>(x, y, rows, cols);
+        }
     }
     note_launches(1);
-    return cudaGetLastError();
+    const cudaError_t last = cudaGetLastError();
+    return err != cudaSuccess ? err : last;
 }
 
 cudaError_t launch_softmax_bwd(const float* y, const float* dy, float* dx, int64_t rows,

@@ -1,0 +1,270 @@
+// topk_kept.cu - top-k kept mask (TorchLean Spec.MoE.kept): entry i of a row is
+// kept when fewer than k entries beat it; j beats i when x_j > x_i, or when
+// neither is larger and j < i.
+//
+// Without NaN, "beats" is the strict order of the 64-bit keys
+//   K_j = (ordered_key(x_j) << 32) | (cols - 1 - j)
+// (-0 and +0 share a key; a lower index gives a larger low word), so the number
+// of entries beating i is the rank of K_i and kept_i = [K_i >= T], T being the
+// k-th largest key.  T is found exactly either by k rounds of "largest key below
+// the previous one" (k or cols-k small: rounds of the smallest key above the
+// previous one) or by a bitwise radix select on the keys.
+//
+// A NaN is neither larger nor smaller than anything, which makes the relation
+// intransitive; any warp (or block) that meets a NaN in its rows counts beats
+// literally, O(cols) comparisons per entry.  Either way the output equals the
+// literal compare-and-count bit for bit.
+#include "common.cuh"
+#include "launch.h"
+
+namespace rowops {
+namespace {
+
+constexpr int kMaxRounds = 8;
+
+__device__ __forceinline__ uint64_t make_key(float x, int col, int cols) {
+    return (uint64_t(ordered_key(x)) << 32) | uint32_t(cols - 1 - col);
+}
+
+template <int LANES>
+__device__ __forceinline__ uint64_t group_max_u64(uint64_t v) {
+#pragma unroll
+    for (int o = LANES / 2; o > 0; o >>= 1) {
+        const uint64_t t = __shfl_xor_sync(kFullMask, v, o);
+        v = t > v ? t : v;
+    }
+    return v;
+}
+
+template <int LANES>
+__device__ __forceinline__ uint64_t group_min_u64(uint64_t v) {
+#pragma unroll
+    for (int o = LANES / 2; o > 0; o >>= 1) {
+        const uint64_t t = __shfl_xor_sync(kFullMask, v, o);
+        v = t < v ? t : v;
+    }
+    return v;
+}
+
+// Number of low-word bits that can be nonzero: cols - 1 < 2^lb.
+__device__ __forceinline__ int low_bits(int cols) { return cols <= 1 ? 0 : 32 - __clz(cols - 1); }
+
+template <int LANES, int NV, int VEC>
+__global__ void __launch_bounds__(kBlockThreads)
+kept_group(const float* __restrict__ x, float* __restrict__ kept, int64_t rows, int cols, int k) {
+    constexpr int GPB = kBlockThreads / LANES;
+    const int g = threadIdx.x % LANES;
+    const int grp = threadIdx.x / LANES;
+    const int leader = (threadIdx.x & 31) - g;
+    const int nch = cols / VEC;
+    const int lb = low_bits(cols);
+    for (int64_t base = int64_t(blockIdx.x) * GPB; base < rows; base += int64_t(gridDim.x) * GPB) {
+        const int64_t row = base + grp;
+        const bool live = row < rows;
+        const int64_t off = (live ? row : 0) * int64_t(cols);
+        float v[NV][VEC];
+        bool has_nan = false;
+#pragma unroll
+        for (int kk = 0; kk < NV; ++kk) {
+            const int c = g + kk * LANES;
+            if (live && c < nch) {
+                ld_chunk<VEC>(x + off + c * VEC, v[kk]);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) has_nan |= isnan(v[kk][e]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) v[kk][e] = 0.f;
+            }
+        }
+        bool keep[NV][VEC];
+        if (__any_sync(kFullMask, has_nan)) {
+            // Literal compare-and-count over the group's row (warp-uniform branch).
+            int cnt[NV][VEC];
+#pragma unroll
+            for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) cnt[kk][e] = 0;
+#pragma unroll
+            for (int ko = 0; ko < NV; ++ko)
+#pragma unroll
+                for (int eo = 0; eo < VEC; ++eo)
+                    for (int o = 0; o < LANES; ++o) {
+                        const float xj = __shfl_sync(kFullMask, v[ko][eo], leader + o);
+                        const int j = (o + ko * LANES) * VEC + eo;
+                        if (j < cols) {
+#pragma unroll
+                            for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+                                for (int e = 0; e < VEC; ++e) {
+                                    const int i = (g + kk * LANES) * VEC + e;
+                                    const float xi = v[kk][e];
+                                    const bool larger = xj > xi;
+                                    const bool neither = !(xj > xi) && !(xi > xj);
+                                    cnt[kk][e] += (larger || (neither && j < i)) ? 1 : 0;
+                                }
+                        }
+                    }
+#pragma unroll
+            for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) keep[kk][e] = cnt[kk][e] < k;
+        } else {
+            uint64_t key[NV][VEC];
+            bool valid[NV][VEC];
+#pragma unroll
+            for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    const int col = (g + kk * LANES) * VEC + e;
+                    valid[kk][e] = live && col < cols;
+                    key[kk][e] = make_key(v[kk][e], col, cols);
+                }
+            const int from_top = k, from_bottom = cols - k;
+            if (from_top <= kMaxRounds) {
+                // T = k-th largest key: k rounds of "largest key below the bound".
+                uint64_t bound = ~uint64_t(0);
+                for (int r = 0; r < from_top; ++r) {
+                    uint64_t best = 0;
+#pragma unroll
+                    for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e)
+                            if (valid[kk][e] && key[kk][e] < bound && key[kk][e] > best) best = key[kk][e];
+                    bound = group_max_u64<LANES>(best);
+                }
+#pragma unroll
+                for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) keep[kk][e] = key[kk][e] >= bound;
+            } else if (from_bottom <= kMaxRounds) {
+                // Not kept = the cols-k smallest keys.
+                uint64_t bound = 0;
+                for (int r = 0; r < from_bottom; ++r) {
+                    uint64_t best = ~uint64_t(0);
+#pragma unroll
+                    for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e)
+                            if (valid[kk][e] && (r == 0 || key[kk][e] > bound) && key[kk][e] < best)
+                                best = key[kk][e];
+                    bound = group_min_u64<LANES>(best);
+                }
+#pragma unroll
+                for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e)
+                        keep[kk][e] = from_bottom == 0 || key[kk][e] > bound;
+            } else {
+                // Radix select: T = max{t : #{K >= t} >= k}, built from the top bit.
+                uint64_t t = 0;
+                for (int b = 63; b >= 0; --b) {
+                    if (b < 32 && b >= lb) continue;  // low-word bits that are always 0
+                    const uint64_t cand = t | (uint64_t(1) << b);
+                    int n = 0;
+#pragma unroll
+                    for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e) n += (valid[kk][e] && key[kk][e] >= cand) ? 1 : 0;
+                    if (group_sum_int<LANES>(n) >= k) t = cand;
+                }
+#pragma unroll
+                for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) keep[kk][e] = key[kk][e] >= t;
+            }
+        }
+#pragma unroll
+        for (int kk = 0; kk < NV; ++kk) {
+            const int c = g + kk * LANES;
+            if (live && c < nch) {
+                float o[VEC];
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) o[e] = keep[kk][e] ? 1.f : 0.f;
+                st_chunk<VEC>(kept + off + c * VEC, o);
+            }
+        }
+    }
+}
+
+// Any length and alignment: one block per row, re-reading the row from global
+// memory (L1/L2) on every counting pass.
+template <int VEC>
+__global__ void __launch_bounds__(kBlockThreads)
+kept_rowblock(const float* __restrict__ x, float* __restrict__ kept, int64_t rows, int cols, int k) {
+    __shared__ int scratch[kBlockThreads / 32];
+    const int nch = cols / VEC;
+    const int lb = low_bits(cols);
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const float* xr = x + row * int64_t(cols);
+        float* kr = kept + row * int64_t(cols);
+        int nans = 0;
+        for (int c = threadIdx.x; c < nch; c += kBlockThreads) {
+            float v[VEC];
+            ld_chunk<VEC>(xr + c * VEC, v);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) nans += isnan(v[e]) ? 1 : 0;
+        }
+        nans = block_sum_int<kBlockThreads>(nans, scratch);
+        if (nans > 0) {
+            for (int c = threadIdx.x; c < nch; c += kBlockThreads) {
+                float v[VEC], o[VEC];
+                ld_chunk<VEC>(xr + c * VEC, v);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    const int i = c * VEC + e;
+                    int n = 0;
+                    for (int j = 0; j < cols; ++j) {
+                        const float xj = __ldg(xr + j);
+                        const bool larger = xj > v[e];
+                        const bool neither = !(xj > v[e]) && !(v[e] > xj);
+                        n += (larger || (neither && j < i)) ? 1 : 0;
+                    }
+                    o[e] = n < k ? 1.f : 0.f;
+                }
+                st_chunk<VEC>(kr + c * VEC, o);
+            }
+            continue;
+        }
+        uint64_t t = 0;
+        for (int b = 63; b >= 0; --b) {
+            if (b < 32 && b >= lb) continue;
+            const uint64_t cand = t | (uint64_t(1) << b);
+            int n = 0;
+            for (int c = threadIdx.x; c < nch; c += kBlockThreads) {
+                float v[VEC];
+                ld_chunk<VEC>(xr + c * VEC, v);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) n += make_key(v[e], c * VEC + e, cols) >= cand ? 1 : 0;
+            }
+            if (block_sum_int<kBlockThreads>(n, scratch) >= k) t = cand;
+        }
+        for (int c = threadIdx.x; c < nch; c += kBlockThreads) {
+            float v[VEC], o[VEC];
+            ld_chunk<VEC>(xr + c * VEC, v);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) o[e] = make_key(v[e], c * VEC + e, cols) >= t ? 1.f : 0.f;
+            st_chunk<VEC>(kr + c * VEC, o);
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_topk_kept(const float* x, float* kept, int64_t rows, int64_t cols, int64_t k,
+                             bool vec4, cudaStream_t stream) {
+    const bool done = with_geometry(vec4, cols, [&](auto geo) {
+        using G = decltype(geo);
+        kept_group<G::LANES, G::NV, G::VEC><<<group_grid(rows, G::LANES), kBlockThreads, 0, stream>>>(
+            x, kept, rows, int(cols), int(k));
+    });
+    if (!done) {
+        if (vec4)
+            kept_rowblock<4><<<row_grid(rows), kBlockThreads, 0, stream>>>(x, kept, rows, int(cols), int(k));
+        else
+            kept_rowblock<1><<<row_grid(rows), kBlockThreads, 0, stream>>>(x, kept, rows, int(cols), int(k));
+    }
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace rowops
