@@ -1,0 +1,232 @@
+"""Python binding of librowops (include/rowops.h): argument marshalling only.
+
+Every function has the name of its C entry point, takes torch CUDA tensors
+(fp32, contiguous, last dimension = cols, rows = numel / cols), allocates the
+outputs the caller leaves as ``None`` with torch, passes raw device pointers
+and the current torch stream to the C ABI and raises ``RowopsError`` on a
+nonzero status.  All arithmetic happens in the library's CUDA kernels; there
+is no other code path.  The library is loaded on first use and a missing build
+is an error, never a fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "librowops.so")
+
+_lib = None
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_F = ctypes.c_float
+
+SIGNATURES = {
+    "rowops_status_string": ([ctypes.c_int], ctypes.c_char_p),
+    "rowops_kernel_launches": ([], ctypes.c_uint64),
+    "rowops_softmax_fwd": ([_P, _P, _I64, _I64, _P], ctypes.c_int),
+    "rowops_softmax_bwd": ([_P, _P, _P, _I64, _I64, _P], ctypes.c_int),
+    "rowops_attn_softmax_fwd": ([_P, _P, _I64, _I64, _I64, _F, _P], ctypes.c_int),
+    "rowops_attn_softmax_bwd": ([_P, _P, _P, _I64, _I64, _I64, _F, _P], ctypes.c_int),
+    "rowops_masked_softmax": ([_P, _P, _P, _I64, _I64, _P], ctypes.c_int),
+    "rowops_logsumexp": ([_P, _P, _I64, _I64, _P], ctypes.c_int),
+    "rowops_softmax_ce": ([_P, _P, _P, _P, _P, _I64, _I64, _F, _P], ctypes.c_int),
+    "rowops_layernorm_fwd": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _P], ctypes.c_int),
+    "rowops_layernorm_bwd_workspace": ([_I64, _I64], ctypes.c_size_t),
+    "rowops_layernorm_bwd": ([_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P, ctypes.c_size_t, _P],
+                             ctypes.c_int),
+    "rowops_topk_kept": ([_P, _P, _I64, _I64, _I64, _P], ctypes.c_int),
+}
+
+
+class RowopsError(RuntimeError):
+    """A rowops_* entry point returned a nonzero status."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__(message)
+        self.status = status
+
+
+def library():
+    """The loaded librowops (ctypes.CDLL) with its C signatures declared."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with row_wise_softmax_warp_gb300.build.build() "
+                "(or __graft_entry__.build()); there is no fallback implementation")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+    return _lib
+
+
+def _check(status: int):
+    if status != 0:
+        raise RowopsError(status, library().rowops_status_string(status).decode())
+
+
+def _stream(t: torch.Tensor, stream):
+    if stream is None:
+        return torch.cuda.current_stream(t.device).cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _mat(t: torch.Tensor, name: str, dtype=torch.float32):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _shape(t: torch.Tensor):
+    if t.dim() == 0:
+        return 1, 1
+    cols = int(t.shape[-1])
+    return math.prod(t.shape[:-1]), cols
+
+
+def _out(t, like: torch.Tensor, name: str, shape=None, dtype=torch.float32):
+    if t is None:
+        return torch.empty(like.shape if shape is None else shape, dtype=dtype, device=like.device)
+    return _mat(t, name, dtype)
+
+
+def rowops_kernel_launches() -> int:
+    return int(library().rowops_kernel_launches())
+
+
+def rowops_softmax_fwd(x, y=None, stream=None):
+    """y = softmax(x) along the last dimension (y may be x)."""
+    x = _mat(x, "x")
+    y = _out(y, x, "y")
+    rows, cols = _shape(x)
+    _check(library().rowops_softmax_fwd(x.data_ptr(), y.data_ptr(), rows, cols, _stream(x, stream)))
+    return y
+
+
+def rowops_softmax_bwd(y, dy, dx=None, stream=None):
+    """dx = y * (dy - sum(y * dy)) along the last dimension."""
+    y, dy = _mat(y, "y"), _mat(dy, "dy")
+    dx = _out(dx, y, "dx")
+    rows, cols = _shape(y)
+    _check(library().rowops_softmax_bwd(y.data_ptr(), dy.data_ptr(), dx.data_ptr(), rows, cols,
+                                        _stream(y, stream)))
+    return dx
+
+
+def rowops_attn_softmax_fwd(scores, p=None, seq_len=None, scale=1.0, stream=None):
+    """Scaled causal softmax of stacked (batch*heads*seq_len, seq_len) score rows."""
+    scores = _mat(scores, "scores")
+    p = _out(p, scores, "p")
+    rows, cols = _shape(scores)
+    seq_len = cols if seq_len is None else seq_len
+    _check(library().rowops_attn_softmax_fwd(scores.data_ptr(), p.data_ptr(), rows, cols, seq_len,
+                                             scale, _stream(scores, stream)))
+    return p
+
+
+def rowops_attn_softmax_bwd(p, dp, ds=None, seq_len=None, scale=1.0, stream=None):
+    """Gradient of rowops_attn_softmax_fwd with respect to the raw scores, from p."""
+    p, dp = _mat(p, "p"), _mat(dp, "dp")
+    ds = _out(ds, p, "ds")
+    rows, cols = _shape(p)
+    seq_len = cols if seq_len is None else seq_len
+    _check(library().rowops_attn_softmax_bwd(p.data_ptr(), dp.data_ptr(), ds.data_ptr(), rows, cols,
+                                             seq_len, scale, _stream(p, stream)))
+    return ds
+
+
+def rowops_masked_softmax(x, mask, y=None, stream=None):
+    """Softmax over entries with mask != 0; blocked entries and empty rows are +0."""
+    x = _mat(x, "x")
+    mask = _mat(mask, "mask", torch.uint8)
+    y = _out(y, x, "y")
+    rows, cols = _shape(x)
+    _check(library().rowops_masked_softmax(x.data_ptr(), mask.data_ptr(), y.data_ptr(), rows, cols,
+                                           _stream(x, stream)))
+    return y
+
+
+def rowops_logsumexp(x, lse=None, stream=None):
+    """lse = log(sum(exp(x))) along the last dimension."""
+    x = _mat(x, "x")
+    rows, cols = _shape(x)
+    lse = _out(lse, x, "lse", shape=x.shape[:-1])
+    _check(library().rowops_logsumexp(x.data_ptr(), lse.data_ptr(), rows, cols, _stream(x, stream)))
+    return lse
+
+
+def rowops_softmax_ce(logits, targets, grad=None, row_loss=None, mean_loss=None, grad_scale=None,
+                      stream=None):
+    """Returns (grad, row_loss, mean_loss); mean_loss is a one-element float64 CUDA tensor."""
+    logits = _mat(logits, "logits")
+    targets = _mat(targets, "targets", torch.int32)
+    rows, cols = _shape(logits)
+    grad = _out(grad, logits, "grad")
+    row_loss = _out(row_loss, logits, "row_loss", shape=(rows,))
+    mean_loss = _out(mean_loss, logits, "mean_loss", shape=(1,), dtype=torch.float64)
+    if grad_scale is None:
+        grad_scale = 1.0 / rows if rows else 1.0
+    _check(library().rowops_softmax_ce(logits.data_ptr(), targets.data_ptr(), grad.data_ptr(),
+                                       row_loss.data_ptr(), mean_loss.data_ptr(), rows, cols,
+                                       grad_scale, _stream(logits, stream)))
+    return grad, row_loss, mean_loss
+
+
+def rowops_layernorm_fwd(x, gamma, beta, out=None, xhat=None, inv_std=None, eps=1e-5, stream=None):
+    """Returns (out, xhat, inv_std)."""
+    x, gamma, beta = _mat(x, "x"), _mat(gamma, "gamma"), _mat(beta, "beta")
+    rows, cols = _shape(x)
+    out = _out(out, x, "out")
+    xhat = _out(xhat, x, "xhat")
+    inv_std = _out(inv_std, x, "inv_std", shape=(rows,))
+    _check(library().rowops_layernorm_fwd(x.data_ptr(), gamma.data_ptr(), beta.data_ptr(),
+                                          out.data_ptr(), xhat.data_ptr(), inv_std.data_ptr(), rows,
+                                          cols, eps, _stream(x, stream)))
+    return out, xhat, inv_std
+
+
+def rowops_layernorm_bwd_workspace(rows: int, cols: int) -> int:
+    return int(library().rowops_layernorm_bwd_workspace(rows, cols))
+
+
+def rowops_layernorm_bwd(dy, gamma, xhat, inv_std, dx=None, dgamma=None, dbeta=None, workspace=None,
+                         stream=None):
+    """Returns (dx, dgamma, dbeta)."""
+    dy, gamma, xhat = _mat(dy, "dy"), _mat(gamma, "gamma"), _mat(xhat, "xhat")
+    inv_std = _mat(inv_std, "inv_std")
+    rows, cols = _shape(dy)
+    dx = _out(dx, dy, "dx")
+    dgamma = _out(dgamma, dy, "dgamma", shape=(cols,))
+    dbeta = _out(dbeta, dy, "dbeta", shape=(cols,))
+    need = rowops_layernorm_bwd_workspace(rows, cols)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dy.device)
+    _check(library().rowops_layernorm_bwd(dy.data_ptr(), gamma.data_ptr(), xhat.data_ptr(),
+                                          inv_std.data_ptr(), dx.data_ptr(), dgamma.data_ptr(),
+                                          dbeta.data_ptr(), rows, cols, workspace.data_ptr(),
+                                          workspace.numel() * workspace.element_size(),
+                                          _stream(dy, stream)))
+    return dx, dgamma, dbeta
+
+
+def rowops_topk_kept(x, k, kept=None, stream=None):
+    """1.0 where fewer than k entries of the row beat the entry, else 0.0."""
+    x = _mat(x, "x")
+    kept = _out(kept, x, "kept")
+    rows, cols = _shape(x)
+    _check(library().rowops_topk_kept(x.data_ptr(), kept.data_ptr(), rows, cols, k,
+                                      _stream(x, stream)))
+    return kept

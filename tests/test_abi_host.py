@@ -1,0 +1,135 @@
+"""The C ABI on the host: the library loads, exports what include/rowops.h
+declares, and rejects bad arguments with the documented status codes before
+touching the GPU.  The pointers below are never dereferenced: every call here
+fails validation (or is an empty no-op), so no kernel is launched."""
+import os
+import re
+
+import pytest
+
+import __graft_entry__
+from row_wise_softmax_warp_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+OK, NULL, SHAPE, ALIAS, WORKSPACE, CUDA = 0, 1, 2, 3, 4, 5
+
+A = 0x7000_0000_0000  # fake, 256-byte aligned device addresses far apart
+B = 0x7100_0000_0000
+C = 0x7200_0000_0000
+D = 0x7300_0000_0000
+E = 0x7400_0000_0000
+F = 0x7500_0000_0000
+G = 0x7600_0000_0000
+H = 0x7700_0000_0000
+W = 0x7800_0000_0000
+
+
+@pytest.fixture(scope="module")
+def lib():
+    __graft_entry__.build()
+    return binding.library()
+
+
+def test_exports_every_declared_symbol(lib):
+    header = open(os.path.join(ROOT, "include", "rowops.h")).read()
+    declared = set(re.findall(r"\b(rowops_[a-z0-9_]+)\s*\(", header))
+    assert len(declared) >= 13
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert declared == set(binding.SIGNATURES), declared ^ set(binding.SIGNATURES)
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert lib.rowops_status_string(s).startswith(b"ROWOPS")
+    assert b"unknown" in lib.rowops_status_string(99)
+
+
+def test_dims(lib):
+    n0 = lib.rowops_kernel_launches()
+    assert lib.rowops_softmax_fwd(A, B, -1, 4, None) == SHAPE
+    assert lib.rowops_softmax_fwd(A, B, 4, -1, None) == SHAPE
+    assert lib.rowops_softmax_fwd(A, B, 4, 1 << 31, None) == SHAPE
+    assert lib.rowops_softmax_fwd(A, B, 1 << 40, 1 << 30, None) == SHAPE
+    assert lib.rowops_softmax_fwd(A, B, 0, 128, None) == OK  # empty: no-op
+    assert lib.rowops_softmax_fwd(None, None, 0, 128, None) == OK
+    assert lib.rowops_softmax_fwd(A, B, 8, 0, None) == OK
+    assert lib.rowops_softmax_bwd(A, B, C, 8, 0, None) == OK
+    assert lib.rowops_masked_softmax(A, B, C, 8, 0, None) == OK
+    assert lib.rowops_kernel_launches() == n0
+
+
+def test_null_pointers(lib):
+    assert lib.rowops_softmax_fwd(None, B, 2, 4, None) == NULL
+    assert lib.rowops_softmax_bwd(A, None, C, 2, 4, None) == NULL
+    assert lib.rowops_attn_softmax_fwd(A, None, 8, 8, 8, 0.5, None) == NULL
+    assert lib.rowops_attn_softmax_bwd(A, B, None, 8, 8, 8, 0.5, None) == NULL
+    assert lib.rowops_masked_softmax(A, None, C, 2, 4, None) == NULL
+    assert lib.rowops_logsumexp(A, None, 2, 4, None) == NULL
+    assert lib.rowops_softmax_ce(A, B, C, D, None, 2, 4, 0.5, None) == NULL
+    assert lib.rowops_layernorm_fwd(A, B, C, D, E, None, 2, 4, 1e-5, None) == NULL
+    assert lib.rowops_layernorm_bwd(A, B, C, D, E, F, None, 2, 4, W, 1 << 20, None) == NULL
+    assert lib.rowops_topk_kept(None, B, 2, 4, 1, None) == NULL
+
+
+def test_aliasing(lib):
+    n = 16 * 64 * 4
+    assert lib.rowops_softmax_fwd(A, A + 64, 16, 64, None) == ALIAS       # partial overlap
+    assert lib.rowops_softmax_bwd(A, B, A, 16, 64, None) == ALIAS         # dx == y
+    assert lib.rowops_softmax_bwd(A, B, B + n - 4, 16, 64, None) == ALIAS  # dx tail overlaps dy
+    assert lib.rowops_attn_softmax_fwd(A, A, 64, 64, 64, 0.125, None) == ALIAS
+    assert lib.rowops_attn_softmax_bwd(A, B, B, 64, 64, 64, 0.125, None) == ALIAS
+    assert lib.rowops_masked_softmax(A, A + 128, B, 16, 64, None) == ALIAS  # mask inside x
+    assert lib.rowops_logsumexp(A, A + 8, 16, 64, None) == ALIAS
+    assert lib.rowops_softmax_ce(A, B, A, D, E, 16, 64, 0.1, None) == ALIAS        # grad == logits
+    assert lib.rowops_softmax_ce(A, B, C, D, D + 4, 16, 64, 0.1, None) == ALIAS    # mean in row_loss
+    assert lib.rowops_layernorm_fwd(A, B, C, D, D, E, 16, 64, 1e-5, None) == ALIAS  # out == xhat
+    assert lib.rowops_layernorm_bwd(A, B, C, D, A, F, G, 16, 64, W, 1 << 20, None) == ALIAS
+    assert lib.rowops_layernorm_bwd(A, B, C, D, E, F, F, 16, 64, W, 1 << 20, None) == ALIAS
+    assert lib.rowops_layernorm_bwd(A, B, C, D, E, F, G, 16, 64, E, 1 << 20, None) == ALIAS
+    assert lib.rowops_topk_kept(A, A, 16, 64, 2, None) == ALIAS
+
+
+def test_attention_shape_rules(lib):
+    assert lib.rowops_attn_softmax_fwd(A, B, 64, 32, 64, 0.125, None) == SHAPE  # cols != seq_len
+    assert lib.rowops_attn_softmax_fwd(A, B, 65, 64, 64, 0.125, None) == SHAPE  # rows % seq_len
+    assert lib.rowops_attn_softmax_fwd(A, B, 64, 64, 0, 0.125, None) == SHAPE
+    assert lib.rowops_attn_softmax_fwd(A, B, 64, 64, 64, 0.0, None) == SHAPE
+    assert lib.rowops_attn_softmax_fwd(A, B, 64, 64, 64, -1.0, None) == SHAPE
+    assert lib.rowops_attn_softmax_fwd(A, B, 64, 64, 64, float("inf"), None) == SHAPE
+    assert lib.rowops_attn_softmax_bwd(A, B, C, 64, 64, 64, float("nan"), None) == SHAPE
+    assert lib.rowops_attn_softmax_fwd(A, B, 0, 64, 64, 0.125, None) == OK
+
+
+def test_scalar_rules(lib):
+    assert lib.rowops_topk_kept(A, B, 4, 8, 0, None) == SHAPE
+    assert lib.rowops_topk_kept(A, B, 4, 8, 9, None) == SHAPE
+    assert lib.rowops_topk_kept(A, B, 4, 0, 1, None) == SHAPE
+    assert lib.rowops_topk_kept(A, B, 0, 8, 8, None) == OK
+    assert lib.rowops_softmax_ce(A, B, C, D, E, 4, 0, 0.25, None) == SHAPE
+    assert lib.rowops_softmax_ce(A, B, C, D, E, 4, 8, float("nan"), None) == SHAPE
+    assert lib.rowops_layernorm_fwd(A, B, C, D, E, F, 4, 0, 1e-5, None) == SHAPE
+    assert lib.rowops_layernorm_fwd(A, B, C, D, E, F, 4, 8, -1e-5, None) == SHAPE
+    assert lib.rowops_layernorm_fwd(A, B, C, D, E, F, 4, 8, float("inf"), None) == SHAPE
+    assert lib.rowops_layernorm_bwd(A, B, C, D, E, F, G, 4, 0, W, 1 << 20, None) == SHAPE
+
+
+def test_layernorm_workspace(lib):
+    need = lib.rowops_layernorm_bwd_workspace(4096, 768)
+    assert need > 0 and need % 16 == 0
+    assert lib.rowops_layernorm_bwd_workspace(0, 768) == 0
+    assert lib.rowops_layernorm_bwd_workspace(-1, 768) == 0
+    # the partial count is capped, so the workspace grows at most linearly in cols
+    big = lib.rowops_layernorm_bwd_workspace(1 << 24, 768)
+    assert big <= 128 * 2 * 768 * 4
+    assert lib.rowops_layernorm_bwd(A, B, C, D, E, F, G, 4096, 768, None, need, None) == WORKSPACE
+    assert lib.rowops_layernorm_bwd(A, B, C, D, E, F, G, 4096, 768, W, need - 4, None) == WORKSPACE
+    assert lib.rowops_layernorm_bwd(A, B, C, D, E, F, G, 4096, 768, W + 4, need, None) == WORKSPACE
+    assert lib.rowops_layernorm_bwd(A, B, C, D, E, F, G, 0, 768, None, 0, None) == OK
+
+
+def test_rejected_calls_launch_nothing(lib):
+    n0 = lib.rowops_kernel_launches()
+    lib.rowops_topk_kept(A, A, 16, 64, 2, None)
+    lib.rowops_softmax_ce(A, B, C, D, E, 4, 0, 0.25, None)
+    assert lib.rowops_kernel_launches() == n0
