@@ -1,0 +1,518 @@
+"""Benchmark of the row-op hot path on GB300.
+
+One step = one call of every row op, each on its workload at full size:
+
+  softmax_fwd / softmax_bwd   256 x 128
+  layernorm_fwd / _bwd        4096 x 768 (dx, dgamma, dbeta)
+  attn_softmax_fwd / _bwd     8 x 12 heads x 1024 x 1024, causal, scale 1/8
+  logsumexp / softmax_ce      8192 x 50304 (mean loss + logits gradient)
+  masked_softmax / topk_kept  262144 x 64, k = 2
+
+The L2 cache is flushed (a 512 MiB write) before every op, outside its CUDA
+events, so every op starts cold.  value = algorithmic bytes of all ops (the
+minimum each must read and write) / summed device time, in GB/s, over all
+ranks.  e2e repeats the steps through the same public calls with the inputs
+copied from pinned host memory and the outputs copied back inside the timed
+region.  ``--impl reference`` times the CPU oracle instead (see cpu_leg).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "achieved HBM GB/s (fraction of GB300 peak) and rows/sec per row-op, fp32"
+WORKLOAD = ("transformer-step row ops, full sizes: softmax fwd+bwd 256x128; LayerNorm fwd+bwd 4096x768; "
+            "causal attention softmax fwd+bwd 8x12x1024x1024; logsumexp + softmax-CE 8192x50304; "
+            "masked softmax + top-2 kept mask 262144x64")
+FLUSH_BYTES = 512 << 20
+
+
+# ---------------------------------------------------------------- workloads
+
+def algorithmic_bytes():
+    """Minimum bytes each op must read + write (fp32 = 4 bytes, mask = 1 byte)."""
+    r1, c1 = 256, 128
+    r2, c2 = 4096, 768
+    b, h, s = 8, 12, 1024
+    lower = b * h * s * (s + 1) // 2
+    full = b * h * s * s
+    r4, c4 = 8192, 50304
+    r5, c5 = 262144, 64
+    return {
+        "softmax_fwd": (2 * r1 * c1 * 4, r1),
+        "softmax_bwd": (3 * r1 * c1 * 4, r1),
+        "layernorm_fwd": (4 * (3 * r2 * c2 + 2 * c2 + r2), r2),
+        "layernorm_bwd": (4 * (3 * r2 * c2 + r2 + 3 * c2), r2),
+        "attn_softmax_fwd": (4 * (lower + full), b * h * s),
+        "attn_softmax_bwd": (4 * (2 * lower + full), b * h * s),
+        "logsumexp": (4 * (r4 * c4 + r4), r4),
+        "softmax_ce": (4 * (2 * r4 * c4 + r4) + 8, r4),
+        "masked_softmax": (9 * r5 * c5, r5),
+        "topk_kept": (8 * r5 * c5, r5),
+    }
+
+
+def make_inputs():
+    from row_wise_softmax_warp_gb300 import inputs
+    return {
+        "softmax": inputs.softmax_pair(0),
+        "layernorm": inputs.layernorm(0),
+        "attention": inputs.attention(0),
+        "ce": inputs.cross_entropy(0),
+        "router": inputs.router(0),
+    }
+
+
+class Ops:
+    """Device buffers and one closure per op (the public binding calls)."""
+
+    def __init__(self, data, dev):
+        import torch
+        import row_wise_softmax_warp_gb300 as ro
+        self.ro = ro
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+        d = data["softmax"]
+        self.sx, self.sdy = t(d["x"]), t(d["dy"])
+        self.sy, self.sdx = torch.empty_like(self.sx), torch.empty_like(self.sx)
+        n = data["layernorm"]
+        self.eps = n["eps"]
+        self.lx, self.lg, self.lb, self.ldy = t(n["x"]), t(n["gamma"]), t(n["beta"]), t(n["dy"])
+        self.lout, self.lxh = torch.empty_like(self.lx), torch.empty_like(self.lx)
+        self.lrs = torch.empty(self.lx.shape[0], device=dev)
+        self.ldx = torch.empty_like(self.lx)
+        self.ldg, self.ldb = torch.empty_like(self.lg), torch.empty_like(self.lg)
+        self.lws = torch.empty(ro.rowops_layernorm_bwd_workspace(*self.lx.shape), dtype=torch.uint8, device=dev)
+        a = data["attention"]
+        self.seq, self.scale = a["seq_len"], a["scale"]
+        self.as_, self.adp = t(a["scores"]), t(a["dp"])
+        self.ap, self.ads = torch.empty_like(self.as_), torch.empty_like(self.as_)
+        c = data["ce"]
+        self.cx, self.ct, self.cgs = t(c["logits"]), t(c["targets"]), c["grad_scale"]
+        self.clse = torch.empty(self.cx.shape[0], device=dev)
+        self.cg = torch.empty_like(self.cx)
+        self.crl = torch.empty(self.cx.shape[0], device=dev)
+        self.cml = torch.empty(1, dtype=torch.float64, device=dev)
+        r = data["router"]
+        self.rx, self.rm, self.k = t(r["x"]), t(r["mask"]), r["k"]
+        self.rp, self.rk = torch.empty_like(self.rx), torch.empty_like(self.rx)
+
+    def table(self):
+        ro = self.ro
+        return [
+            ("softmax_fwd", lambda: ro.rowops_softmax_fwd(self.sx, self.sy)),
+            ("softmax_bwd", lambda: ro.rowops_softmax_bwd(self.sy, self.sdy, self.sdx)),
+            ("layernorm_fwd", lambda: ro.rowops_layernorm_fwd(self.lx, self.lg, self.lb, self.lout, self.lxh,
+                                                              self.lrs, eps=self.eps)),
+            ("layernorm_bwd", lambda: ro.rowops_layernorm_bwd(self.ldy, self.lg, self.lxh, self.lrs, self.ldx,
+                                                              self.ldg, self.ldb, workspace=self.lws)),
+            ("attn_softmax_fwd", lambda: ro.rowops_attn_softmax_fwd(self.as_, self.ap, seq_len=self.seq,
+                                                                    scale=self.scale)),
+            ("attn_softmax_bwd", lambda: ro.rowops_attn_softmax_bwd(self.ap, self.adp, self.ads,
+                                                                    seq_len=self.seq, scale=self.scale)),
+            ("logsumexp", lambda: ro.rowops_logsumexp(self.cx, self.clse)),
+            ("softmax_ce", lambda: ro.rowops_softmax_ce(self.cx, self.ct, self.cg, self.crl, self.cml,
+                                                        grad_scale=self.cgs)),
+            ("masked_softmax", lambda: ro.rowops_masked_softmax(self.rx, self.rm, self.rp)),
+            ("topk_kept", lambda: ro.rowops_topk_kept(self.rp, self.k, self.rk)),
+        ]
+
+    def e2e_io(self):
+        """Per op: (device inputs, device outputs) that an end-to-end call moves."""
+        return {
+            "softmax_fwd": ([self.sx], [self.sy]),
+            "softmax_bwd": ([self.sy, self.sdy], [self.sdx]),
+            "layernorm_fwd": ([self.lx, self.lg, self.lb], [self.lout, self.lxh, self.lrs]),
+            "layernorm_bwd": ([self.ldy, self.lg, self.lxh, self.lrs], [self.ldx, self.ldg, self.ldb]),
+            "attn_softmax_fwd": ([self.as_], [self.ap]),
+            "attn_softmax_bwd": ([self.ap, self.adp], [self.ads]),
+            "logsumexp": ([self.cx], [self.clse]),
+            "softmax_ce": ([self.cx, self.ct], [self.cg, self.crl, self.cml]),
+            "masked_softmax": ([self.rx, self.rm], [self.rp]),
+            "topk_kept": ([self.rp], [self.rk]),
+        }
+
+
+# ------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while running (read-only queries)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid=None):
+        self.rows, self.proc, self.uuid = [], None, uuid
+        self.mark = False
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.uuid:
+            cmd += ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append((self.mark, parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        loaded = [p for m, p in self.rows if m] or [p for _, p in self.rows]
+        if not loaded:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in loaded if num(p[1]) is not None]
+        mx = [num(p[2]) for p in loaded if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in loaded for i in range(4) if p[5 + i].lower() == "active"})
+        power = [num(p[3]) for p in loaded if num(p[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(loaded),
+                "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------- helpers
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_fingerprint():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "row_wise_softmax_warp_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(op):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("kernel_fingerprint") != kernel_fingerprint():
+        return None
+    v = d.get("per_launch_bytes", {}).get(op)
+    return int(v) if v is not None else None
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws <= 1:
+        return 0, 1, None
+    import torch
+    import torch.distributed as dist
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    dist.init_process_group(backend)
+    return dist.get_rank(), dist.get_world_size(), dist
+
+
+def max_over_ranks(x, dist, device):
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist, device):
+    if dist is not None:
+        import torch
+        dist.barrier(device_ids=[device.index]) if device.type == "cuda" else dist.barrier()
+
+
+# ----------------------------------------------------------------- GPU arm
+
+def gpu_leg(args):
+    import torch
+    rank, world, dist = dist_setup()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from row_wise_softmax_warp_gb300 import build
+    build.build()
+    import row_wise_softmax_warp_gb300 as ro
+    ro.library()
+
+    data = make_inputs()
+    ops = Ops(data, dev)
+    table = ops.table()
+    abytes = algorithmic_bytes()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        uuid = None
+    clocks = ClockSampler(uuid)
+    clocks.start()
+
+    for _ in range(args.warmup):
+        for _, fn in table:
+            flush.zero_()
+            fn()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    starts = {n: [torch.cuda.Event(enable_timing=True) for _ in range(K)] for n, _ in table}
+    ends = {n: [torch.cuda.Event(enable_timing=True) for _ in range(K)] for n, _ in table}
+    outer0, outer1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist, dev)
+    torch.cuda.synchronize()
+    clocks.mark = True
+    launches0 = ro.rowops_kernel_launches()
+    outer0.record(stream)
+    for k in range(K):
+        for name, fn in table:
+            flush.zero_()
+            starts[name][k].record(stream)
+            fn()
+            ends[name][k].record(stream)
+    outer1.record(stream)
+    torch.cuda.synchronize()
+    launches = ro.rowops_kernel_launches() - launches0
+    barrier(dist, dev)
+    per_op_ms = {n: sum(starts[n][k].elapsed_time(ends[n][k]) for k in range(K)) / K for n, _ in table}
+    step_ms_local = sum(per_op_ms.values())
+    wall_ms_local = outer0.elapsed_time(outer1) / K
+
+    # ------------------------------------------------------------ e2e
+    io = ops.e2e_io()
+    pinned_in = {n: [torch.empty(x.shape, dtype=x.dtype, pin_memory=True).copy_(x) for x in io[n][0]]
+                 for n, _ in table}
+    pinned_out = {n: [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in io[n][1]]
+                  for n, _ in table}
+    h2d = sum(x.numel() * x.element_size() for n, _ in table for x in io[n][0])
+    d2h = sum(x.numel() * x.element_size() for n, _ in table for x in io[n][1])
+    ke = max(1, args.e2e_steps if args.e2e_steps else K)
+
+    def e2e_step():
+        for name, fn in table:
+            for dst, src in zip(io[name][0], pinned_in[name]):
+                dst.copy_(src, non_blocking=True)
+            fn()
+            for dst, src in zip(pinned_out[name], io[name][1]):
+                dst.copy_(src, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(dist, dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(ke):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms_local = e0.elapsed_time(e1) / ke
+    clocks.mark = False
+    clocks.stop()
+
+    step_ms = max_over_ranks(step_ms_local, dist, dev)
+    e2e_ms = max_over_ranks(e2e_ms_local, dist, dev)
+    wall_ms = max_over_ranks(wall_ms_local, dist, dev)
+    per_op = {n: max_over_ranks(per_op_ms[n], dist, dev) for n, _ in table}
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    peak, peak_kind = peaks()
+    total_bytes = sum(b for b, _ in abytes.values())
+    value = world * total_bytes / (step_ms * 1e-3) / 1e9
+    breakdown = {}
+    for n, _ in table:
+        b, rows = abytes[n]
+        gbs = b / (per_op[n] * 1e-3) / 1e9
+        breakdown[n] = {"ms": round(per_op[n], 5), "GB/s": round(gbs, 1), "frac_of_measured": round(gbs / peak, 4),
+                        "frac_of_8TBs": round(gbs / 8000.0, 4), "rows_per_s": round(rows / (per_op[n] * 1e-3), 1),
+                        "alg_bytes": b}
+    top = max(per_op, key=per_op.get)
+    top_gbs = abytes[top][0] / (per_op[top] * 1e-3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded numpy PCG64, the five workloads' distributions)",
+        "config": {"workload": WORKLOAD, "l2": "flushed before every op (512 MiB device write), outside the op's events",
+                   "ms_per_step_incl_flushes": round(wall_ms, 4), "parallelism": f"replicas x{world} (rows independent)"},
+        "roofline": {"bound": "hbm", "kernel": top, "achieved": round(top_gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(top_gbs / peak, 4), "peak_kind": peak_kind,
+                     "traffic": recorded_traffic(top)},
+        "ops": breakdown,
+        "gpu_launches": int(launches),
+        "e2e": {"value": round(world * total_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "ms_per_step": round(e2e_ms, 3), "steps": ke},
+        "clocks": clocks.summary(),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_leg(data, budget_s=args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------- CPU leg
+
+def cpu_leg(data, budget_s=12.0):
+    """Times the double-precision oracle (as it stands) on all host cores, on a
+    bounded, deterministic sample of each workload's rows; returns GB/s of the
+    same algorithmic bytes per processed row."""
+    import oracle
+    threads = oracle.threads()
+    share = budget_s / 10.0  # seconds of work per op, roughly
+    results = []
+
+    def run(name, fn, row_bytes, rows_total, probe_rows):
+        # size the sample from a short probe so each op takes about `share` seconds
+        t0 = time.perf_counter()
+        fn(0, probe_rows)
+        dt = max(time.perf_counter() - t0, 1e-6)
+        n = int(min(rows_total, max(probe_rows, probe_rows * share / dt)))
+        t0 = time.perf_counter()
+        fn(0, n)
+        dt = time.perf_counter() - t0
+        results.append((name, n, row_bytes(0, n), dt))
+
+    d = data["softmax"]
+    y32 = oracle.softmax_rows(d["x"]).astype(np.float32)
+    run("softmax_fwd", lambda a, b: oracle.softmax_rows(d["x"][a:b]), lambda a, b: (b - a) * 128 * 8, 256, 256)
+    run("softmax_bwd", lambda a, b: oracle.softmax_rows_backward(y32[a:b], d["dy"][a:b]),
+        lambda a, b: (b - a) * 128 * 12, 256, 256)
+    n = data["layernorm"]
+    run("layernorm_fwd", lambda a, b: oracle.layernorm_forward(n["x"][a:b], n["gamma"], n["beta"], n["eps"]),
+        lambda a, b: (b - a) * (768 * 12 + 4), 4096, 256)
+    _, xh, rs = oracle.layernorm_forward(n["x"], n["gamma"], n["beta"], n["eps"])
+    xh32, rs32 = xh.astype(np.float32), rs.astype(np.float32)
+    run("layernorm_bwd", lambda a, b: oracle.layernorm_backward(n["dy"][a:b], n["gamma"], xh32[a:b], rs32[a:b]),
+        lambda a, b: (b - a) * (768 * 12 + 4), 4096, 256)
+    at = data["attention"]
+    S, sc = at["seq_len"], at["scale"]
+
+    def attn_bytes(a, b, reads):
+        q = np.arange(a, b) % S
+        return int(4 * (reads * (q + 1).sum() + (b - a) * S))
+    run("attn_softmax_fwd", lambda a, b: oracle.attn_softmax_forward(at["scores"][a:b], S, sc),
+        lambda a, b: attn_bytes(a, b, 1), at["scores"].shape[0], 1024)
+    run("attn_softmax_bwd", lambda a, b: oracle.attn_softmax_backward(at["scores"][a:b], at["dp"][a:b], S, sc),
+        lambda a, b: attn_bytes(a, b, 2), at["scores"].shape[0], 1024)
+    c = data["ce"]
+    run("logsumexp", lambda a, b: oracle.logsumexp_rows(c["logits"][a:b]), lambda a, b: (b - a) * (50304 * 4 + 4),
+        8192, 16)
+    run("softmax_ce", lambda a, b: oracle.softmax_cross_entropy(c["logits"][a:b], c["targets"][a:b], 1 / 8192),
+        lambda a, b: (b - a) * (50304 * 8 + 4), 8192, 16)
+    r = data["router"]
+    run("masked_softmax", lambda a, b: oracle.masked_softmax(r["x"][a:b], r["mask"][a:b]),
+        lambda a, b: (b - a) * 64 * 9, 262144, 8192)
+    run("topk_kept", lambda a, b: oracle.topk_kept(r["x"][a:b], 2), lambda a, b: (b - a) * 64 * 8, 262144, 8192)
+    tot_b = sum(x[2] for x in results)
+    tot_t = sum(x[3] for x in results)
+    return {"value": round(tot_b / tot_t / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "seconds": round(tot_t, 2),
+            "sample": "; ".join(f"{n}: {k} rows" for n, k, _, _ in results) +
+                      " (first rows of each workload, double-precision C oracle, all host cores)"}
+
+
+def reference_leg(args):
+    """--impl reference: the CPU oracle as the reference arm (rank 0 only)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    data = make_inputs()
+    for _ in range(args.warmup):
+        cpu_leg(data, budget_s=1.0)
+    vals, secs, last = [], 0.0, None
+    for _ in range(args.steps):
+        last = cpu_leg(data, budget_s=args.ref_step_seconds)
+        vals.append(last["value"])
+        secs += last["seconds"]
+    value = statistics.mean(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1000 * secs / args.steps, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded numpy PCG64)",
+        "config": {"workload": WORKLOAD, "sample": "bounded row sample per op, see cpu_baseline"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": last["cores"], "kind": "oracle",
+                         "sample": last["sample"]},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=0, help="end-to-end steps (default: --steps)")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=4.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        reference_leg(args)
+    else:
+        gpu_leg(args)
+
+
+if __name__ == "__main__":
+    main()

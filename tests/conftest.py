@@ -30,3 +30,12 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def ro():
+    """The built rowops package (compiles librowops.so and the oracle if needed)."""
+    import __graft_entry__
+    __graft_entry__.build()
+    import row_wise_softmax_warp_gb300 as pkg
+    return pkg

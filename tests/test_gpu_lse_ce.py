@@ -1,0 +1,70 @@
+"""GPU parity: logsumexp and fused softmax cross-entropy (loss, gradient,
+mean loss)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity_util import check_abs, check_rel, gpu, host
+from row_wise_softmax_warp_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+COLS = [1, 3, 4, 7, 32, 64, 129, 256, 1000, 1024, 1028, 3001, 4096, 8192, 50304, 50305, 131072, 140000]
+
+
+@pytest.mark.parametrize("cols", COLS)
+@pytest.mark.parametrize("misalign", [False, True])
+def test_lse_ce_shapes(ro, cols, misalign):
+    rows = 6 if cols > 4096 else 33
+    c = inputs.cross_entropy(cols, rows=rows, cols=cols, outlier_frac=2e-3)
+    x, t = c["logits"], c["targets"]
+    lse = host(ro.rowops_logsumexp(gpu(x, misalign)))
+    check_rel(lse, oracle.logsumexp_rows(x), f"lse cols={cols}")
+    g, rl, ml = ro.rowops_softmax_ce(gpu(x, misalign), gpu(t), grad_scale=c["grad_scale"])
+    gr, rlr, mlr = oracle.softmax_cross_entropy(x, t, c["grad_scale"])
+    check_abs(host(g), gr, 2e-6 * c["grad_scale"], f"ce grad cols={cols}")
+    check_rel(host(rl), rlr, f"ce row loss cols={cols}")
+    check_rel(host(ml), [mlr], f"ce mean loss cols={cols}")
+
+
+def test_ce_scaled_workload(ro):
+    c = inputs.cross_entropy(0, rows=96, cols=50304)
+    x, t = c["logits"], c["targets"]
+    g, rl, ml = ro.rowops_softmax_ce(gpu(x), gpu(t), grad_scale=c["grad_scale"])
+    gr, rlr, mlr = oracle.softmax_cross_entropy(x, t, c["grad_scale"])
+    check_abs(host(g), gr, 2e-6 * c["grad_scale"], "ce grad 96x50304")
+    check_rel(host(rl), rlr, "ce row loss")
+    check_rel(host(ml), [mlr], "ce mean loss")
+    check_rel(host(ro.rowops_logsumexp(gpu(x))), oracle.logsumexp_rows(x), "lse 96x50304")
+
+
+def test_ce_out_of_range_targets(ro):
+    c = inputs.cross_entropy(1, rows=4, cols=300)
+    x = c["logits"]
+    t = np.array([5, 300, -1, 299], np.int32)
+    g, rl, ml = ro.rowops_softmax_ce(gpu(x), gpu(t), grad_scale=0.5)
+    gr, rlr, mlr = oracle.softmax_cross_entropy(x, t, 0.5)
+    rl = host(rl)
+    assert not np.isnan(rl[0]) and np.isnan(rl[1]) and np.isnan(rl[2]) and not np.isnan(rl[3])
+    assert np.isnan(host(ml)[0]) and np.isnan(mlr)
+    check_abs(host(g), gr, 1e-6, "grad without one-hot term")
+
+
+def test_lse_special_rows(ro):
+    x = np.array([[-np.inf] * 8, [np.inf, 0, 0, 0, 0, 0, 0, 0], [1000] * 8, [-1000] * 8], np.float32)
+    got = host(ro.rowops_logsumexp(gpu(x)))
+    ref = oracle.logsumexp_rows(x)
+    assert got[0] == -np.inf and got[1] == np.inf
+    check_rel(got[2:], ref[2:], "lse +-1000")
+    x = torch.empty((5, 0), device="cuda")
+    assert (host(ro.rowops_logsumexp(x)) == -np.inf).all()
+
+
+def test_ce_deterministic(ro):
+    c = inputs.cross_entropy(2, rows=64, cols=50304)
+    x, t = gpu(c["logits"]), gpu(c["targets"])
+    a = ro.rowops_softmax_ce(x, t)
+    b = ro.rowops_softmax_ce(x, t)
+    for u, v in zip(a, b):
+        assert torch.equal(u, v)

@@ -1,0 +1,91 @@
+"""GPU parity: hard-masked softmax and the top-k kept mask (bit-exact)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity_util import check_exact_zero, check_probs, gpu, host
+from row_wise_softmax_warp_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def test_router_workload_scaled(ro):
+    r = inputs.router(0, rows=8192)
+    x, mask = r["x"], r["mask"]
+    p = host(ro.rowops_masked_softmax(gpu(x), gpu(mask)))
+    pr = oracle.masked_softmax(x, mask)
+    check_probs(p, pr, "masked softmax")
+    check_exact_zero(p, mask == 0, "blocked entries")
+    assert (p[r["blocked_rows"]] == 0).all()
+    p32 = pr.astype(np.float32)
+    kept = host(ro.rowops_topk_kept(gpu(p32), 2))
+    assert np.array_equal(kept, oracle.topk_kept(p32, 2).astype(np.float32))
+    kept_x = host(ro.rowops_topk_kept(gpu(x), 2))
+    assert np.array_equal(kept_x, oracle.topk_kept(x, 2).astype(np.float32))
+
+
+MASK_COLS = [1, 2, 3, 4, 7, 8, 16, 33, 64, 128, 255, 256, 1024, 1028, 5000]
+
+
+@pytest.mark.parametrize("cols", MASK_COLS)
+@pytest.mark.parametrize("misalign", [False, True])
+def test_masked_shapes(ro, cols, misalign):
+    r = inputs.router(cols, rows=50, cols=cols, p_allow=0.6, blocked_row_frac=0.1)
+    x, mask = r["x"], r["mask"]
+    mask = mask * np.uint8(1 + (np.arange(mask.size).reshape(mask.shape) % 7))  # any nonzero byte allows
+    p = host(ro.rowops_masked_softmax(gpu(x, misalign), gpu(mask, misalign)))
+    check_probs(p, oracle.masked_softmax(x, mask), f"masked cols={cols}")
+    check_exact_zero(p, mask == 0, "blocked")
+
+
+def test_masked_in_place(ro):
+    r = inputs.router(2, rows=100)
+    t = gpu(r["x"])
+    ro.rowops_masked_softmax(t, gpu(r["mask"]), t)
+    check_probs(host(t), oracle.masked_softmax(r["x"], r["mask"]), "in place")
+
+
+KEPT_CASES = [(c, k) for c in (1, 2, 3, 4, 5, 8, 16, 31, 64, 100, 256, 1000, 1024, 1100, 4096)
+              for k in sorted({1, min(2, c), min(3, c), min(8, c), min(9, c), max(1, c // 2),
+                               max(1, c - 8), max(1, c - 1), c})]
+
+
+@pytest.mark.parametrize("cols,k", KEPT_CASES)
+def test_kept_exact(ro, cols, k):
+    rng = np.random.default_rng(cols * 1000 + k)
+    rows = 40 if cols <= 1024 else 6
+    x = (rng.integers(-8, 9, (rows, cols)) / 4.0).astype(np.float32)  # many ties
+    x[x == 0] = np.where(rng.random(int((x == 0).sum())) < 0.5, 0.0, -0.0).astype(np.float32)
+    for misalign in (False, True):
+        kept = host(ro.rowops_topk_kept(gpu(x, misalign), k))
+        ref = oracle.topk_kept(x, k).astype(np.float32)
+        assert np.array_equal(kept, ref), (cols, k, misalign, np.argwhere(kept != ref)[:5])
+
+
+@pytest.mark.parametrize("cols", [3, 8, 64, 300, 1024, 2000])
+def test_kept_with_nan_and_infinities(ro, cols):
+    rng = np.random.default_rng(cols)
+    x = (rng.integers(-4, 5, (24, cols)) / 2.0).astype(np.float32)
+    x[rng.random(x.shape) < 0.05] = np.nan
+    x[rng.random(x.shape) < 0.03] = np.inf
+    x[rng.random(x.shape) < 0.03] = -np.inf
+    x[5] = np.nan
+    for k in sorted({1, 2, min(3, cols), cols}):
+        kept = host(ro.rowops_topk_kept(gpu(x), k))
+        assert np.array_equal(kept, oracle.topk_kept(x, k).astype(np.float32)), (cols, k)
+
+
+def test_kept_denormals(ro):
+    tiny = np.float32(1e-45)
+    x = np.array([[tiny, 0.0, -tiny, -0.0, 2 * tiny, tiny]], np.float32)
+    for k in range(1, 7):
+        kept = host(ro.rowops_topk_kept(gpu(x), k))
+        assert np.array_equal(kept, oracle.topk_kept(x, k).astype(np.float32)), k
+
+
+def test_router_empty(ro):
+    x = torch.empty((0, 64), device="cuda")
+    m = torch.empty((0, 64), dtype=torch.uint8, device="cuda")
+    assert ro.rowops_masked_softmax(x, m).shape == (0, 64)
+    assert ro.rowops_topk_kept(x, 2).shape == (0, 64)
