@@ -186,6 +186,42 @@ int rowops_layernorm_bwd(const float *dy, const float *gamma, const float *xhat,
                          rowops_stream stream);
 
 /*
+ * LayerNorm backward that allocates nothing and takes no workspace.  The pages
+ * have no counterpart; this is a convenience of this library.
+ *
+ * Some callers cannot obtain device memory when they need this op: code that
+ * runs under a fixed device-memory budget set aside up front, plugins whose
+ * host framework owns every allocation and offers no scratch space, or code
+ * that must not enter an allocator at all (inside an allocator's own
+ * out-of-memory path, for instance).  For them this entry point computes
+ * exactly what rowops_layernorm_bwd computes, with the same argument rules,
+ * using a workspace that lives inside the library: a fixed array of
+ * rowops_layernorm_bwd_noalloc_max_bytes() bytes (1 MiB) of device memory,
+ * which every GPU that loads the library holds until the process exits.
+ *
+ *   - The first call on each device looks up that array's device address
+ *     (with the device current); make that first call before any stream
+ *     capture.  Later calls reuse the address.
+ *   - Shapes whose workspace, rowops_layernorm_bwd_workspace(rows, cols), is
+ *     larger than the array are refused with ROWOPS_ERR_WORKSPACE.  With
+ *     cols <= 1024 every row count fits; wider rows fit while rows is small
+ *     enough.
+ *   - All calls on a device share the one array, and it keeps the contents of
+ *     the last call.  Nothing in it needs to start at zero: each call writes
+ *     every partial sum it later reads.  Calls that can overlap on the GPU
+ *     (different streams, no ordering between them) race on the array and may
+ *     return wrong dgamma/dbeta; order them, or use rowops_layernorm_bwd with
+ *     separate workspaces.
+ *   - It never calls cudaMalloc, cudaFree or any other allocating routine.
+ */
+int rowops_layernorm_bwd_noalloc(const float *dy, const float *gamma, const float *xhat,
+                                 const float *inv_std, float *dx, float *dgamma, float *dbeta,
+                                 int64_t rows, int64_t cols, rowops_stream stream);
+
+/* Size in bytes of the array rowops_layernorm_bwd_noalloc uses (1 MiB). */
+size_t rowops_layernorm_bwd_noalloc_max_bytes(void);
+
+/*
  * Top-k kept mask.  [P3] kept mask (Spec.MoE.kept): entry i of a row is kept
  * when fewer than k entries of the row beat it; entry j beats entry i when
  * x_j > x_i, or when neither is larger and j < i.

@@ -39,6 +39,8 @@ SIGNATURES = {
     "rowops_layernorm_bwd": ([_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P, ctypes.c_size_t, _P],
                              ctypes.c_int),
     "rowops_topk_kept": ([_P, _P, _I64, _I64, _I64, _P], ctypes.c_int),
+    "rowops_layernorm_bwd_noalloc": ([_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P], ctypes.c_int),
+    "rowops_layernorm_bwd_noalloc_max_bytes": ([], ctypes.c_size_t),
 }
 
 
@@ -230,3 +232,19 @@ def rowops_topk_kept(x, k, kept=None, stream=None):
     _check(library().rowops_topk_kept(x.data_ptr(), kept.data_ptr(), rows, cols, k,
                                       _stream(x, stream)))
     return kept
+
+
+def rowops_layernorm_bwd_noalloc(dy, gamma, xhat, inv_std, dx=None, dgamma=None, dbeta=None, stream=None):
+    """rowops_layernorm_bwd without a workspace argument: the library's own
+    fixed device array serves as workspace (calls on one device must not
+    overlap on the GPU).  Returns (dx, dgamma, dbeta)."""
+    dy, gamma, xhat = _mat(dy, "dy"), _mat(gamma, "gamma"), _mat(xhat, "xhat")
+    inv_std = _mat(inv_std, "inv_std")
+    rows, cols = _shape(dy)
+    dx = _out(dx, dy, "dx")
+    dgamma = _out(dgamma, dy, "dgamma", shape=(cols,))
+    dbeta = _out(dbeta, dy, "dbeta", shape=(cols,))
+    _check(library().rowops_layernorm_bwd_noalloc(dy.data_ptr(), gamma.data_ptr(), xhat.data_ptr(),
+                                                  inv_std.data_ptr(), dx.data_ptr(), dgamma.data_ptr(),
+                                                  dbeta.data_ptr(), rows, cols, _stream(dy, stream)))
+    return dx, dgamma, dbeta

@@ -434,3 +434,62 @@ cudaError_t launch_layernorm_bwd(const float* dy, const float* gamma, const floa
 }
 
 }  // namespace rowops
+
+// ------------------------------------------------ allocation-free variant
+// LayerNorm backward for callers that cannot hand the library a workspace
+// (see rowops_layernorm_bwd_noalloc in include/rowops.h).  Its workspace is a
+// fixed array in device memory that the library owns for the life of the
+// process on every GPU that loads it.
+
+#include <mutex>
+
+#include "../../include/rowops.h"
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;  // 1 MiB per device
+constexpr int kNoAllocMaxDevices = 64;
+
+static __device__ __align__(256) float g_ln_bwd_scratch[kNoAllocScratchBytes / sizeof(float)];
+
+std::mutex g_scratch_mu;
+float* g_scratch_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  Host code only
+// holds a host-side stand-in under the array's name, so the real address is
+// asked for once per device, with that device current.
+int scratch_for_current_device(float** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices)
+        return ROWOPS_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (g_scratch_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_ln_bwd_scratch) != cudaSuccess || p == nullptr)
+            return ROWOPS_ERR_CUDA;
+        g_scratch_ptr[dev] = static_cast<float*>(p);
+    }
+    *out = g_scratch_ptr[dev];
+    return ROWOPS_OK;
+}
+
+}  // namespace
+
+extern "C" size_t rowops_layernorm_bwd_noalloc_max_bytes(void) { return kNoAllocScratchBytes; }
+
+extern "C" int rowops_layernorm_bwd_noalloc(const float* dy, const float* gamma, const float* xhat,
+                                            const float* inv_std, float* dx, float* dgamma,
+                                            float* dbeta, int64_t rows, int64_t cols,
+                                            rowops_stream stream) {
+    // Same argument rules as rowops_layernorm_bwd, checked there; only the
+    // workspace is ours.  Sizes whose workspace exceeds the array are refused.
+    if (rows > 0 && cols > 0 && rowops_layernorm_bwd_workspace(rows, cols) > kNoAllocScratchBytes)
+        return ROWOPS_ERR_WORKSPACE;
+    if (rows <= 0 || cols <= 0)  // nothing to set up; let the common checks answer
+        return rowops_layernorm_bwd(dy, gamma, xhat, inv_std, dx, dgamma, dbeta, rows, cols, nullptr,
+                                    0, stream);
+    float* ws = nullptr;
+    if (int e = scratch_for_current_device(&ws)) return e;
+    return rowops_layernorm_bwd(dy, gamma, xhat, inv_std, dx, dgamma, dbeta, rows, cols, ws,
+                                kNoAllocScratchBytes, stream);
+}
