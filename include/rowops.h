@@ -67,8 +67,8 @@ uint64_t rowops_kernel_launches(void);
  * softmax_rows(x); [P4] softmax(..., axis) on the last axis.
  *   y_ij = exp(x_ij - m_i) / sum_k exp(x_ik - m_i),  m_i = max_k x_ik.
  * x, y: rows x cols.  y may be exactly x (in place, as [P1] allows); any other
- * overlap is ROWOPS_ERR_ALIAS.  cols == 0 is a no-op ([P3] softmax "including
- * empty tensors").
+ * overlap is ROWOPS_ERR_ALIAS.  cols == 0 is a no-op ([P3]'s softmax accepts
+ * empty tensors).
  */
 int rowops_softmax_fwd(const float *x, float *y, int64_t rows, int64_t cols,
                        rowops_stream stream);

@@ -25,7 +25,7 @@
  *
  * Parity pins: every function here is pinned by tests that do not reuse its own
  * formula (closed forms, invariants, finite differences, brute force and
- * textbook library routines); no function is "parity unpinned".
+ * textbook library routines); no function lacks a pin.
  */
 #include <math.h>
 #include <stddef.h>
@@ -45,8 +45,8 @@ static double row_max(const double *x, int64_t n)
  * maximum subtracted before exponentiation; [P2] softmax_rows(x); [P4]
  * softmax(input, output, shape, axis) along the last axis.
  *   m = max_j x_j,  y_j = exp(x_j - m) / sum_k exp(x_k - m).
- * cols == 0 leaves nothing to write ([P3] stable softmax "including empty
- * tensors").
+ * cols == 0 leaves nothing to write ([P3]'s stable softmax accepts empty
+ * tensors).
  */
 void oracle_softmax_rows(const double *x, double *y, int64_t rows, int64_t cols)
 {
@@ -84,7 +84,7 @@ void oracle_softmax_rows_backward(const double *y, const double *dy, double *dx,
 }
 
 /*
- * [P2] fused_attn_softmax(scores, scale): "scale + causal mask + softmax", whose
+ * [P2] fused_attn_softmax(scores, scale): scaling, causal masking and softmax in one op, whose
  * default implementation is the composition of the separate ops; rows are the
  * stacked (batch * heads * seq_len, seq_len) score matrix of
  * causal_mask_batched(scores, seq_len), so row r holds query position
@@ -119,7 +119,7 @@ void oracle_attn_softmax_forward(const double *s, double *p, int64_t rows, int64
 /*
  * [P2] fused_attn_softmax_backward(s, ds, scale): the vector-Jacobian product of
  * the map above with respect to the raw scores, from its output p (the same
- * "from the output" form as [P1] softmax_rows_backward), times the chain-rule
+ * output-based form as [P1] softmax_rows_backward), times the chain-rule
  * factor scale:
  *   c = sum_{k<=i} p_k dp_k,  ds_j = scale * p_j * (dp_j - c)  (j <= i),
  *   ds_j = 0  (j > i).
