@@ -62,6 +62,12 @@ const char *rowops_status_string(int status);
  * all threads).  Diagnostic counter for benchmarks. */
 uint64_t rowops_kernel_launches(void);
 
+/* Number of times a pipelined kernel of this library gave up a bounded wait on
+ * the current device since the library was loaded (0 in correct operation; a
+ * kernel that gives up leaves its outputs incomplete).  Synchronous: copies a
+ * counter from the device; returns 0xffffffff if the copy fails. */
+uint32_t rowops_pipeline_timeouts(void);
+
 /*
  * Row softmax, max-subtracted.  [P1] softmax_rows(in, out, rows, cols); [P2]
  * softmax_rows(x); [P4] softmax(..., axis) on the last axis.

@@ -27,6 +27,7 @@ _F = ctypes.c_float
 SIGNATURES = {
     "rowops_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "rowops_kernel_launches": ([], ctypes.c_uint64),
+    "rowops_pipeline_timeouts": ([], ctypes.c_uint32),
     "rowops_softmax_fwd": ([_P, _P, _I64, _I64, _P], ctypes.c_int),
     "rowops_softmax_bwd": ([_P, _P, _P, _I64, _I64, _P], ctypes.c_int),
     "rowops_attn_softmax_fwd": ([_P, _P, _I64, _I64, _I64, _F, _P], ctypes.c_int),

@@ -79,6 +79,15 @@ cudaError_t launch_softmax_fwd(const float* x, float* y, int64_t rows, int64_t c
 // Returns false (nothing launched) when the row exceeds its capacity.
 bool launch_softmax_fwd_long(const float* x, float* y, int64_t rows, int64_t cols,
                              cudaStream_t stream, cudaError_t* err);
+// TMA-streamed long rows (tma_rows.cu): vectorised rows only; each returns
+// false, launching nothing, when the shape does not suit it (too short, or the
+// row does not fit in shared memory where it must stay resident).
+bool launch_lse_tma(const float* x, float* lse, int64_t rows, int64_t cols, cudaStream_t stream,
+                    cudaError_t* err);
+bool launch_ce_tma(const float* x, const int32_t* targets, float* grad, float* row_loss, int64_t rows,
+                   int64_t cols, float grad_scale, cudaStream_t stream, cudaError_t* err);
+bool launch_softmax_tma(const float* x, float* y, int64_t rows, int64_t cols, cudaStream_t stream,
+                        cudaError_t* err);
 cudaError_t launch_softmax_bwd(const float* y, const float* dy, float* dx, int64_t rows,
                                int64_t cols, bool vec4, cudaStream_t stream);
 cudaError_t launch_attn_fwd(const float* s, float* p, int64_t rows, int64_t cols, int64_t seq_len,

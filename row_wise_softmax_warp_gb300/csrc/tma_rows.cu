@@ -1,0 +1,335 @@
+// tma_rows.cu - long rows (logsumexp, softmax cross-entropy, softmax forward)
+// streamed through shared memory by the Tensor Memory Accelerator.
+//
+// One persistent CTA per SM walks rows blockIdx.x, blockIdx.x + gridDim.x, ...
+// Warp 0 is the producer: one lane issues bulk copies (cp.async.bulk, global ->
+// shared, completion counted on an mbarrier) of row chunks into a ring of
+// `nslot` slots.  Warps 1..16 are consumers:
+//   phase A  waits for each chunk and folds it into a running (max, sum exp);
+//            the 16 warps then merge their pairs in warp order (an mbarrier
+//            rendezvous, double-buffered by row parity);
+//   phase B  (cross-entropy, softmax) re-reads the chunks, still resident in
+//            shared memory, writes the gradient / probabilities straight to
+//            global memory and releases each slot to the producer.
+// For logsumexp a slot is released right after phase A, so the ring streams
+// continuously; for cross-entropy and softmax the ring holds the whole row
+// (nslot * chunk >= cols), and the next row's chunks are loaded as soon as the
+// current row's gradient has been written from them.  HBM sees exactly one read
+// of every input element and one write of every output element.
+//
+// exp(x - m) is evaluated as 2^(x*log2(e) - m*log2(e)) with the ex2.approx
+// instruction (one FFMA and one MUFU per element).
+//
+// Every wait is bounded: a wait that runs out (which only a bug could cause)
+// raises an abort flag that all waits of the CTA watch, counts one timeout in
+// g_pipeline_timeouts and makes every thread leave; the producer first waits,
+// again bounded, for the copies it has in flight.
+#include "common.cuh"
+#include "launch.h"
+#include "../../include/rowops.h"
+
+namespace rowops {
+
+__device__ unsigned int g_pipeline_timeouts;
+
+namespace {
+
+constexpr int kConsumerWarps = 16;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kTmaThreads = kConsumers + 32;
+constexpr int kMaxSlots = 16;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr uint32_t kWaitPolls = 1u << 22;
+
+enum class RowOp { kLse, kCe, kSoftmax };
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for the phase with the given parity; false on timeout or abort.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+    for (uint32_t i = 0; i < kWaitPolls; ++i) {
+        if (mbar_test(bar, parity)) return true;
+        if (*abort_flag) return false;
+    }
+    return false;
+}
+
+__device__ __forceinline__ void bulk_load(float* dst, const float* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Running (max, sum 2^((x - max) log2 e)) over a float4.
+__device__ __forceinline__ void push4(float& m, float& s, const float4 v) {
+    const float mx = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+    if (mx > m) {
+        s *= ex2((m - mx) * kLog2e);  // m = -inf gives 0
+        m = mx;
+    }
+    const float ml = m * kLog2e;
+    s += ex2(fmaf(v.x, kLog2e, -ml)) + ex2(fmaf(v.y, kLog2e, -ml)) + ex2(fmaf(v.z, kLog2e, -ml)) +
+         ex2(fmaf(v.w, kLog2e, -ml));
+}
+
+__device__ __forceinline__ void merge2(float& m, float& s, float m2, float s2) {
+    const float mm = fmaxf(m, m2);
+    if (mm == -INFINITY) return;
+    s = s * ex2((m - mm) * kLog2e) + s2 * ex2((m2 - mm) * kLog2e);
+    m = mm;
+}
+
+__device__ void raise_abort(volatile int* abort_flag) {
+    if (!*abort_flag) {
+        *abort_flag = 1;
+        atomicAdd(&g_pipeline_timeouts, 1u);
+    }
+}
+
+template <RowOp OP>
+__global__ void __launch_bounds__(kTmaThreads, 1)
+tma_rows(const float* x, float* out, const int32_t* __restrict__ targets, float* __restrict__ aux,
+         int64_t rows, int cols, int chunk, int nslot, float grad_scale) {
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    float* buf = reinterpret_cast<float*>(smem_raw);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + size_t(nslot) * chunk * sizeof(float));
+    uint64_t* empty = full + nslot;
+    __shared__ uint64_t red_bar[2];
+    __shared__ float red[2][kConsumerWarps][2];
+    __shared__ volatile int abort_flag;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int nch = (cols + chunk - 1) / chunk;
+
+    if (tid == 0) {
+        for (int s = 0; s < nslot; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumerWarps);
+        }
+        mbar_init(&red_bar[0], kConsumerWarps);
+        mbar_init(&red_bar[1], kConsumerWarps);
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        // ------------------------------------------------------- producer
+        if (lane != 0) return;
+        uint64_t n = 0;
+        bool ok = true;
+        for (int64_t row = blockIdx.x; ok && row < rows; row += gridDim.x) {
+            const float* src = x + row * int64_t(cols);
+            for (int k = 0; k < nch; ++k, ++n) {
+                const int s = int(n % nslot);
+                const uint64_t use = n / nslot;
+                if (use > 0 && !mbar_wait(&empty[s], uint32_t((use - 1) & 1), &abort_flag)) {
+                    raise_abort(&abort_flag);
+                    ok = false;
+                    break;
+                }
+                const int cnt = min(chunk, cols - k * chunk);
+                mbar_arrive_expect_tx(&full[s], uint32_t(cnt) * 4u);
+                bulk_load(buf + size_t(s) * chunk, src + size_t(k) * chunk, uint32_t(cnt) * 4u, &full[s]);
+            }
+        }
+        if (!ok) {
+            // Let the copies already issued land before the CTA's shared memory goes away.
+            const uint64_t first = n > uint64_t(nslot) ? n - nslot : 0;
+            for (uint64_t j = first; j < n; ++j) {
+                volatile int never = 0;
+                mbar_wait(&full[j % nslot], uint32_t((j / nslot) & 1), &never);
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------- consumers
+    const int ct = tid - 32;
+    const int cw = warp - 1;
+    uint64_t n = 0;
+    int it = 0;
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x, ++it) {
+        float m = -INFINITY, s = 0.f;
+        for (int k = 0; k < nch; ++k) {
+            const uint64_t q = n + k;
+            const int slot = int(q % nslot);
+            if (!mbar_wait(&full[slot], uint32_t((q / nslot) & 1), &abort_flag)) {
+                raise_abort(&abort_flag);
+                return;
+            }
+            const int cnt4 = min(chunk, cols - k * chunk) >> 2;
+            const float4* c4 = reinterpret_cast<const float4*>(buf + size_t(slot) * chunk);
+            for (int i = ct; i < cnt4; i += kConsumers) push4(m, s, c4[i]);
+            if constexpr (OP == RowOp::kLse) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[slot]);
+            }
+        }
+        // (max, sum) of the row: warp butterfly, then the 16 warps in order.
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            merge2(m, s, __shfl_xor_sync(kFullMask, m, o), __shfl_xor_sync(kFullMask, s, o));
+        const int par = it & 1;
+        if (lane == 0) {
+            red[par][cw][0] = m;
+            red[par][cw][1] = s;
+            mbar_arrive(&red_bar[par]);
+        }
+        if (!mbar_wait(&red_bar[par], uint32_t((it >> 1) & 1), &abort_flag)) {
+            raise_abort(&abort_flag);
+            return;
+        }
+        float M = red[par][0][0], S = red[par][0][1];
+        for (int w = 1; w < kConsumerWarps; ++w) merge2(M, S, red[par][w][0], red[par][w][1]);
+        const float ml = M * kLog2e;
+        const float lse = isinf(M) ? M : ml * kLn2 + logf(S);
+
+        if constexpr (OP == RowOp::kLse) {
+            if (ct == 0) out[row] = lse;
+        } else {
+            const float inv = 1.0f / S;
+            int t = -1;
+            if constexpr (OP == RowOp::kCe) {
+                t = __ldg(targets + row);
+                if (ct == 0) {
+                    float loss = __int_as_float(0x7fc00000);
+                    if (t >= 0 && t < cols) {
+                        const uint64_t qt = n + t / chunk;
+                        loss = lse - buf[size_t(qt % nslot) * chunk + t % chunk];
+                    }
+                    aux[row] = loss;
+                }
+            }
+            float* dst = out + row * int64_t(cols);
+            for (int k = 0; k < nch; ++k) {
+                const int slot = int((n + k) % nslot);
+                const int cnt4 = min(chunk, cols - k * chunk) >> 2;
+                const float4* c4 = reinterpret_cast<const float4*>(buf + size_t(slot) * chunk);
+                float4* d4 = reinterpret_cast<float4*>(dst + size_t(k) * chunk);
+                for (int i = ct; i < cnt4; i += kConsumers) {
+                    const float4 v = c4[i];
+                    float4 p;
+                    p.x = ex2(fmaf(v.x, kLog2e, -ml)) * inv;
+                    p.y = ex2(fmaf(v.y, kLog2e, -ml)) * inv;
+                    p.z = ex2(fmaf(v.z, kLog2e, -ml)) * inv;
+                    p.w = ex2(fmaf(v.w, kLog2e, -ml)) * inv;
+                    if constexpr (OP == RowOp::kCe) {
+                        const int j = k * chunk + 4 * i;
+                        p.x = grad_scale * (p.x - (j == t ? 1.f : 0.f));
+                        p.y = grad_scale * (p.y - (j + 1 == t ? 1.f : 0.f));
+                        p.z = grad_scale * (p.z - (j + 2 == t ? 1.f : 0.f));
+                        p.w = grad_scale * (p.w - (j + 3 == t ? 1.f : 0.f));
+                    }
+                    d4[i] = p;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[slot]);
+            }
+        }
+        n += nch;
+    }
+}
+
+int sm_count() {
+    static int cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+    if (dev < 64 && cached[dev]) return cached[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev < 64) cached[dev] = n;
+    return n;
+}
+
+constexpr size_t kMaxDynSmem = 226 * 1024;  // 227 KB per block, less room for static shared memory
+
+template <RowOp OP>
+bool launch_tma(const float* x, float* out, const int32_t* targets, float* aux, int64_t rows,
+                int64_t cols, float grad_scale, cudaStream_t stream, cudaError_t* err) {
+    if (cols < 4 || cols % 4 != 0 || cols > INT32_MAX / 2) return false;
+    int chunk, nslot;
+    if constexpr (OP == RowOp::kLse) {
+        chunk = int(cols < 4096 ? cols : 4096);
+        nslot = 8;
+    } else {
+        nslot = 8;
+        chunk = int(((cols + nslot - 1) / nslot + 3) / 4 * 4);
+        nslot = int((cols + chunk - 1) / chunk);  // whole row resident
+    }
+    const size_t smem = size_t(nslot) * chunk * sizeof(float) + 2 * size_t(nslot) * sizeof(uint64_t);
+    if (smem > kMaxDynSmem || nslot > kMaxSlots) return false;
+    const int sms = sm_count();
+    if (sms <= 0) return false;
+    auto kern = tma_rows<OP>;
+    *err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (*err != cudaSuccess) return true;
+    const int64_t grid = rows < sms ? rows : sms;
+    kern<<<unsigned(grid), kTmaThreads, smem, stream>>>(x, out, targets, aux, rows, int(cols), chunk, nslot,
+                                                         grad_scale);
+    *err = cudaGetLastError();
+    return true;
+}
+
+}  // namespace
+
+bool launch_lse_tma(const float* x, float* lse, int64_t rows, int64_t cols, cudaStream_t stream,
+                    cudaError_t* err) {
+    return launch_tma<RowOp::kLse>(x, lse, nullptr, nullptr, rows, cols, 1.f, stream, err);
+}
+
+bool launch_ce_tma(const float* x, const int32_t* targets, float* grad, float* row_loss, int64_t rows,
+                   int64_t cols, float grad_scale, cudaStream_t stream, cudaError_t* err) {
+    return launch_tma<RowOp::kCe>(x, grad, targets, row_loss, rows, cols, grad_scale, stream, err);
+}
+
+bool launch_softmax_tma(const float* x, float* y, int64_t rows, int64_t cols, cudaStream_t stream,
+                        cudaError_t* err) {
+    return launch_tma<RowOp::kSoftmax>(x, y, nullptr, nullptr, rows, cols, 1.f, stream, err);
+}
+
+}  // namespace rowops
+
+extern "C" uint32_t rowops_pipeline_timeouts(void) {
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, rowops::g_pipeline_timeouts, sizeof(v)) != cudaSuccess) return 0xffffffffu;
+    return v;
+}

@@ -68,3 +68,20 @@ def test_ce_deterministic(ro):
     b = ro.rowops_softmax_ce(x, t)
     for u, v in zip(a, b):
         assert torch.equal(u, v)
+
+
+@pytest.mark.parametrize("cols", [1028, 4096, 50304, 58000])
+def test_long_rows_many_rows_per_cta(ro, cols):
+    # more rows than SMs, so every persistent CTA walks several rows through its ring
+    c = inputs.cross_entropy(cols + 1, rows=400, cols=cols, outlier_frac=1e-3)
+    x, t = c["logits"], c["targets"]
+    xg = gpu(x)
+    check_rel(host(ro.rowops_logsumexp(xg)), oracle.logsumexp_rows(x), f"lse 400x{cols}")
+    g, rl, ml = ro.rowops_softmax_ce(xg, gpu(t), grad_scale=c["grad_scale"])
+    idx = np.arange(0, 400, 37)
+    gr, rlr, mlr = oracle.softmax_cross_entropy(x, t, c["grad_scale"])
+    check_abs(host(g)[idx], gr[idx], 2e-6 * c["grad_scale"], "ce grad")
+    check_rel(host(rl), rlr, "ce row loss")
+    y = host(ro.rowops_softmax_fwd(xg))
+    check_abs(y[idx], oracle.softmax_rows(x[idx]), 2e-6, "softmax long rows")
+    assert ro.library().rowops_pipeline_timeouts() == 0
