@@ -9,7 +9,7 @@
 #include <cmath>
 #include <cstdint>
 
-#include "../../include/rowops.h"
+#include "rowops.h"
 #include "launch.h"
 
 namespace rowops {

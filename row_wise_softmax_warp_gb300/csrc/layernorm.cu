@@ -443,7 +443,7 @@ cudaError_t launch_layernorm_bwd(const float* dy, const float* gamma, const floa
 
 #include <mutex>
 
-#include "../../include/rowops.h"
+#include "rowops.h"
 
 namespace {
 

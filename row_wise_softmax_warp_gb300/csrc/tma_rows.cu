@@ -26,7 +26,7 @@
 // again bounded, for the copies it has in flight.
 #include "common.cuh"
 #include "launch.h"
-#include "../../include/rowops.h"
+#include "rowops.h"
 
 namespace rowops {
 
