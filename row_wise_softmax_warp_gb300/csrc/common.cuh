@@ -20,6 +20,22 @@ namespace rowops {
 constexpr unsigned kFullMask = 0xffffffffu;
 constexpr int kBlockThreads = 256;
 
+constexpr float kLog2e = 1.4426950408889634f;  // log2(e)
+constexpr float kLn2 = 0.6931471805599453f;     // ln(2)
+
+// 2^x by the MUFU ex2 instruction (subnormal results flush to zero).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// exp(x - m) as 2^((x - m) * log2(e)).  The difference is taken first so that no
+// intermediate overflows for finite x and m (m * log2(e) would for |m| > 2.3e38).
+__device__ __forceinline__ float exp_shifted(float x, float m) {
+    return ex2_approx((x - m) * kLog2e);
+}
+
 // ----------------------------------------------------------------- memory
 
 template <int VEC>
@@ -93,6 +109,27 @@ template <int LANES>
 __device__ __forceinline__ int group_sum_int(int v) {
 #pragma unroll
     for (int o = LANES / 2; o > 0; o >>= 1) v += __shfl_xor_sync(kFullMask, v, o);
+    return v;
+}
+
+template <int LANES>
+__device__ __forceinline__ float group_min(float v) {
+#pragma unroll
+    for (int o = LANES / 2; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(kFullMask, v, o));
+    return v;
+}
+
+template <int LANES>
+__device__ __forceinline__ int group_min_int(int v) {
+#pragma unroll
+    for (int o = LANES / 2; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(kFullMask, v, o));
+    return v;
+}
+
+template <int LANES>
+__device__ __forceinline__ int group_max_int(int v) {
+#pragma unroll
+    for (int o = LANES / 2; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(kFullMask, v, o));
     return v;
 }
 

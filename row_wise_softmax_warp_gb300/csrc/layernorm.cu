@@ -160,7 +160,8 @@ __device__ __forceinline__ void cl_wait() {
     asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
 
-// Dynamic shared memory: red[8 warps][2][MAXC] then bpart[2][MAXC], MAXC = the
+// Dynamic shared memory: red[GPB groups][2][MAXC] (each group's column
+// partials, dgamma then dbeta) then bpart[2][MAXC] (the CTA's), MAXC = the
 // geometry's largest row.
 template <int LANES, int NV, int VEC>
 __global__ void __launch_bounds__(kBlockThreads)
@@ -171,23 +172,30 @@ ln_bwd_group(const float* __restrict__ dy, const float* __restrict__ gamma,
     namespace cg = cooperative_groups;
     constexpr int MAXC = LANES * NV * VEC;
     constexpr int GPB = kBlockThreads / LANES;
-    extern __shared__ float smem[];
-    float* red = smem;                      // [8][2][MAXC]
-    float* bpart = smem + 8 * 2 * MAXC;     // [2][MAXC]
+    extern __shared__ __align__(16) float smem[];
+    float* red = smem;
+    float* bpart = smem + GPB * 2 * MAXC;
+    // Let the dependent stage-2 kernel be scheduled now; it waits for this
+    // grid's completion before reading the workspace.
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     const int g = threadIdx.x % LANES;
     const int grp = threadIdx.x / LANES;
-    const int warp = threadIdx.x >> 5;
     const int nch = cols / VEC;
     const float inv_cols = 1.0f / float(cols);
     const int64_t r_begin = int64_t(blockIdx.x) * rows_per_cta;
     int64_t r_end = r_begin + rows_per_cta;
     if (r_end > rows) r_end = rows;
 
-    float pg[NV][VEC], pb[NV][VEC];  // this group's column partials (dgamma, dbeta)
+    float* pg = red + grp * 2 * MAXC;  // this group's dgamma partials
+    float* pb = pg + MAXC;             // and dbeta partials (lanes own disjoint columns)
 #pragma unroll
     for (int k = 0; k < NV; ++k)
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) pg[k][e] = pb[k][e] = 0.f;
+        for (int e = 0; e < VEC; ++e) {
+            const int col = (g + k * LANES) * VEC + e;
+            pg[col] = 0.f;
+            pb[col] = 0.f;
+        }
 
     for (int64_t base = r_begin; base < r_end; base += GPB) {  // block-uniform
         const int64_t row = base + grp;
@@ -215,8 +223,9 @@ ln_bwd_group(const float* __restrict__ dy, const float* __restrict__ gamma,
                 ld_chunk<VEC>(gamma + c * VEC, gm);
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) {
-                    pg[k][e] = fmaf(a[k][e], h[k][e], pg[k][e]);
-                    pb[k][e] += a[k][e];
+                    const int col = c * VEC + e;
+                    pg[col] = fmaf(a[k][e], h[k][e], pg[col]);
+                    pb[col] += a[k][e];
                     a[k][e] *= gm[e];  // g' = dy * gamma
                     s1 += a[k][e];
                     s2 = fmaf(a[k][e], h[k][e], s2);
@@ -236,31 +245,11 @@ ln_bwd_group(const float* __restrict__ dy, const float* __restrict__ gamma,
             }
         }
     }
-
-    // Groups of a warp -> warp partial (identical in every group of the warp).
-#pragma unroll
-    for (int k = 0; k < NV; ++k)
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-            pg[k][e] = across_groups_sum<LANES>(pg[k][e]);
-            pb[k][e] = across_groups_sum<LANES>(pb[k][e]);
-        }
-    if ((threadIdx.x & 31) < LANES) {
-#pragma unroll
-        for (int k = 0; k < NV; ++k)
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                const int col = (g + k * LANES) * VEC + e;
-                red[(warp * 2 + 0) * MAXC + col] = pg[k][e];
-                red[(warp * 2 + 1) * MAXC + col] = pb[k][e];
-            }
-    }
     __syncthreads();
-    // Warps -> CTA partial, warp order.
+    // Groups -> CTA partial, in group order.
     for (int i = threadIdx.x; i < 2 * MAXC; i += kBlockThreads) {
         float t = red[i];
-#pragma unroll
-        for (int w = 1; w < 8; ++w) t += red[w * 2 * MAXC + i];
+        for (int q = 1; q < GPB; ++q) t += red[q * 2 * MAXC + i];
         bpart[i] = t;
     }
     // CTAs of the cluster -> cluster partial, rank order.  Rank q adds the
@@ -343,14 +332,27 @@ ln_bwd_rowblock(const float* __restrict__ dy, const float* __restrict__ gamma,
     }
 }
 
-// Stage 2: out[i] = sum_p ws[p][i] for i in [0, 2*cols), p increasing.
+// Stage 2: out[i] = sum_p ws[p][i] for i in [0, 2*cols), p increasing.  Launched
+// as a programmatic dependent of stage 1: it may start early and waits here
+// for stage 1 to finish and its writes to be visible.  Loads are issued eight
+// at a time and added in order.
 __global__ void __launch_bounds__(kBlockThreads)
-ln_params_reduce(const float* __restrict__ ws, int64_t partials, int64_t cols,
+ln_params_reduce(const float* ws, int64_t partials, int64_t cols,
                  float* __restrict__ dgamma, float* __restrict__ dbeta) {
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
     const int64_t i = int64_t(blockIdx.x) * kBlockThreads + threadIdx.x;
     if (i >= 2 * cols) return;
+    const int64_t stride = 2 * cols;
     float t = 0.f;
-    for (int64_t p = 0; p < partials; ++p) t += ws[p * 2 * cols + i];
+    int64_t p = 0;
+    for (; p + 8 <= partials; p += 8) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = ws[(p + u) * stride + i];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) t += v[u];
+    }
+    for (; p < partials; ++p) t += ws[p * stride + i];
     if (i < cols)
         dgamma[i] = t;
     else
@@ -395,7 +397,8 @@ cudaError_t launch_layernorm_bwd(const float* dy, const float* gamma, const floa
     const bool done = with_geometry(vec4, cols, [&](auto geo) {
         using G = decltype(geo);
         constexpr int MAXC = G::LANES * G::NV * G::VEC;
-        const size_t smem = size_t(9) * 2 * MAXC * sizeof(float);
+        constexpr int GPB = kBlockThreads / G::LANES;
+        const size_t smem = size_t(GPB + 1) * 2 * MAXC * sizeof(float);
         auto kern = ln_bwd_group<G::LANES, G::NV, G::VEC>;
         err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
         if (err != cudaSuccess) return;
@@ -428,9 +431,19 @@ cudaError_t launch_layernorm_bwd(const float* dy, const float* gamma, const floa
     if (err == cudaSuccess) err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     const int64_t nb = (2 * cols + kBlockThreads - 1) / kBlockThreads;
-    ln_params_reduce<<<unsigned(nb), kBlockThreads, 0, stream>>>(ws, partials, cols, dgamma, dbeta);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(nb));
+    cfg.blockDim = dim3(kBlockThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    err = cudaLaunchKernelEx(&cfg, ln_params_reduce, static_cast<const float*>(ws), partials, cols,
+                             dgamma, dbeta);
     note_launches(2);
-    return cudaGetLastError();
+    return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 }  // namespace rowops

@@ -52,7 +52,7 @@ lse_group(const float* __restrict__ x, float* __restrict__ lse, int64_t rows, in
 #pragma unroll
             for (int k = 0; k < NV; ++k)
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) s += expf(v[k][e] - m);
+                for (int e = 0; e < VEC; ++e) s += exp_shifted(v[k][e], m);
         }
         s = group_sum<LANES>(s);
         if (live && g == 0) lse[row] = isinf(m) ? m : m + logf(s);
@@ -95,7 +95,7 @@ ce_group(const float* __restrict__ x, const int32_t* __restrict__ targets, float
         for (int k = 0; k < NV; ++k)
 #pragma unroll
             for (int e = 0; e < VEC; ++e) {
-                v[k][e] = expf(v[k][e] - m);
+                v[k][e] = exp_shifted(v[k][e], m);
                 s += v[k][e];
             }
         s = group_sum<LANES>(s);
@@ -335,11 +335,22 @@ ce_rowblock(const float* __restrict__ x, const int32_t* __restrict__ targets,
 
 // Mean of the row losses in double: each thread sums a fixed strided subset in
 // order, then a fixed tree; one block, so the order never changes.
+// Launched as a programmatic dependent of the loss kernel: it waits here for
+// that grid to finish.  Loads go out eight at a time and are added in order.
 __global__ void __launch_bounds__(1024)
-ce_mean(const float* __restrict__ row_loss, int64_t rows, double* __restrict__ mean) {
+ce_mean(const float* row_loss, int64_t rows, double* __restrict__ mean) {
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
     __shared__ double sh[1024];
     double s = 0.0;
-    for (int64_t i = threadIdx.x; i < rows; i += 1024) s += double(row_loss[i]);
+    int64_t i = threadIdx.x;
+    for (; i + 7 * 1024 < rows; i += 8 * 1024) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = row_loss[i + u * 1024];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) s += double(v[u]);
+    }
+    for (; i < rows; i += 1024) s += double(row_loss[i]);
     sh[threadIdx.x] = s;
     __syncthreads();
     for (int w = 512; w > 0; w >>= 1) {
@@ -415,9 +426,18 @@ cudaError_t launch_softmax_ce(const float* logits, const int32_t* targets, float
     }
     if (err == cudaSuccess) err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    ce_mean<<<1, 1024, 0, stream>>>(row_loss, rows, mean_loss);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(1024);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    err = cudaLaunchKernelEx(&cfg, ce_mean, static_cast<const float*>(row_loss), rows, mean_loss);
     note_launches(2);
-    return cudaGetLastError();
+    return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 // Long vectorised rows of softmax_fwd use the cluster kernel; called from

@@ -49,7 +49,7 @@ softmax_fwd_group(const float* x, float* y, int64_t rows, int cols) {
         for (int k = 0; k < NV; ++k)
 #pragma unroll
             for (int e = 0; e < VEC; ++e) {
-                v[k][e] = expf(v[k][e] - m);
+                v[k][e] = exp_shifted(v[k][e], m);
                 s += v[k][e];
             }
         s = group_sum<LANES>(s);
@@ -173,8 +173,10 @@ softmax_bwd_rowblock(const float* __restrict__ y, const float* __restrict__ dy,
 // query q = r mod seq_len; keys j <= q keep scale*s_j, keys j > q get p = +0.
 // Only the visible prefix of each row is read.
 
+// Four 256-thread blocks per SM: the register cap (64) keeps the 1024-column
+// row (32 floats per lane) spill-free and doubles the loads in flight.
 template <int LANES, int NV, int VEC>
-__global__ void __launch_bounds__(kBlockThreads)
+__global__ void __launch_bounds__(kBlockThreads, 4)
 attn_fwd_group(const float* __restrict__ s, float* __restrict__ p, int64_t rows, int cols,
                int64_t seq_len, float scale) {
     constexpr int GPB = kBlockThreads / LANES;
@@ -194,18 +196,21 @@ attn_fwd_group(const float* __restrict__ s, float* __restrict__ p, int64_t rows,
             if (live && c0 < nvis) {
                 ld_chunk<VEC>(s + off + c0, v[k]);
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) v[k][e] = (c0 + e < nvis) ? scale * v[k][e] : -INFINITY;
+                for (int e = 0; e < VEC; ++e) v[k][e] = (c0 + e < nvis) ? v[k][e] : -INFINITY;
             } else {
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) v[k][e] = -INFINITY;
             }
         }
+        // max(scale * s) = scale * max(s) for scale > 0; exp(scale*s - max) is
+        // evaluated as 2^((s - max(s)) * scale*log2(e)).
         float m = -INFINITY;
 #pragma unroll
         for (int k = 0; k < NV; ++k)
 #pragma unroll
             for (int e = 0; e < VEC; ++e) m = fmaxf(m, v[k][e]);
         m = group_max<LANES>(m);
+        const float sl = scale * kLog2e;
         float sum = 0.f;
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
@@ -213,7 +218,7 @@ attn_fwd_group(const float* __restrict__ s, float* __restrict__ p, int64_t rows,
             if (c0 < nvis) {
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) {
-                    v[k][e] = (c0 + e < nvis) ? expf(v[k][e] - m) : 0.f;
+                    v[k][e] = (c0 + e < nvis) ? ex2_approx((v[k][e] - m) * sl) : 0.f;
                     sum += v[k][e];
                 }
             } else {
@@ -275,8 +280,10 @@ attn_fwd_rowblock(const float* __restrict__ s, float* __restrict__ p, int64_t ro
 // MicroGPT CuBLASBackend::fused_attn_softmax_backward: from the output p,
 // ds = scale * p * (dp - sum_{k<=q} p_k dp_k) on the visible keys, +0 beyond.
 
+// Three 256-thread blocks per SM (register cap 85) for the 2 x 32 floats per
+// lane of a 1024-column row.
 template <int LANES, int NV, int VEC>
-__global__ void __launch_bounds__(kBlockThreads)
+__global__ void __launch_bounds__(kBlockThreads, 3)
 attn_bwd_group(const float* __restrict__ p, const float* __restrict__ dp, float* __restrict__ ds,
                int64_t rows, int cols, int64_t seq_len, float scale) {
     constexpr int GPB = kBlockThreads / LANES;
@@ -406,7 +413,7 @@ masked_group(const float* x, const uint8_t* __restrict__ mask, float* y, int64_t
         for (int k = 0; k < NV; ++k)
 #pragma unroll
             for (int e = 0; e < VEC; ++e) {
-                v[k][e] = al[k][e] ? expf(v[k][e] - m) : 0.f;
+                v[k][e] = al[k][e] ? exp_shifted(v[k][e], m) : 0.f;
                 s += v[k][e];
             }
         s = group_sum<LANES>(s);

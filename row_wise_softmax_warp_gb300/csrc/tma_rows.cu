@@ -17,8 +17,8 @@
 // current row's gradient has been written from them.  HBM sees exactly one read
 // of every input element and one write of every output element.
 //
-// exp(x - m) is evaluated as 2^(x*log2(e) - m*log2(e)) with the ex2.approx
-// instruction (one FFMA and one MUFU per element).
+// exp(x - m) is evaluated as 2^((x - m)*log2(e)) with the ex2.approx
+// instruction.
 //
 // Every wait is bounded: a wait that runs out (which only a bug could cause)
 // raises an abort flag that all waits of the CTA watch, counts one timeout in
@@ -38,8 +38,6 @@ constexpr int kConsumerWarps = 16;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kTmaThreads = kConsumers + 32;
 constexpr int kMaxSlots = 16;
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint32_t kSuspendNs = 100000;  // per try_wait
 constexpr uint32_t kWaitPolls = 1u << 15;  // with the hint: a few seconds at most
 
@@ -94,11 +92,7 @@ __device__ __forceinline__ void bulk_load(float* dst, const float* src, uint32_t
         : "memory");
 }
 
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
-    return y;
-}
+__device__ __forceinline__ float ex2(float x) { return ex2_approx(x); }
 
 // Running (max, sum 2^((x - max) log2 e)) over a float4.
 __device__ __forceinline__ void push4(float& m, float& s, const float4 v) {
@@ -107,9 +101,8 @@ __device__ __forceinline__ void push4(float& m, float& s, const float4 v) {
         s *= ex2((m - mx) * kLog2e);  // m = -inf gives 0
         m = mx;
     }
-    const float ml = m * kLog2e;
-    s += ex2(fmaf(v.x, kLog2e, -ml)) + ex2(fmaf(v.y, kLog2e, -ml)) + ex2(fmaf(v.z, kLog2e, -ml)) +
-         ex2(fmaf(v.w, kLog2e, -ml));
+    s += ex2((v.x - m) * kLog2e) + ex2((v.y - m) * kLog2e) + ex2((v.z - m) * kLog2e) +
+         ex2((v.w - m) * kLog2e);
 }
 
 __device__ __forceinline__ void merge2(float& m, float& s, float m2, float s2) {
@@ -142,6 +135,10 @@ tma_rows(const float* x, float* out, const int32_t* __restrict__ targets, float*
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const int nch = (cols + chunk - 1) / chunk;
+    if constexpr (OP == RowOp::kCe) {
+        // The mean-loss kernel may be scheduled now; it waits for this grid.
+        asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    }
 
     if (tid == 0) {
         for (int s = 0; s < nslot; ++s) {
@@ -224,8 +221,7 @@ tma_rows(const float* x, float* out, const int32_t* __restrict__ targets, float*
         }
         float M = red[par][0][0], S = red[par][0][1];
         for (int w = 1; w < kConsumerWarps; ++w) merge2(M, S, red[par][w][0], red[par][w][1]);
-        const float ml = M * kLog2e;
-        const float lse = isinf(M) ? M : ml * kLn2 + logf(S);
+        const float lse = isinf(M) ? M : M + logf(S);
 
         if constexpr (OP == RowOp::kLse) {
             if (ct == 0) out[row] = lse;
@@ -252,10 +248,10 @@ tma_rows(const float* x, float* out, const int32_t* __restrict__ targets, float*
                 for (int i = ct; i < cnt4; i += kConsumers) {
                     const float4 v = c4[i];
                     float4 p;
-                    p.x = ex2(fmaf(v.x, kLog2e, -ml)) * inv;
-                    p.y = ex2(fmaf(v.y, kLog2e, -ml)) * inv;
-                    p.z = ex2(fmaf(v.z, kLog2e, -ml)) * inv;
-                    p.w = ex2(fmaf(v.w, kLog2e, -ml)) * inv;
+                    p.x = ex2((v.x - M) * kLog2e) * inv;
+                    p.y = ex2((v.y - M) * kLog2e) * inv;
+                    p.z = ex2((v.z - M) * kLog2e) * inv;
+                    p.w = ex2((v.w - M) * kLog2e) * inv;
                     if constexpr (OP == RowOp::kCe) {
                         const int j = k * chunk + 4 * i;
                         p.x = grad_scale * (p.x - (j == t ? 1.f : 0.f));

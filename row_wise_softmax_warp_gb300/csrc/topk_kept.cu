@@ -2,18 +2,24 @@
 // kept when fewer than k entries beat it; j beats i when x_j > x_i, or when
 // neither is larger and j < i.
 //
-// Without NaN, "beats" is the strict order of the 64-bit keys
-//   K_j = (ordered_key(x_j) << 32) | (cols - 1 - j)
-// (-0 and +0 share a key; a lower index gives a larger low word), so the number
-// of entries beating i is the rank of K_i and kept_i = [K_i >= T], T being the
-// k-th largest key.  T is found exactly either by k rounds of "largest key below
-// the previous one" (k or cols-k small: rounds of the smallest key above the
-// previous one) or by a bitwise radix select on the keys.
+// Without NaN, "beats" is a strict total order: larger value first, and among
+// equal values (-0 == +0 included) the lower column.  The entries beating i are
+// then exactly those ranked above it, so kept_i = [rank_i < k].  The kernels find
+// the kept set exactly, without counting:
+//   k <= 8      k rounds of "best remaining entry": a group max of the
+//               remaining floats, then a group min of the columns holding that
+//               value (the index tie-break);
+//   cols-k <= 8 the same from the bottom (min value, highest column): the
+//               cols-k entries found are the ones dropped;
+//   otherwise   a bitwise radix select of the k-th largest 64-bit key
+//               (order-preserving value bits << 32 | cols-1-column).
 //
 // A NaN is neither larger nor smaller than anything, which makes the relation
 // intransitive; any warp (or block) that meets a NaN in its rows counts beats
 // literally, O(cols) comparisons per entry.  Either way the output equals the
 // literal compare-and-count bit for bit.
+#include <climits>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -26,29 +32,10 @@ __device__ __forceinline__ uint64_t make_key(float x, int col, int cols) {
     return (uint64_t(ordered_key(x)) << 32) | uint32_t(cols - 1 - col);
 }
 
-template <int LANES>
-__device__ __forceinline__ uint64_t group_max_u64(uint64_t v) {
-#pragma unroll
-    for (int o = LANES / 2; o > 0; o >>= 1) {
-        const uint64_t t = __shfl_xor_sync(kFullMask, v, o);
-        v = t > v ? t : v;
-    }
-    return v;
-}
-
-template <int LANES>
-__device__ __forceinline__ uint64_t group_min_u64(uint64_t v) {
-#pragma unroll
-    for (int o = LANES / 2; o > 0; o >>= 1) {
-        const uint64_t t = __shfl_xor_sync(kFullMask, v, o);
-        v = t < v ? t : v;
-    }
-    return v;
-}
-
 // Number of low-word bits that can be nonzero: cols - 1 < 2^lb.
 __device__ __forceinline__ int low_bits(int cols) { return cols <= 1 ? 0 : 32 - __clz(cols - 1); }
 
+// Group kernel (geometry of common.cuh): a group of LANES lanes owns a row.
 template <int LANES, int NV, int VEC>
 __global__ void __launch_bounds__(kBlockThreads)
 kept_group(const float* __restrict__ x, float* __restrict__ kept, int64_t rows, int cols, int k) {
@@ -63,6 +50,7 @@ kept_group(const float* __restrict__ x, float* __restrict__ kept, int64_t rows, 
         const bool live = row < rows;
         const int64_t off = (live ? row : 0) * int64_t(cols);
         float v[NV][VEC];
+        bool valid[NV][VEC];
         bool has_nan = false;
 #pragma unroll
         for (int kk = 0; kk < NV; ++kk) {
@@ -75,10 +63,12 @@ kept_group(const float* __restrict__ x, float* __restrict__ kept, int64_t rows, 
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) v[kk][e] = 0.f;
             }
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) valid[kk][e] = live && c < nch;
         }
         bool keep[NV][VEC];
         if (__any_sync(kFullMask, has_nan)) {
-            // Literal compare-and-count over the group's row (warp-uniform branch).
+            // A NaN makes "beats" intransitive: count beats literally (warp-uniform branch).
             int cnt[NV][VEC];
 #pragma unroll
             for (int kk = 0; kk < NV; ++kk)
@@ -108,70 +98,68 @@ kept_group(const float* __restrict__ x, float* __restrict__ kept, int64_t rows, 
             for (int kk = 0; kk < NV; ++kk)
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) keep[kk][e] = cnt[kk][e] < k;
-        } else {
-            uint64_t key[NV][VEC];
-            bool valid[NV][VEC];
+        } else if (k <= kMaxRounds || cols - k <= kMaxRounds) {
+            // Rounds of "best remaining entry".  Without NaN, float comparison is
+            // the order of the rule (-0 == +0 ties, broken by column): from the
+            // top, the largest value and the lowest column holding it; from the
+            // bottom, the smallest value and the highest column holding it.
+            const bool top = k <= kMaxRounds;
+            const int rounds = top ? k : cols - k;
+            bool taken[NV][VEC];
 #pragma unroll
             for (int kk = 0; kk < NV; ++kk)
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) {
-                    const int col = (g + kk * LANES) * VEC + e;
-                    valid[kk][e] = live && col < cols;
-                    key[kk][e] = make_key(v[kk][e], col, cols);
-                }
-            const int from_top = k, from_bottom = cols - k;
-            if (from_top <= kMaxRounds) {
-                // T = k-th largest key: k rounds of "largest key below the bound".
-                uint64_t bound = ~uint64_t(0);
-                for (int r = 0; r < from_top; ++r) {
-                    uint64_t best = 0;
-#pragma unroll
-                    for (int kk = 0; kk < NV; ++kk)
-#pragma unroll
-                        for (int e = 0; e < VEC; ++e)
-                            if (valid[kk][e] && key[kk][e] < bound && key[kk][e] > best) best = key[kk][e];
-                    bound = group_max_u64<LANES>(best);
-                }
-#pragma unroll
-                for (int kk = 0; kk < NV; ++kk)
-#pragma unroll
-                    for (int e = 0; e < VEC; ++e) keep[kk][e] = key[kk][e] >= bound;
-            } else if (from_bottom <= kMaxRounds) {
-                // Not kept = the cols-k smallest keys.
-                uint64_t bound = 0;
-                for (int r = 0; r < from_bottom; ++r) {
-                    uint64_t best = ~uint64_t(0);
-#pragma unroll
-                    for (int kk = 0; kk < NV; ++kk)
-#pragma unroll
-                        for (int e = 0; e < VEC; ++e)
-                            if (valid[kk][e] && (r == 0 || key[kk][e] > bound) && key[kk][e] < best)
-                                best = key[kk][e];
-                    bound = group_min_u64<LANES>(best);
-                }
+                for (int e = 0; e < VEC; ++e) taken[kk][e] = false;
+            for (int r = 0; r < rounds; ++r) {
+                float best = top ? -INFINITY : INFINITY;
 #pragma unroll
                 for (int kk = 0; kk < NV; ++kk)
 #pragma unroll
                     for (int e = 0; e < VEC; ++e)
-                        keep[kk][e] = from_bottom == 0 || key[kk][e] > bound;
-            } else {
-                // Radix select: T = max{t : #{K >= t} >= k}, built from the top bit.
-                uint64_t t = 0;
-                for (int b = 63; b >= 0; --b) {
-                    if (b < 32 && b >= lb) continue;  // low-word bits that are always 0
-                    const uint64_t cand = t | (uint64_t(1) << b);
-                    int n = 0;
-#pragma unroll
-                    for (int kk = 0; kk < NV; ++kk)
-#pragma unroll
-                        for (int e = 0; e < VEC; ++e) n += (valid[kk][e] && key[kk][e] >= cand) ? 1 : 0;
-                    if (group_sum_int<LANES>(n) >= k) t = cand;
-                }
+                        if (valid[kk][e] && !taken[kk][e])
+                            best = top ? fmaxf(best, v[kk][e]) : fminf(best, v[kk][e]);
+                best = top ? group_max<LANES>(best) : group_min<LANES>(best);
+                int pick = top ? INT_MAX : -1;
 #pragma unroll
                 for (int kk = 0; kk < NV; ++kk)
 #pragma unroll
-                    for (int e = 0; e < VEC; ++e) keep[kk][e] = key[kk][e] >= t;
+                    for (int e = 0; e < VEC; ++e) {
+                        const int col = (g + kk * LANES) * VEC + e;
+                        if (valid[kk][e] && !taken[kk][e] && v[kk][e] == best)
+                            pick = top ? min(pick, col) : max(pick, col);
+                    }
+                pick = top ? group_min_int<LANES>(pick) : group_max_int<LANES>(pick);
+#pragma unroll
+                for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) taken[kk][e] |= ((g + kk * LANES) * VEC + e) == pick;
             }
+#pragma unroll
+            for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) keep[kk][e] = top ? taken[kk][e] : !taken[kk][e];
+        } else {
+            // Radix select of the k-th largest 64-bit key (value, cols-1-col).
+            uint64_t key[NV][VEC];
+#pragma unroll
+            for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) key[kk][e] = make_key(v[kk][e], (g + kk * LANES) * VEC + e, cols);
+            uint64_t t = 0;
+            for (int b = 63; b >= 0; --b) {
+                if (b < 32 && b >= lb) continue;  // low-word bits that are always 0
+                const uint64_t cand = t | (uint64_t(1) << b);
+                int n = 0;
+#pragma unroll
+                for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) n += (valid[kk][e] && key[kk][e] >= cand) ? 1 : 0;
+                if (group_sum_int<LANES>(n) >= k) t = cand;
+            }
+#pragma unroll
+            for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) keep[kk][e] = key[kk][e] >= t;
         }
 #pragma unroll
         for (int kk = 0; kk < NV; ++kk) {
