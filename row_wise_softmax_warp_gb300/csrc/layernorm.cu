@@ -162,9 +162,10 @@ __device__ __forceinline__ void cl_wait() {
 
 // Dynamic shared memory: red[GPB groups][2][MAXC] (each group's column
 // partials, dgamma then dbeta) then bpart[2][MAXC] (the CTA's), MAXC = the
-// geometry's largest row.
+// geometry's largest row.  Four blocks per SM (at most 64 registers) keep the
+// grid (<= 512 CTAs on 4096 rows) in a single wave on 152 SMs.
 template <int LANES, int NV, int VEC>
-__global__ void __launch_bounds__(kBlockThreads)
+__global__ void __launch_bounds__(kBlockThreads, 4)
 ln_bwd_group(const float* __restrict__ dy, const float* __restrict__ gamma,
              const float* __restrict__ xhat, const float* __restrict__ inv_std,
              float* __restrict__ dx, float* __restrict__ ws, int64_t rows, int cols,

@@ -281,7 +281,10 @@ int sm_count() {
 }
 
 constexpr int64_t kMaxChunk = 16384;       // floats per bulk copy, at most
-constexpr size_t kRingBytes = 200 * 1024;   // target ring size
+constexpr size_t kRingBytes = 200 * 1024;   // target ring size (whole rows resident)
+// Streaming ring (logsumexp).  On GB300, 8192 x 50304: 3 slots of 12576 floats
+// (147 KB) ran at 0.98 of the HBM copy rate, 4 slots (one row, 196 KB) at 0.89.
+constexpr size_t kStreamRingBytes = 160 * 1024;
 constexpr size_t kMaxDynSmem = 226 * 1024;  // 227 KB per block, less room for static shared memory
 
 template <RowOp OP>
@@ -295,7 +298,7 @@ bool launch_tma(const float* x, float* out, const int32_t* targets, float* aux, 
     // cross-entropy and softmax it must hold a whole row.
     const int64_t per_row = (cols + kMaxChunk - 1) / kMaxChunk;
     const int chunk = int(((cols + per_row - 1) / per_row + 3) / 4 * 4);
-    int64_t fit = int64_t(kRingBytes) / (int64_t(chunk) * 4);
+    int64_t fit = int64_t(OP == RowOp::kLse ? kStreamRingBytes : kRingBytes) / (int64_t(chunk) * 4);
     if (fit > 8) fit = 8;
     if constexpr (OP == RowOp::kLse) {
         if (fit < 2) fit = 2;

@@ -6,6 +6,8 @@
 // equal values (-0 == +0 included) the lower column.  The entries beating i are
 // then exactly those ranked above it, so kept_i = [rank_i < k].  The kernels find
 // the kept set exactly, without counting:
+//   k <= 2      one pass keeping each lane's best two (value, column) pairs,
+//               then a butterfly merge of the pairs across the group;
 //   k <= 8      k rounds of "best remaining entry": a group max of the
 //               remaining floats, then a group min of the columns holding that
 //               value (the index tie-break);
@@ -27,6 +29,12 @@ namespace rowops {
 namespace {
 
 constexpr int kMaxRounds = 8;
+
+// (xv, xc) comes before (yv, yc) in the rule's order (no NaN): larger value,
+// or equal value (-0 == +0) and lower column.
+__device__ __forceinline__ bool beats(float xv, int xc, float yv, int yc) {
+    return xv > yv || (xv == yv && xc < yc);
+}
 
 __device__ __forceinline__ uint64_t make_key(float x, int col, int cols) {
     return (uint64_t(ordered_key(x)) << 32) | uint32_t(cols - 1 - col);
@@ -98,6 +106,50 @@ kept_group(const float* __restrict__ x, float* __restrict__ kept, int64_t rows, 
             for (int kk = 0; kk < NV; ++kk)
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) keep[kk][e] = cnt[kk][e] < k;
+        } else if (k <= 2) {
+            // Top two in one pass: each lane keeps its best two (value, column)
+            // pairs in the rule's order (its columns arrive in increasing order),
+            // then the group merges the pairs with a butterfly; every lane ends
+            // with the row's best two.
+            float m1 = -INFINITY, m2 = -INFINITY;
+            int i1 = INT_MAX, i2 = INT_MAX;
+#pragma unroll
+            for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    const float xv = v[kk][e];
+                    const int c = (g + kk * LANES) * VEC + e;
+                    if (valid[kk][e]) {
+                        if (beats(xv, c, m1, i1)) {
+                            m2 = m1; i2 = i1; m1 = xv; i1 = c;
+                        } else if (beats(xv, c, m2, i2)) {
+                            m2 = xv; i2 = c;
+                        }
+                    }
+                }
+#pragma unroll
+            for (int o = LANES / 2; o > 0; o >>= 1) {
+                const float om1 = __shfl_xor_sync(kFullMask, m1, o), om2 = __shfl_xor_sync(kFullMask, m2, o);
+                const int oi1 = __shfl_xor_sync(kFullMask, i1, o), oi2 = __shfl_xor_sync(kFullMask, i2, o);
+                if (beats(om1, oi1, m1, i1)) {
+                    if (beats(om2, oi2, m1, i1)) {
+                        m2 = om2; i2 = oi2;
+                    } else {
+                        m2 = m1; i2 = i1;
+                    }
+                    m1 = om1; i1 = oi1;
+                } else if (beats(om1, oi1, m2, i2)) {
+                    m2 = om1; i2 = oi1;
+                }
+            }
+            if (k == 1) i2 = -1;
+#pragma unroll
+            for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    const int c = (g + kk * LANES) * VEC + e;
+                    keep[kk][e] = c == i1 || c == i2;
+                }
         } else if (k <= kMaxRounds || cols - k <= kMaxRounds) {
             // Rounds of "best remaining entry".  Without NaN, float comparison is
             // the order of the rule (-0 == +0 ties, broken by column): from the
