@@ -225,17 +225,17 @@ def kernel_fingerprint():
 
 
 def recorded_traffic(op):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel sources; else None."""
-    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    """DRAM bytes per launch from the committed ncu summary (profiles/dram_traffic.md),
+    if it was taken on the current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.md")
     if not os.path.exists(p):
         return None
-    with open(p) as f:
-        d = json.load(f)
-    if d.get("kernel_fingerprint") != kernel_fingerprint():
-        return None
-    v = d.get("per_launch_bytes", {}).get(op)
-    return int(v) if v is not None else None
+    fp = kernel_fingerprint()
+    for line in open(p):
+        cells = [c.strip() for c in line.strip().strip("|").split("|")]
+        if len(cells) == 3 and cells[0] == op and cells[1].isdigit():
+            return int(cells[1]) if cells[2] == fp else None
+    return None
 
 
 def dist_setup():
