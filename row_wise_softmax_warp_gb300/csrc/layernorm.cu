@@ -333,31 +333,44 @@ ln_bwd_rowblock(const float* __restrict__ dy, const float* __restrict__ gamma,
     }
 }
 
-// Stage 2: out[i] = sum_p ws[p][i] for i in [0, 2*cols), p increasing.  Launched
-// as a programmatic dependent of stage 1: it may start early and waits here
-// for stage 1 to finish and its writes to be visible.  Loads are issued eight
-// at a time and added in order.
+// Stage 2: out[i] = sum_p ws[p][i] for i in [0, 2*cols).  A block covers 32
+// outputs with 8 warps: warp j adds partials j, j+8, j+16, ... in order (loads
+// coalesced across the 32 outputs), then thread i adds the 8 warp sums in warp
+// order; the association is fixed, so results are deterministic.  Launched as a
+// programmatic dependent of stage 1: it waits here for stage 1's writes.
 __global__ void __launch_bounds__(kBlockThreads)
 ln_params_reduce(const float* ws, int64_t partials, int64_t cols,
                  float* __restrict__ dgamma, float* __restrict__ dbeta) {
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
-    const int64_t i = int64_t(blockIdx.x) * kBlockThreads + threadIdx.x;
-    if (i >= 2 * cols) return;
+    __shared__ float part[kBlockThreads / 32][32];
+    const int lane = threadIdx.x & 31;
+    const int w = threadIdx.x >> 5;
+    const int64_t i = int64_t(blockIdx.x) * 32 + lane;
     const int64_t stride = 2 * cols;
     float t = 0.f;
-    int64_t p = 0;
-    for (; p + 8 <= partials; p += 8) {
-        float v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) v[u] = ws[(p + u) * stride + i];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) t += v[u];
+    if (i < stride) {
+        int64_t p = w;
+        for (; p + 3 * 8 < partials; p += 4 * 8) {
+            const float a = ws[p * stride + i], b = ws[(p + 8) * stride + i];
+            const float c = ws[(p + 16) * stride + i], d = ws[(p + 24) * stride + i];
+            t += a;
+            t += b;
+            t += c;
+            t += d;
+        }
+        for (; p < partials; p += 8) t += ws[p * stride + i];
     }
-    for (; p < partials; ++p) t += ws[p * stride + i];
-    if (i < cols)
-        dgamma[i] = t;
-    else
-        dbeta[i - cols] = t;
+    part[w][lane] = t;
+    __syncthreads();
+    if (w == 0 && i < stride) {
+        float r = part[0][lane];
+#pragma unroll
+        for (int q = 1; q < kBlockThreads / 32; ++q) r += part[q][lane];
+        if (i < cols)
+            dgamma[i] = r;
+        else
+            dbeta[i - cols] = r;
+    }
 }
 
 }  // namespace
@@ -431,7 +444,7 @@ cudaError_t launch_layernorm_bwd(const float* dy, const float* gamma, const floa
     }
     if (err == cudaSuccess) err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    const int64_t nb = (2 * cols + kBlockThreads - 1) / kBlockThreads;
+    const int64_t nb = (2 * cols + 31) / 32;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(nb));
     cfg.blockDim = dim3(kBlockThreads);

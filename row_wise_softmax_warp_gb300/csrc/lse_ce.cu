@@ -333,14 +333,14 @@ ce_rowblock(const float* __restrict__ x, const int32_t* __restrict__ targets,
     }
 }
 
-// Mean of the row losses in double: each thread sums a fixed strided subset in
-// order, then a fixed tree; one block, so the order never changes.
-// Launched as a programmatic dependent of the loss kernel: it waits here for
-// that grid to finish.  Loads go out eight at a time and are added in order.
+// Mean of the row losses in double.  Launched as a programmatic dependent of
+// the loss kernel: it waits here for that grid.  Thread t adds rows t, t+1024,
+// ... in order (eight loads in flight), warps reduce with a fixed xor
+// butterfly and warp 0 adds the 32 warp sums in order: one block, fixed order.
 __global__ void __launch_bounds__(1024)
 ce_mean(const float* row_loss, int64_t rows, double* __restrict__ mean) {
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
-    __shared__ double sh[1024];
+    __shared__ double part[32];
     double s = 0.0;
     int64_t i = threadIdx.x;
     for (; i + 7 * 1024 < rows; i += 8 * 1024) {
@@ -351,13 +351,15 @@ ce_mean(const float* row_loss, int64_t rows, double* __restrict__ mean) {
         for (int u = 0; u < 8; ++u) s += double(v[u]);
     }
     for (; i < rows; i += 1024) s += double(row_loss[i]);
-    sh[threadIdx.x] = s;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFullMask, s, o);
+    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = s;
     __syncthreads();
-    for (int w = 512; w > 0; w >>= 1) {
-        if (threadIdx.x < w) sh[threadIdx.x] += sh[threadIdx.x + w];
-        __syncthreads();
+    if (threadIdx.x == 0) {
+        double t = 0.0;
+        for (int w = 0; w < 32; ++w) t += part[w];
+        *mean = t / double(rows);
     }
-    if (threadIdx.x == 0) *mean = sh[0] / double(rows);
 }
 
 __global__ void fill_value(float* __restrict__ p, int64_t n, float v) {

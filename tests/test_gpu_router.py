@@ -89,3 +89,16 @@ def test_router_empty(ro):
     m = torch.empty((0, 64), dtype=torch.uint8, device="cuda")
     assert ro.rowops_masked_softmax(x, m).shape == (0, 64)
     assert ro.rowops_topk_kept(x, 2).shape == (0, 64)
+
+
+def test_kept_infinities_without_nan_rows(ro):
+    rng = np.random.default_rng(77)
+    for cols in (2, 3, 5, 64, 200, 1500):
+        x = (rng.integers(-2, 3, (64, cols)) / 2.0).astype(np.float32)
+        x[rng.random(x.shape) < 0.2] = np.inf
+        x[rng.random(x.shape) < 0.2] = -np.inf
+        x[3] = -np.inf
+        x[4] = np.inf
+        for k in sorted({1, min(2, cols), min(3, cols), max(1, cols - 1), cols}):
+            kept = host(ro.rowops_topk_kept(gpu(x), k))
+            assert np.array_equal(kept, oracle.topk_kept(x, k).astype(np.float32)), (cols, k)
