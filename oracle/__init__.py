@@ -54,6 +54,7 @@ _SIGNATURES = {
     "oracle_layernorm_backward_params": [_D, _D, _D, _D, _I64, _I64],
     "oracle_masked_softmax": [_D, _U8, _D, _I64, _I64],
     "oracle_topk_kept": [_D, _U8, _I64, _I64, _I64],
+    "oracle_top_k_rows": [_D, _D, _D, _I64, _I64, _I64, ctypes.c_int, _U8],
 }
 
 
@@ -272,3 +273,29 @@ def topk_kept(x, k: int, n_threads=None) -> np.ndarray:
     _run(_row_blocks(rows, cols * cols, n_threads),
          lambda a, b: lib.oracle_topk_kept(_p(x[a:b]), _p(kept[a:b], _U8), b - a, cols, k))
     return kept
+
+
+def top_k_rows(x, k: int, largest: bool = True, n_threads=None):
+    """Returns (values, indices) of shape (rows, k): the k largest (or smallest)
+    entries of each row in rank order (NaN above every number, equal values
+    lower column first); indices as float64 whole numbers."""
+    lib = _load()
+    x = _2d(x)
+    rows, cols = x.shape
+    values = np.empty((rows, k))
+    indices = np.empty((rows, k))
+
+    def run(a, b):
+        taken = np.empty(max(cols, 1), dtype=np.uint8)
+        lib.oracle_top_k_rows(_p(x[a:b]), _p(values[a:b]), _p(indices[a:b]), b - a, cols, k,
+                              1 if largest else 0, _p(taken, _U8))
+    _run(_row_blocks(rows, cols * max(k, 1), n_threads), run)
+    return values, indices
+
+
+def router_masked_topk(x, mask, k: int, n_threads=None):
+    """The fused MoE router: P = masked_softmax(x, mask) and the top-k kept mask
+    of P.  The kept decision is taken on P rounded to fp32, the precision in
+    which the kernel stores P.  Returns (P in float64, kept as uint8)."""
+    p = masked_softmax(x, mask, n_threads)
+    return p, topk_kept(p.astype(np.float32), k, n_threads)

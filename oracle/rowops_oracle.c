@@ -346,3 +346,47 @@ void oracle_topk_kept(const double *x, uint8_t *kept, int64_t rows, int64_t cols
         }
     }
 }
+
+/*
+ * [P1] top_k_rows(in, values, indices, rows, cols, k, largest): per row, the k
+ * largest (largest != 0) or smallest values in rank order, and their column
+ * indices as whole-number floats.  Order: NaN ranks above every number (so it
+ * comes first when selecting the largest and last when selecting the
+ * smallest); equal values (all NaNs among themselves, and -0 with +0) keep the
+ * lower column first.  Selection: k passes, each taking the best entry not yet
+ * taken.
+ */
+static int ranks_before(double a, int64_t ia, double b, int64_t ib, int largest)
+{
+    const int na = isnan(a), nb = isnan(b);
+    int a_above, b_above; /* in the value order, NaN above every number */
+    if (na || nb) {
+        a_above = na && !nb;
+        b_above = nb && !na;
+    } else {
+        a_above = a > b;
+        b_above = b > a;
+    }
+    if (a_above || b_above)
+        return largest ? a_above : b_above;
+    return ia < ib; /* equal rank: lower column first */
+}
+
+void oracle_top_k_rows(const double *x, double *values, double *indices, int64_t rows,
+                       int64_t cols, int64_t k, int largest, unsigned char *taken)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        const double *xr = x + r * cols;
+        for (int64_t j = 0; j < cols; ++j)
+            taken[j] = 0;
+        for (int64_t t = 0; t < k; ++t) {
+            int64_t best = -1;
+            for (int64_t j = 0; j < cols; ++j)
+                if (!taken[j] && (best < 0 || ranks_before(xr[j], j, xr[best], best, largest)))
+                    best = j;
+            taken[best] = 1;
+            values[r * k + t] = xr[best];
+            indices[r * k + t] = (double)best;
+        }
+    }
+}

@@ -504,4 +504,76 @@ def pin_kept_matches_torch_sort_and_argmax():
     assert np.array_equal(one, first)
 
 
+
+
+# ------------------------------------------------------------------ top_k_rows
+
+def pin_top_k_rows_golden():
+    for c in _golden("row_op_examples.json")["top_k_rows"]["cases"]:
+        v, i = oracle.top_k_rows(_f(c["x"])[None], c["k"], c["largest"])
+        want_v, want_i = _f(c["values"]), _f(c["indices"])
+        assert np.array_equal(i[0], want_i), (c["why"], i[0], want_i)
+        same = (v[0] == want_v) | (np.isnan(v[0]) & np.isnan(want_v))
+        assert same.all() and (np.signbit(v[0]) == np.signbit(want_v)).all(), c["why"]
+
+
+def _top_k_by_sorting(row, k, largest):
+    def rank(j):
+        x = row[j]
+        if np.isnan(x):
+            return (0, 0.0, j) if largest else (1, 0.0, j)
+        return (1, -x, j) if largest else (0, x, j)
+    order = sorted(range(len(row)), key=rank)[:k]
+    return np.array([row[j] for j in order]), np.array(order, dtype=np.float64)
+
+
+def pin_top_k_rows_brute_force_sort():
+    rng = _rng(28)
+    for C in (1, 2, 5, 16, 64):
+        x = rng.integers(-4, 5, (20, C)) / 2.0
+        x[rng.random(x.shape) < 0.1] = np.nan
+        x[rng.random(x.shape) < 0.05] = np.inf
+        for k in sorted({1, min(2, C), C}):
+            for largest in (True, False):
+                v, i = oracle.top_k_rows(x, k, largest)
+                for r in range(20):
+                    wv, wi = _top_k_by_sorting(list(x[r]), k, largest)
+                    assert np.array_equal(i[r], wi), (C, k, largest, r)
+                    assert ((v[r] == wv) | (np.isnan(v[r]) & np.isnan(wv))).all()
+
+
+def pin_top_k_rows_matches_torch_on_distinct_values():
+    rng = _rng(29)
+    x = rng.permutation(40 * 50).reshape(40, 50).astype(np.float64) / 7.0
+    for largest in (True, False):
+        v, i = oracle.top_k_rows(x, 6, largest)
+        tv, ti = torch.topk(torch.from_numpy(x), 6, dim=1, largest=largest, sorted=True)
+        assert np.array_equal(v, tv.numpy()) and np.array_equal(i, ti.numpy().astype(np.float64))
+
+
+def pin_top_k_rows_agrees_with_kept_mask():
+    # Without NaN both pages' rules rank by value, then lower column: the k
+    # largest are exactly the kept entries.
+    rng = _rng(30)
+    x = rng.integers(-3, 4, (30, 24)) / 4.0
+    for k in (1, 2, 5, 24):
+        _, idx = oracle.top_k_rows(x, k, True)
+        kept = oracle.topk_kept(x, k)
+        for r in range(30):
+            assert set(idx[r].astype(int)) == set(np.flatnonzero(kept[r]))
+
+
+def pin_router_composition():
+    rng = _rng(31)
+    x = rng.integers(-32, 33, (64, 64)) / 8.0
+    mask = (rng.random((64, 64)) < 0.8).astype(np.uint8)
+    mask[7] = 0
+    p, kept = oracle.router_masked_topk(x, mask, 2)
+    assert (kept.sum(axis=1) == 2).all()
+    assert np.array_equal(kept[7], np.r_[1, 1, np.zeros(62)].astype(np.uint8)), "all-blocked row keeps columns 0, 1"
+    p32 = p.astype(np.float32)
+    for r in range(64):
+        assert np.array_equal(kept[r], _kept_by_sorting(list(p32[r].astype(np.float64)), 2))
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

@@ -54,6 +54,10 @@ MUTANTS = [
     ("kept_tie_direction", "if (larger || (neither && j < i))", "if (larger || (neither && j > i))"),
     ("kept_ties_ignored", "if (larger || (neither && j < i))", "if (larger)"),
     ("kept_count_bound", "            kr[i] = beaten_by < k ? 1 : 0;", "            kr[i] = beaten_by <= k ? 1 : 0;"),
+    ("top_k_tie_direction", "    return ia < ib; /* equal rank: lower column first */", "    return ia > ib;"),
+    ("top_k_nan_below", "        a_above = na && !nb;\n        b_above = nb && !na;", "        a_above = nb && !na;\n        b_above = na && !nb;"),
+    ("top_k_largest_flag_ignored", "        return largest ? a_above : b_above;", "        return a_above;"),
+    ("top_k_index_column", "            indices[r * k + t] = (double)best;", "            indices[r * k + t] = (double)t;"),
     ("kept_larger_or_equal", "                const int larger = xr[j] > xr[i];", "                const int larger = xr[j] >= xr[i];"),
 ]
 
