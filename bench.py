@@ -66,6 +66,15 @@ def algorithmic_bytes():
     }
 
 
+def next_bytes():
+    """Algorithmic bytes of the ops reported beside the step."""
+    r5, c5, k = 262144, 64, 2
+    return {
+        "router_masked_topk": (13 * r5 * c5, r5),       # x, mask read; p, kept written
+        "top_k_rows": (4 * r5 * c5 + 8 * r5 * k, r5),   # x read; values, indices written
+    }
+
+
 def make_inputs():
     from row_wise_softmax_warp_gb300 import inputs
     return {
@@ -128,6 +137,21 @@ class Ops:
                                                         grad_scale=self.cgs)),
             ("masked_softmax", lambda: ro.rowops_masked_softmax(self.rx, self.rm, self.rp)),
             ("topk_kept", lambda: ro.rowops_topk_kept(self.rp, self.k, self.rk)),
+        ]
+
+    def next_table(self):
+        """Ops beyond the step (reported separately): the fused router on the
+        router workload and top_k_rows (k = 2, largest) on its logits."""
+        ro = self.ro
+        if not hasattr(self, "fp"):
+            import torch
+            self.fp, self.fk = torch.empty_like(self.rx), torch.empty_like(self.rx)
+            shape = (self.rx.shape[0], self.k)
+            self.tv = torch.empty(shape, device=self.rx.device)
+            self.ti = torch.empty(shape, device=self.rx.device)
+        return [
+            ("router_masked_topk", lambda: ro.rowops_router_masked_topk(self.rx, self.rm, self.k, self.fp, self.fk)),
+            ("top_k_rows", lambda: ro.rowops_top_k_rows(self.rx, self.k, True, self.tv, self.ti)),
         ]
 
     def e2e_io(self):
@@ -322,6 +346,25 @@ def gpu_leg(args):
     step_ms_local = sum(per_op_ms.values())
     wall_ms_local = outer0.elapsed_time(outer1) / K
 
+    # ------------------------------------------- ops beyond the step
+    nxt = ops.next_table()
+    for _, fn in nxt:
+        for _ in range(3):
+            flush.zero_()
+            fn()
+    next_ms = {}
+    for name, fn in nxt:
+        ts = []
+        for _ in range(max(5, min(K, 20))):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            ts.append((a, b))
+        torch.cuda.synchronize()
+        next_ms[name] = sum(a.elapsed_time(b) for a, b in ts) / len(ts)
+
     # ------------------------------------------------------------ e2e
     # Same calls, inputs from pinned host memory and outputs back to pinned host
     # memory inside the timed region.  Transfers run on two copy streams (one
@@ -422,6 +465,10 @@ def gpu_leg(args):
                      "traffic": recorded_traffic(top)},
         "ops": breakdown,
         "gpu_launches": int(launches),
+        "next_ops": {n: {"ms": round(next_ms[n], 5), "alg_bytes": next_bytes()[n][0],
+                         "GB/s": round(next_bytes()[n][0] / (next_ms[n] * 1e-3) / 1e9, 1),
+                         "frac_of_measured": round(next_bytes()[n][0] / (next_ms[n] * 1e-3) / 1e9 / peak, 4)}
+                     for n in next_ms},
         "e2e": {"value": round(world * total_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "ms_per_step": round(e2e_ms, 3), "steps": ke},

@@ -241,6 +241,35 @@ size_t rowops_layernorm_bwd_noalloc_max_bytes(void);
 int rowops_topk_kept(const float *x, float *kept, int64_t rows, int64_t cols, int64_t k,
                      rowops_stream stream);
 
+/*
+ * Fused MoE router: hard-masked softmax and the top-k kept mask of its output in
+ * one pass.  [P3] hard-masked softmax followed by [P3] kept mask (Spec.MoE.kept)
+ * on the probabilities.
+ *   p = rowops_masked_softmax(x, mask);  kept = rowops_topk_kept(p, k)
+ * computed together: p is stored and the mask is decided on the same fp32
+ * values, so both outputs equal the two separate calls bit for bit, while p is
+ * never read back (13 instead of 17 bytes of HBM traffic per element).
+ * x, p, kept: rows x cols fp32; mask: rows x cols bytes.  p may be exactly x;
+ * kept must not overlap x, mask or p.  1 <= k <= cols, else ROWOPS_ERR_SHAPE.
+ */
+int rowops_router_masked_topk(const float *x, const uint8_t *mask, float *p, float *kept,
+                              int64_t rows, int64_t cols, int64_t k, rowops_stream stream);
+
+/*
+ * Per-row top k values and their columns.  [P1] top_k_rows(in, values, indices,
+ * rows, cols, k, largest).
+ *   values[i][r], indices[i][r]: the entry of row i ranked r (0-based) among the
+ *   k largest (largest != 0) or smallest, its column as a whole-number float.
+ * Rank order: NaN ranks above every number (first for largest, last for
+ * smallest); equal values (NaNs among themselves, -0 with +0) keep the lower
+ * column first.  The output values are the input's bits (sign of zero and NaN
+ * payload kept).  x: rows x cols; values, indices: rows x k.  Requires
+ * 1 <= k <= cols <= 2^24 ([P1] precondition), else ROWOPS_ERR_SHAPE.  Outputs
+ * must not overlap x or each other.  Exact (selection only).
+ */
+int rowops_top_k_rows(const float *x, float *values, float *indices, int64_t rows, int64_t cols,
+                      int64_t k, int largest, rowops_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -17,8 +17,10 @@ from .binding import (  # noqa: F401
     rowops_layernorm_fwd,
     rowops_logsumexp,
     rowops_masked_softmax,
+    rowops_router_masked_topk,
     rowops_softmax_bwd,
     rowops_softmax_ce,
     rowops_softmax_fwd,
+    rowops_top_k_rows,
     rowops_topk_kept,
 )

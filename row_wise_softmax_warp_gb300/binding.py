@@ -40,6 +40,8 @@ SIGNATURES = {
     "rowops_layernorm_bwd": ([_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P, ctypes.c_size_t, _P],
                              ctypes.c_int),
     "rowops_topk_kept": ([_P, _P, _I64, _I64, _I64, _P], ctypes.c_int),
+    "rowops_router_masked_topk": ([_P, _P, _P, _P, _I64, _I64, _I64, _P], ctypes.c_int),
+    "rowops_top_k_rows": ([_P, _P, _P, _I64, _I64, _I64, ctypes.c_int, _P], ctypes.c_int),
     "rowops_layernorm_bwd_noalloc": ([_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P], ctypes.c_int),
     "rowops_layernorm_bwd_noalloc_max_bytes": ([], ctypes.c_size_t),
 }
@@ -233,6 +235,30 @@ def rowops_topk_kept(x, k, kept=None, stream=None):
     _check(library().rowops_topk_kept(x.data_ptr(), kept.data_ptr(), rows, cols, k,
                                       _stream(x, stream)))
     return kept
+
+
+def rowops_router_masked_topk(x, mask, k, p=None, kept=None, stream=None):
+    """Fused router: returns (p, kept) = (masked softmax of x, top-k kept mask of p)."""
+    x = _mat(x, "x")
+    mask = _mat(mask, "mask", torch.uint8)
+    p = _out(p, x, "p")
+    kept = _out(kept, x, "kept")
+    rows, cols = _shape(x)
+    _check(library().rowops_router_masked_topk(x.data_ptr(), mask.data_ptr(), p.data_ptr(), kept.data_ptr(),
+                                               rows, cols, k, _stream(x, stream)))
+    return p, kept
+
+
+def rowops_top_k_rows(x, k, largest=True, values=None, indices=None, stream=None):
+    """Returns (values, indices), each (rows, k): the k largest (or smallest) entries
+    of every row in rank order (NaN above every number; ties by lower column)."""
+    x = _mat(x, "x")
+    rows, cols = _shape(x)
+    values = _out(values, x, "values", shape=(*x.shape[:-1], k))
+    indices = _out(indices, x, "indices", shape=(*x.shape[:-1], k))
+    _check(library().rowops_top_k_rows(x.data_ptr(), values.data_ptr(), indices.data_ptr(), rows, cols, k,
+                                       1 if largest else 0, _stream(x, stream)))
+    return values, indices
 
 
 def rowops_layernorm_bwd_noalloc(dy, gamma, xhat, inv_std, dx=None, dgamma=None, dbeta=None, stream=None):

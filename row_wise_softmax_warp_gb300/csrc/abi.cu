@@ -220,4 +220,35 @@ int rowops_topk_kept(const float* x, float* kept, int64_t rows, int64_t cols, in
     return to_status(rowops::launch_topk_kept(x, kept, rows, cols, k, vec4, st(stream)));
 }
 
+int rowops_router_masked_topk(const float* x, const uint8_t* mask, float* p, float* kept, int64_t rows,
+                              int64_t cols, int64_t k, rowops_stream stream) {
+    if (int e = check_dims(rows, cols)) return e;
+    if (k < 1 || k > cols) return ROWOPS_ERR_SHAPE;
+    if (rows == 0) return ROWOPS_OK;
+    if (!x || !mask || !p || !kept) return ROWOPS_ERR_NULL;
+    const int64_t n = rows * cols * 4;
+    if (static_cast<const void*>(x) != p && overlap({x, n}, {p, n})) return ROWOPS_ERR_ALIAS;
+    if (overlap({mask, rows * cols}, {p, n}) || overlap({mask, rows * cols}, {x, n}) ||
+        overlap({kept, n}, {x, n}) || overlap({kept, n}, {p, n}) || overlap({kept, n}, {mask, rows * cols}))
+        return ROWOPS_ERR_ALIAS;
+    const bool vec4 = cols % 4 == 0 && aligned(x, 16) && aligned(p, 16) && aligned(kept, 16) &&
+                      aligned(mask, 4);
+    return to_status(rowops::launch_router(x, mask, p, kept, rows, cols, k, vec4, st(stream)));
+}
+
+int rowops_top_k_rows(const float* x, float* values, float* indices, int64_t rows, int64_t cols,
+                      int64_t k, int largest, rowops_stream stream) {
+    if (int e = check_dims(rows, cols)) return e;
+    if (k < 1 || k > cols || cols > (int64_t(1) << 24)) return ROWOPS_ERR_SHAPE;
+    if (rows == 0) return ROWOPS_OK;
+    if (!x || !values || !indices) return ROWOPS_ERR_NULL;
+    const int64_t n = rows * cols * 4, nk = rows * k * 4;
+    if (overlap({values, nk}, {x, n}) || overlap({indices, nk}, {x, n}) ||
+        overlap({values, nk}, {indices, nk}))
+        return ROWOPS_ERR_ALIAS;
+    const bool vec4 = cols % 4 == 0 && aligned(x, 16);
+    return to_status(rowops::launch_top_k_rows(x, values, indices, rows, cols, k, largest != 0, vec4,
+                                               st(stream)));
+}
+
 }  // extern "C"

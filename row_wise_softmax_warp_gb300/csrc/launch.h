@@ -110,6 +110,10 @@ cudaError_t launch_layernorm_bwd(const float* dy, const float* gamma, const floa
                                  const float* inv_std, float* dx, float* dgamma, float* dbeta,
                                  int64_t rows, int64_t cols, float* workspace, bool vec4,
                                  cudaStream_t stream);
+cudaError_t launch_router(const float* x, const uint8_t* mask, float* p, float* kept, int64_t rows,
+                          int64_t cols, int64_t k, bool vec4, cudaStream_t stream);
+cudaError_t launch_top_k_rows(const float* x, float* values, float* indices, int64_t rows, int64_t cols,
+                              int64_t k, bool largest, bool vec4, cudaStream_t stream);
 cudaError_t launch_topk_kept(const float* x, float* kept, int64_t rows, int64_t cols, int64_t k,
                              bool vec4, cudaStream_t stream);
 

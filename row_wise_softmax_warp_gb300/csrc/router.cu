@@ -1,0 +1,306 @@
+// router.cu - the fused MoE router (hard-masked softmax and the top-k kept
+// mask of its output in one pass) and pulsatrix top_k_rows (the k largest or
+// smallest values of each row in rank order, with their columns).
+//
+// router_group: a lane group holds a row (geometry of common.cuh), computes
+// P = masked softmax exactly as masked_group does, stores it, and runs the
+// kept-mask selection (kept_core.cuh) on the same fp32 registers, so the mask
+// equals rowops_topk_kept applied to the stored P, bit for bit, while P is
+// never read back from HBM (13 bytes per element instead of 9 + 8).
+//
+// top_k_rows: the order is a strict total order on (key, column) with key the
+// order-preserving uint32 of the value, NaN mapped above +inf and -0 onto +0;
+// k rounds each pick the best remaining key (max for largest, min for
+// smallest) and the lowest column holding it.
+#include "common.cuh"
+#include "kept_core.cuh"
+#include "launch.h"
+
+namespace rowops {
+namespace {
+
+template <int LANES, int NV, int VEC>
+__global__ void __launch_bounds__(kBlockThreads)
+router_group(const float* x, const uint8_t* __restrict__ mask, float* p, float* __restrict__ kept,
+             int64_t rows, int cols, int k) {
+    constexpr int GPB = kBlockThreads / LANES;
+    const int g = threadIdx.x % LANES;
+    const int grp = threadIdx.x / LANES;
+    const int nch = cols / VEC;
+    for (int64_t base = int64_t(blockIdx.x) * GPB; base < rows; base += int64_t(gridDim.x) * GPB) {
+        const int64_t row = base + grp;
+        const bool live = row < rows;
+        const int64_t off = (live ? row : 0) * int64_t(cols);
+        float v[NV][VEC];
+        bool al[NV][VEC], valid[NV][VEC];
+#pragma unroll
+        for (int kk = 0; kk < NV; ++kk) {
+            const int c = g + kk * LANES;
+            if (live && c < nch) {
+                ld_chunk_coherent<VEC>(x + off + c * VEC, v[kk]);  // p may be x
+                ld_mask<VEC>(mask + off + c * VEC, al[kk]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) al[kk][e] = false;
+            }
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) valid[kk][e] = live && c < nch;
+        }
+        // Hard-masked softmax (the arithmetic of masked_group).
+        float m = -INFINITY;
+        int n_allowed = 0;
+#pragma unroll
+        for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e)
+                if (al[kk][e]) {
+                    m = fmaxf(m, v[kk][e]);
+                    ++n_allowed;
+                }
+        m = group_max<LANES>(m);
+        n_allowed = group_sum_int<LANES>(n_allowed);
+        float s = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                v[kk][e] = al[kk][e] ? exp_shifted(v[kk][e], m) : 0.f;
+                s += v[kk][e];
+            }
+        s = group_sum<LANES>(s);
+        const float inv = n_allowed > 0 ? 1.0f / s : 0.f;
+        bool has_nan = false;
+#pragma unroll
+        for (int kk = 0; kk < NV; ++kk) {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                v[kk][e] = al[kk][e] ? v[kk][e] * inv : 0.f;  // the stored probabilities
+                has_nan |= valid[kk][e] && isnan(v[kk][e]);
+            }
+            const int c = g + kk * LANES;
+            if (live && c < nch) st_chunk<VEC>(p + off + c * VEC, v[kk]);
+        }
+        // Top-k kept mask of those probabilities.
+        bool keep[NV][VEC];
+        kept_select<LANES, NV, VEC>(v, valid, __any_sync(kFullMask, has_nan), cols, k, keep);
+#pragma unroll
+        for (int kk = 0; kk < NV; ++kk) {
+            const int c = g + kk * LANES;
+            if (live && c < nch) {
+                float o[VEC];
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) o[e] = keep[kk][e] ? 1.f : 0.f;
+                st_chunk<VEC>(kept + off + c * VEC, o);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------ top_k_rows
+
+__device__ __forceinline__ uint32_t rank_key(float x) {
+    return isnan(x) ? 0xffffffffu : ordered_key(x);
+}
+
+template <int LANES>
+__device__ __forceinline__ uint32_t group_max_u32(uint32_t v) {
+#pragma unroll
+    for (int o = LANES / 2; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(kFullMask, v, o));
+    return v;
+}
+
+template <int LANES>
+__device__ __forceinline__ uint32_t group_min_u32(uint32_t v) {
+#pragma unroll
+    for (int o = LANES / 2; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(kFullMask, v, o));
+    return v;
+}
+
+template <int LANES, int NV, int VEC>
+__global__ void __launch_bounds__(kBlockThreads)
+top_k_rows_group(const float* __restrict__ x, float* __restrict__ values, float* __restrict__ indices,
+                 int64_t rows, int cols, int k, int largest) {
+    constexpr int GPB = kBlockThreads / LANES;
+    const int g = threadIdx.x % LANES;
+    const int grp = threadIdx.x / LANES;
+    const int leader = (threadIdx.x & 31) - g;
+    const int nch = cols / VEC;
+    for (int64_t base = int64_t(blockIdx.x) * GPB; base < rows; base += int64_t(gridDim.x) * GPB) {
+        const int64_t row = base + grp;
+        const bool live = row < rows;
+        const int64_t off = (live ? row : 0) * int64_t(cols);
+        float v[NV][VEC];
+        uint32_t key[NV][VEC];
+        bool avail[NV][VEC];
+#pragma unroll
+        for (int kk = 0; kk < NV; ++kk) {
+            const int c = g + kk * LANES;
+            if (live && c < nch) {
+                ld_chunk<VEC>(x + off + c * VEC, v[kk]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) v[kk][e] = 0.f;
+            }
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                key[kk][e] = rank_key(v[kk][e]);
+                avail[kk][e] = live && c < nch;
+            }
+        }
+        for (int r = 0; r < k; ++r) {
+            uint32_t best = largest ? 0u : 0xffffffffu;
+#pragma unroll
+            for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+                for (int e = 0; e < VEC; ++e)
+                    if (avail[kk][e]) best = largest ? max(best, key[kk][e]) : min(best, key[kk][e]);
+            best = largest ? group_max_u32<LANES>(best) : group_min_u32<LANES>(best);
+            int pick = INT_MAX;
+            float val = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    const int col = (g + kk * LANES) * VEC + e;
+                    if (avail[kk][e] && key[kk][e] == best && col < pick) {
+                        pick = col;
+                        val = v[kk][e];
+                    }
+                }
+            const int gpick = group_min_int<LANES>(pick);
+            // The lane that holds the picked column passes its value to lane 0.
+            const int owner = (gpick / VEC) % LANES;
+            val = __shfl_sync(kFullMask, val, leader + owner);
+#pragma unroll
+            for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+                for (int e = 0; e < VEC; ++e)
+                    if ((g + kk * LANES) * VEC + e == gpick) avail[kk][e] = false;
+            if (live && g == 0) {
+                values[row * int64_t(k) + r] = val;
+                indices[row * int64_t(k) + r] = float(gpick);
+            }
+        }
+    }
+}
+
+// Any length and alignment: one block per row, k rounds of block reductions
+// over the row re-read from global memory (L1/L2); round r takes the best entry
+// ranked strictly after round r-1's pick.
+template <int VEC>
+__global__ void __launch_bounds__(kBlockThreads)
+top_k_rows_rowblock(const float* __restrict__ x, float* __restrict__ values, float* __restrict__ indices,
+                    int64_t rows, int cols, int k, int largest) {
+    __shared__ uint32_t red[kBlockThreads / 32];
+    __shared__ int redi[kBlockThreads / 32];
+    const int nch = cols / VEC;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const float* xr = x + row * int64_t(cols);
+        float* vr = values + row * int64_t(k);
+        float* ir = indices + row * int64_t(k);
+        // The previous pick bounds the next: (key, column) strictly after it.
+        uint32_t prev_key = 0;
+        int prev_col = -1;
+        for (int r = 0; r < k; ++r) {
+            uint32_t best = largest ? 0u : 0xffffffffu;
+            int best_col = INT_MAX;
+            for (int c = threadIdx.x; c < nch; c += kBlockThreads) {
+                float t[VEC];
+                ld_chunk<VEC>(xr + c * VEC, t);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    const uint32_t kx = rank_key(t[e]);
+                    const int col = c * VEC + e;
+                    bool after;  // strictly after the previous pick in rank order
+                    if (r == 0)
+                        after = true;
+                    else if (largest)
+                        after = kx < prev_key || (kx == prev_key && col > prev_col);
+                    else
+                        after = kx > prev_key || (kx == prev_key && col > prev_col);
+                    const bool better = largest ? (kx > best || (kx == best && col < best_col))
+                                                : (kx < best || (kx == best && col < best_col));
+                    if (after && better) {
+                        best = kx;
+                        best_col = col;
+                    }
+                }
+            }
+            // block argbest: (key, column) in rank order
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const uint32_t ok = __shfl_xor_sync(kFullMask, best, o);
+                const int oc = __shfl_xor_sync(kFullMask, best_col, o);
+                const bool take = largest ? (ok > best || (ok == best && oc < best_col))
+                                          : (ok < best || (ok == best && oc < best_col));
+                if (take) {
+                    best = ok;
+                    best_col = oc;
+                }
+            }
+            if (lane == 0) {
+                red[w] = best;
+                redi[w] = best_col;
+            }
+            __syncthreads();
+            uint32_t bk = red[0];
+            int bc = redi[0];
+            for (int q = 1; q < kBlockThreads / 32; ++q) {
+                const bool take = largest ? (red[q] > bk || (red[q] == bk && redi[q] < bc))
+                                          : (red[q] < bk || (red[q] == bk && redi[q] < bc));
+                if (take) {
+                    bk = red[q];
+                    bc = redi[q];
+                }
+            }
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                vr[r] = __ldg(xr + bc);
+                ir[r] = float(bc);
+            }
+            prev_key = bk;
+            prev_col = bc;
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_router(const float* x, const uint8_t* mask, float* p, float* kept, int64_t rows,
+                          int64_t cols, int64_t k, bool vec4, cudaStream_t stream) {
+    const bool done = with_geometry(vec4, cols, [&](auto geo) {
+        using G = decltype(geo);
+        router_group<G::LANES, G::NV, G::VEC><<<group_grid(rows, G::LANES), kBlockThreads, 0, stream>>>(
+            x, mask, p, kept, rows, int(cols), int(k));
+    });
+    if (done) {
+        note_launches(1);
+        return cudaGetLastError();
+    }
+    // Rows longer than a warp holds: the two ops one after the other.
+    cudaError_t err = launch_masked_softmax(x, mask, p, rows, cols, vec4, stream);
+    if (err != cudaSuccess) return err;
+    return launch_topk_kept(p, kept, rows, cols, k, vec4, stream);
+}
+
+cudaError_t launch_top_k_rows(const float* x, float* values, float* indices, int64_t rows, int64_t cols,
+                              int64_t k, bool largest, bool vec4, cudaStream_t stream) {
+    const bool done = with_geometry(vec4, cols, [&](auto geo) {
+        using G = decltype(geo);
+        top_k_rows_group<G::LANES, G::NV, G::VEC><<<group_grid(rows, G::LANES), kBlockThreads, 0, stream>>>(
+            x, values, indices, rows, int(cols), int(k), largest ? 1 : 0);
+    });
+    if (!done) {
+        if (vec4)
+            top_k_rows_rowblock<4><<<row_grid(rows), kBlockThreads, 0, stream>>>(x, values, indices, rows,
+                                                                                 int(cols), int(k), largest);
+        else
+            top_k_rows_rowblock<1><<<row_grid(rows), kBlockThreads, 0, stream>>>(x, values, indices, rows,
+                                                                                 int(cols), int(k), largest);
+    }
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace rowops

@@ -2,46 +2,17 @@
 // kept when fewer than k entries beat it; j beats i when x_j > x_i, or when
 // neither is larger and j < i.
 //
-// Without NaN, "beats" is a strict total order: larger value first, and among
-// equal values (-0 == +0 included) the lower column.  The entries beating i are
-// then exactly those ranked above it, so kept_i = [rank_i < k].  The kernels find
-// the kept set exactly, without counting:
-//   k <= 2      one pass keeping each lane's best two (value, column) pairs,
-//               then a butterfly merge of the pairs across the group;
-//   k <= 8      k rounds of "best remaining entry": a group max of the
-//               remaining floats, then a group min of the columns holding that
-//               value (the index tie-break);
-//   cols-k <= 8 the same from the bottom (min value, highest column): the
-//               cols-k entries found are the ones dropped;
-//   otherwise   a bitwise radix select of the k-th largest 64-bit key
-//               (order-preserving value bits << 32 | cols-1-column).
-//
-// A NaN is neither larger nor smaller than anything, which makes the relation
-// intransitive; any warp (or block) that meets a NaN in its rows counts beats
-// literally, O(cols) comparisons per entry.  Either way the output equals the
-// literal compare-and-count bit for bit.
-#include <climits>
-
+// The selection itself (exact for every input, NaN included) is in
+// kept_core.cuh; this file holds the kernels that load rows and store the mask.
 #include "common.cuh"
+#include "kept_core.cuh"
 #include "launch.h"
 
 namespace rowops {
 namespace {
 
-constexpr int kMaxRounds = 8;
-
-// (xv, xc) comes before (yv, yc) in the rule's order (no NaN): larger value,
-// or equal value (-0 == +0) and lower column.
-__device__ __forceinline__ bool beats(float xv, int xc, float yv, int yc) {
-    return xv > yv || (xv == yv && xc < yc);
-}
-
-__device__ __forceinline__ uint64_t make_key(float x, int col, int cols) {
-    return (uint64_t(ordered_key(x)) << 32) | uint32_t(cols - 1 - col);
-}
-
-// Number of low-word bits that can be nonzero: cols - 1 < 2^lb.
-__device__ __forceinline__ int low_bits(int cols) { return cols <= 1 ? 0 : 32 - __clz(cols - 1); }
+using kept_detail::low_bits;
+using kept_detail::make_key;
 
 // Group kernel (geometry of common.cuh): a group of LANES lanes owns a row.
 template <int LANES, int NV, int VEC>
@@ -50,9 +21,7 @@ kept_group(const float* __restrict__ x, float* __restrict__ kept, int64_t rows, 
     constexpr int GPB = kBlockThreads / LANES;
     const int g = threadIdx.x % LANES;
     const int grp = threadIdx.x / LANES;
-    const int leader = (threadIdx.x & 31) - g;
     const int nch = cols / VEC;
-    const int lb = low_bits(cols);
     for (int64_t base = int64_t(blockIdx.x) * GPB; base < rows; base += int64_t(gridDim.x) * GPB) {
         const int64_t row = base + grp;
         const bool live = row < rows;
@@ -75,144 +44,7 @@ kept_group(const float* __restrict__ x, float* __restrict__ kept, int64_t rows, 
             for (int e = 0; e < VEC; ++e) valid[kk][e] = live && c < nch;
         }
         bool keep[NV][VEC];
-        if (__any_sync(kFullMask, has_nan)) {
-            // A NaN makes "beats" intransitive: count beats literally (warp-uniform branch).
-            int cnt[NV][VEC];
-#pragma unroll
-            for (int kk = 0; kk < NV; ++kk)
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) cnt[kk][e] = 0;
-#pragma unroll
-            for (int ko = 0; ko < NV; ++ko)
-#pragma unroll
-                for (int eo = 0; eo < VEC; ++eo)
-                    for (int o = 0; o < LANES; ++o) {
-                        const float xj = __shfl_sync(kFullMask, v[ko][eo], leader + o);
-                        const int j = (o + ko * LANES) * VEC + eo;
-                        if (j < cols) {
-#pragma unroll
-                            for (int kk = 0; kk < NV; ++kk)
-#pragma unroll
-                                for (int e = 0; e < VEC; ++e) {
-                                    const int i = (g + kk * LANES) * VEC + e;
-                                    const float xi = v[kk][e];
-                                    const bool larger = xj > xi;
-                                    const bool neither = !(xj > xi) && !(xi > xj);
-                                    cnt[kk][e] += (larger || (neither && j < i)) ? 1 : 0;
-                                }
-                        }
-                    }
-#pragma unroll
-            for (int kk = 0; kk < NV; ++kk)
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) keep[kk][e] = cnt[kk][e] < k;
-        } else if (k <= 2) {
-            // Top two in one pass: each lane keeps its best two (value, column)
-            // pairs in the rule's order (its columns arrive in increasing order),
-            // then the group merges the pairs with a butterfly; every lane ends
-            // with the row's best two.
-            float m1 = -INFINITY, m2 = -INFINITY;
-            int i1 = INT_MAX, i2 = INT_MAX;
-#pragma unroll
-            for (int kk = 0; kk < NV; ++kk)
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) {
-                    const float xv = v[kk][e];
-                    const int c = (g + kk * LANES) * VEC + e;
-                    if (valid[kk][e]) {
-                        if (beats(xv, c, m1, i1)) {
-                            m2 = m1; i2 = i1; m1 = xv; i1 = c;
-                        } else if (beats(xv, c, m2, i2)) {
-                            m2 = xv; i2 = c;
-                        }
-                    }
-                }
-#pragma unroll
-            for (int o = LANES / 2; o > 0; o >>= 1) {
-                const float om1 = __shfl_xor_sync(kFullMask, m1, o), om2 = __shfl_xor_sync(kFullMask, m2, o);
-                const int oi1 = __shfl_xor_sync(kFullMask, i1, o), oi2 = __shfl_xor_sync(kFullMask, i2, o);
-                if (beats(om1, oi1, m1, i1)) {
-                    if (beats(om2, oi2, m1, i1)) {
-                        m2 = om2; i2 = oi2;
-                    } else {
-                        m2 = m1; i2 = i1;
-                    }
-                    m1 = om1; i1 = oi1;
-                } else if (beats(om1, oi1, m2, i2)) {
-                    m2 = om1; i2 = oi1;
-                }
-            }
-            if (k == 1) i2 = -1;
-#pragma unroll
-            for (int kk = 0; kk < NV; ++kk)
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) {
-                    const int c = (g + kk * LANES) * VEC + e;
-                    keep[kk][e] = c == i1 || c == i2;
-                }
-        } else if (k <= kMaxRounds || cols - k <= kMaxRounds) {
-            // Rounds of "best remaining entry".  Without NaN, float comparison is
-            // the order of the rule (-0 == +0 ties, broken by column): from the
-            // top, the largest value and the lowest column holding it; from the
-            // bottom, the smallest value and the highest column holding it.
-            const bool top = k <= kMaxRounds;
-            const int rounds = top ? k : cols - k;
-            bool taken[NV][VEC];
-#pragma unroll
-            for (int kk = 0; kk < NV; ++kk)
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) taken[kk][e] = false;
-            for (int r = 0; r < rounds; ++r) {
-                float best = top ? -INFINITY : INFINITY;
-#pragma unroll
-                for (int kk = 0; kk < NV; ++kk)
-#pragma unroll
-                    for (int e = 0; e < VEC; ++e)
-                        if (valid[kk][e] && !taken[kk][e])
-                            best = top ? fmaxf(best, v[kk][e]) : fminf(best, v[kk][e]);
-                best = top ? group_max<LANES>(best) : group_min<LANES>(best);
-                int pick = top ? INT_MAX : -1;
-#pragma unroll
-                for (int kk = 0; kk < NV; ++kk)
-#pragma unroll
-                    for (int e = 0; e < VEC; ++e) {
-                        const int col = (g + kk * LANES) * VEC + e;
-                        if (valid[kk][e] && !taken[kk][e] && v[kk][e] == best)
-                            pick = top ? min(pick, col) : max(pick, col);
-                    }
-                pick = top ? group_min_int<LANES>(pick) : group_max_int<LANES>(pick);
-#pragma unroll
-                for (int kk = 0; kk < NV; ++kk)
-#pragma unroll
-                    for (int e = 0; e < VEC; ++e) taken[kk][e] |= ((g + kk * LANES) * VEC + e) == pick;
-            }
-#pragma unroll
-            for (int kk = 0; kk < NV; ++kk)
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) keep[kk][e] = top ? taken[kk][e] : !taken[kk][e];
-        } else {
-            // Radix select of the k-th largest 64-bit key (value, cols-1-col).
-            uint64_t key[NV][VEC];
-#pragma unroll
-            for (int kk = 0; kk < NV; ++kk)
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) key[kk][e] = make_key(v[kk][e], (g + kk * LANES) * VEC + e, cols);
-            uint64_t t = 0;
-            for (int b = 63; b >= 0; --b) {
-                if (b < 32 && b >= lb) continue;  // low-word bits that are always 0
-                const uint64_t cand = t | (uint64_t(1) << b);
-                int n = 0;
-#pragma unroll
-                for (int kk = 0; kk < NV; ++kk)
-#pragma unroll
-                    for (int e = 0; e < VEC; ++e) n += (valid[kk][e] && key[kk][e] >= cand) ? 1 : 0;
-                if (group_sum_int<LANES>(n) >= k) t = cand;
-            }
-#pragma unroll
-            for (int kk = 0; kk < NV; ++kk)
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) keep[kk][e] = key[kk][e] >= t;
-        }
+        kept_select<LANES, NV, VEC>(v, valid, __any_sync(kFullMask, has_nan), cols, k, keep);
 #pragma unroll
         for (int kk = 0; kk < NV; ++kk) {
             const int c = g + kk * LANES;

@@ -128,6 +128,19 @@ def test_layernorm_workspace(lib):
     assert lib.rowops_layernorm_bwd(A, B, C, D, E, F, G, 0, 768, None, 0, None) == OK
 
 
+def test_router_and_top_k_rules(lib):
+    assert lib.rowops_router_masked_topk(A, B, C, D, 4, 8, 0, None) == SHAPE
+    assert lib.rowops_router_masked_topk(A, B, C, D, 4, 8, 9, None) == SHAPE
+    assert lib.rowops_router_masked_topk(A, B, C, C, 4, 8, 2, None) == ALIAS   # kept == p
+    assert lib.rowops_router_masked_topk(A, B, A + 4, D, 4, 8, 2, None) == ALIAS  # p overlaps x partially
+    assert lib.rowops_router_masked_topk(A, None, C, D, 4, 8, 2, None) == NULL
+    assert lib.rowops_top_k_rows(A, B, C, 4, 8, 9, 1, None) == SHAPE
+    assert lib.rowops_top_k_rows(A, B, C, 4, (1 << 24) + 4, 2, 1, None) == SHAPE
+    assert lib.rowops_top_k_rows(A, B, B, 4, 8, 2, 1, None) == ALIAS
+    assert lib.rowops_top_k_rows(A, None, C, 4, 8, 2, 0, None) == NULL
+    assert lib.rowops_top_k_rows(A, B, C, 0, 8, 2, 0, None) == OK
+
+
 def test_rejected_calls_launch_nothing(lib):
     n0 = lib.rowops_kernel_launches()
     lib.rowops_topk_kept(A, A, 16, 64, 2, None)

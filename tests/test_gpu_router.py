@@ -102,3 +102,63 @@ def test_kept_infinities_without_nan_rows(ro):
         for k in sorted({1, min(2, cols), min(3, cols), max(1, cols - 1), cols}):
             kept = host(ro.rowops_topk_kept(gpu(x), k))
             assert np.array_equal(kept, oracle.topk_kept(x, k).astype(np.float32)), (cols, k)
+
+
+# ------------------------------------------------------------ fused router
+
+def test_router_fused_full_workload(ro):
+    r = inputs.router(0)
+    x, mask = r["x"], r["mask"]
+    p, kept = ro.rowops_router_masked_topk(gpu(x), gpu(mask), r["k"])
+    pr, keptr = oracle.router_masked_topk(x, mask, r["k"])
+    check_probs(host(p), pr, "router p")
+    check_exact_zero(host(p), mask == 0, "router blocked")
+    assert np.array_equal(host(kept), keptr.astype(np.float32))
+    # bit-identical to the two separate ops
+    p2 = ro.rowops_masked_softmax(gpu(x), gpu(mask))
+    k2 = ro.rowops_topk_kept(p2, r["k"])
+    assert torch.equal(p, p2) and torch.equal(kept, k2)
+
+
+@pytest.mark.parametrize("cols", [1, 3, 8, 33, 64, 256, 1024, 1100])
+@pytest.mark.parametrize("misalign", [False, True])
+def test_router_shapes(ro, cols, misalign):
+    r = inputs.router(cols, rows=64, cols=cols, p_allow=0.7, blocked_row_frac=0.05)
+    x, mask = r["x"], r["mask"]
+    for k in sorted({1, min(2, cols), min(5, cols), cols}):
+        p, kept = ro.rowops_router_masked_topk(gpu(x, misalign), gpu(mask, misalign), k)
+        pr, keptr = oracle.router_masked_topk(x, mask, k)
+        check_probs(host(p), pr, f"router p cols={cols}")
+        assert np.array_equal(host(kept), keptr.astype(np.float32)), (cols, k, misalign)
+
+
+# --------------------------------------------------------------- top_k_rows
+
+def _same_bits(a, b):
+    return np.array_equal(np.asarray(a, np.float32).view(np.uint32), np.asarray(b, np.float32).view(np.uint32)) \
+        or (np.array_equal(np.isnan(a), np.isnan(b)) and np.array_equal(np.where(np.isnan(a), 0, a).view(np.uint32),
+                                                                         np.where(np.isnan(b), 0, b).view(np.uint32)))
+
+
+@pytest.mark.parametrize("cols", [1, 2, 5, 16, 64, 100, 256, 1024, 1500])
+@pytest.mark.parametrize("misalign", [False, True])
+def test_top_k_rows_exact(ro, cols, misalign):
+    rng = np.random.default_rng(cols + 7)
+    x = (rng.integers(-6, 7, (37, cols)) / 4.0).astype(np.float32)
+    x[x == 0] = np.where(rng.random(int((x == 0).sum())) < 0.5, 0.0, -0.0).astype(np.float32)
+    x[rng.random(x.shape) < 0.05] = np.nan
+    x[rng.random(x.shape) < 0.03] = np.inf
+    x[rng.random(x.shape) < 0.03] = -np.inf
+    for k in sorted({1, min(2, cols), min(7, cols), cols}):
+        for largest in (True, False):
+            v, i = ro.rowops_top_k_rows(gpu(x, misalign), k, largest)
+            vr, ir = oracle.top_k_rows(x, k, largest)
+            assert np.array_equal(host(i), ir.astype(np.float32)), (cols, k, largest)
+            assert _same_bits(host(v), vr.astype(np.float32)), (cols, k, largest)
+
+
+def test_top_k_rows_router_logits(ro):
+    r = inputs.router(1, rows=20000)
+    v, i = ro.rowops_top_k_rows(gpu(r["x"]), 2, True)
+    vr, ir = oracle.top_k_rows(r["x"], 2, True)
+    assert np.array_equal(host(i), ir.astype(np.float32)) and np.array_equal(host(v), vr.astype(np.float32))
