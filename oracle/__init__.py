@@ -55,6 +55,9 @@ _SIGNATURES = {
     "oracle_masked_softmax": [_D, _U8, _D, _I64, _I64],
     "oracle_topk_kept": [_D, _U8, _I64, _I64, _I64],
     "oracle_top_k_rows": [_D, _D, _D, _I64, _I64, _I64, ctypes.c_int, _U8],
+    "oracle_rms_norm_forward": [_D, _D, _D, _D, _I64, _I64, ctypes.c_double],
+    "oracle_rms_norm_backward": [_D, _D, _D, _D, _D, _D, _I64, _I64],
+    "oracle_column_sums": [_D, _D, _I64, _I64, ctypes.c_double],
 }
 
 
@@ -299,3 +302,40 @@ def router_masked_topk(x, mask, k: int, n_threads=None):
     which the kernel stores P.  Returns (P in float64, kept as uint8)."""
     p = masked_softmax(x, mask, n_threads)
     return p, topk_kept(p.astype(np.float32), k, n_threads)
+
+
+def rms_norm_forward(x, gamma, eps: float, n_threads=None):
+    """Returns (out, row_rms)."""
+    lib = _load()
+    x = _2d(x)
+    rows, cols = x.shape
+    gamma = _f64(gamma).reshape(cols)
+    out, rms = np.empty_like(x), np.empty(rows)
+    _run(_row_blocks(rows, cols, n_threads),
+         lambda a, b: lib.oracle_rms_norm_forward(_p(x[a:b]), _p(gamma), _p(out[a:b]), _p(rms[a:b]), b - a,
+                                                  cols, eps))
+    return out, rms
+
+
+def rms_norm_backward(g, gamma, x, row_rms, n_threads=None):
+    """Returns (dx, gamma_terms)."""
+    lib = _load()
+    g, x = _2d(g), _2d(x)
+    rows, cols = g.shape
+    gamma = _f64(gamma).reshape(cols)
+    r = _f64(row_rms).reshape(rows)
+    dx, gt = np.empty_like(g), np.empty_like(g)
+    _run(_row_blocks(rows, cols, n_threads),
+         lambda a, b: lib.oracle_rms_norm_backward(_p(g[a:b]), _p(gamma), _p(x[a:b]), _p(r[a:b]), _p(dx[a:b]),
+                                                   _p(gt[a:b]), b - a, cols))
+    return dx, gt
+
+
+def column_sums(m, out=None, beta: float = 0.0):
+    """out_j = beta * out_j + sum_i m_ij (rows in increasing order, one thread)."""
+    lib = _load()
+    m = _2d(m)
+    rows, cols = m.shape
+    o = np.zeros(cols) if out is None else _f64(out).reshape(cols).copy()
+    lib.oracle_column_sums(_p(m), _p(o), rows, cols, beta)
+    return o

@@ -390,3 +390,63 @@ void oracle_top_k_rows(const double *x, double *values, double *indices, int64_t
         }
     }
 }
+
+/*
+ * [P1] rms_norm_forward(in, gamma, out, row_rms, rows, cols, eps):
+ *   rms_i = sqrt((1/C) sum_j x_ij^2 + eps),  out_ij = gamma_j * x_ij / rms_i.
+ * The cached per-row statistic is rms_i itself ([P1] row_rms).
+ */
+void oracle_rms_norm_forward(const double *x, const double *gamma, double *out, double *row_rms,
+                             int64_t rows, int64_t cols, double eps)
+{
+    for (int64_t i = 0; i < rows; ++i) {
+        const double *xi = x + i * cols;
+        double ss = 0.0;
+        for (int64_t j = 0; j < cols; ++j)
+            ss += xi[j] * xi[j];
+        const double rms = sqrt(ss / (double)cols + eps);
+        row_rms[i] = rms;
+        for (int64_t j = 0; j < cols; ++j)
+            out[i * cols + j] = gamma[j] * xi[j] / rms;
+    }
+}
+
+/*
+ * [P1] rms_norm_backward(grad_out, gamma, in, row_rms, grad_in, gamma_terms, ...):
+ * input gradient of the forward above, plus the per-row contributions to gamma's
+ * gradient, gamma_terms_ij = g_ij * x_ij / rms_i ([P1]: column_sums reduces them).
+ * With g' = g * gamma, y_j = gamma_j x_j / r and d r / d x_k = x_k / (C r):
+ *   dx_k = (1/r) * (g'_k - x_k * ((1/C) sum_j g'_j x_j) / r^2).
+ */
+void oracle_rms_norm_backward(const double *g, const double *gamma, const double *x,
+                              const double *row_rms, double *dx, double *gamma_terms,
+                              int64_t rows, int64_t cols)
+{
+    for (int64_t i = 0; i < rows; ++i) {
+        const double *gi = g + i * cols, *xi = x + i * cols;
+        const double r = row_rms[i];
+        double s = 0.0;
+        for (int64_t j = 0; j < cols; ++j)
+            s += gi[j] * gamma[j] * xi[j];
+        s /= (double)cols;
+        for (int64_t j = 0; j < cols; ++j) {
+            dx[i * cols + j] = (gi[j] * gamma[j] - xi[j] * s / (r * r)) / r;
+            gamma_terms[i * cols + j] = gi[j] * xi[j] / r;
+        }
+    }
+}
+
+/*
+ * [P1] column_sums(in, out, rows, cols, beta): out_j = beta * out_j + sum_i in_ij,
+ * rows summed in increasing i.  beta == 0 does not read out (a NaN there does not
+ * survive).
+ */
+void oracle_column_sums(const double *in, double *out, int64_t rows, int64_t cols, double beta)
+{
+    for (int64_t j = 0; j < cols; ++j) {
+        double s = 0.0;
+        for (int64_t i = 0; i < rows; ++i)
+            s += in[i * cols + j];
+        out[j] = (beta == 0.0 ? 0.0 : beta * out[j]) + s;
+    }
+}

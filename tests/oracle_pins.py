@@ -576,4 +576,79 @@ def pin_router_composition():
         assert np.array_equal(kept[r], _kept_by_sorting(list(p32[r].astype(np.float64)), 2))
 
 
+
+
+# --------------------------------------------------------------------- RMSNorm
+
+def pin_rms_norm_forward():
+    x, gamma, _, _ = _ln_case(32, R=9, C=40)
+    for eps in (1e-6, 0.3):
+        out, rms = oracle.rms_norm_forward(x, gamma, eps)
+        ms = np.mean(x * x, axis=1)
+        _close(rms, np.sqrt(ms + eps), 1e-15, 0, "rms closed form")
+        _close(np.mean((out / gamma) ** 2, axis=1), ms / (ms + eps), 1e-12, 0, "mean square of out/gamma")
+        ref = torch.nn.functional.rms_norm(torch.from_numpy(x), (40,), torch.from_numpy(gamma), eps).numpy()
+        _close(out, ref, 1e-12, 1e-14, "torch rms_norm")
+    o1, _ = oracle.rms_norm_forward(x, gamma, 0.0)
+    o2, _ = oracle.rms_norm_forward(4.0 * x, gamma, 0.0)
+    _close(o1, o2, 1e-13, 1e-14, "scale invariance at eps=0")
+    out, rms = oracle.rms_norm_forward(np.array([[3.0, 4.0]]), np.array([1.0, 2.0]), 0.0)
+    _close(rms, [math.sqrt(12.5)], 1e-15, 0, "rms of (3, 4)")
+    _close(out[0], [3 / math.sqrt(12.5), 8 / math.sqrt(12.5)], 1e-15, 0, "out of (3, 4)")
+
+
+def pin_rms_norm_backward_finite_differences():
+    x, gamma, _, g = _ln_case(33, R=3, C=6)
+    eps = 1e-3
+    out, rms = oracle.rms_norm_forward(x, gamma, eps)
+    dx, gt = oracle.rms_norm_backward(g, gamma, x, rms)
+    h = 1e-6
+
+    def loss(xx, gg):
+        return np.sum(g * oracle.rms_norm_forward(xx, gg, eps)[0])
+
+    fdx = np.zeros_like(x)
+    for i in range(3):
+        for j in range(6):
+            xp, xm = x.copy(), x.copy()
+            xp[i, j] += h
+            xm[i, j] -= h
+            fdx[i, j] = (loss(xp, gamma) - loss(xm, gamma)) / (2 * h)
+    fdg = np.zeros_like(gamma)
+    for j in range(6):
+        e = np.zeros_like(gamma)
+        e[j] = h
+        fdg[j] = (loss(x, gamma + e) - loss(x, gamma - e)) / (2 * h)
+    _close(dx, fdx, 1e-6, 1e-8, "dx")
+    _close(oracle.column_sums(gt), fdg, 1e-7, 1e-9, "column sums of gamma_terms = dgamma")
+    _close(gt, g * x / rms[:, None], 1e-15, 1e-15, "gamma_terms")
+
+
+def pin_rms_norm_backward_matches_torch_autograd():
+    x, gamma, _, g = _ln_case(34, R=6, C=80)
+    xt = torch.from_numpy(x).requires_grad_(True)
+    gt_ = torch.from_numpy(gamma).requires_grad_(True)
+    y = torch.nn.functional.rms_norm(xt, (80,), gt_, 1e-5)
+    dxr, dgr = torch.autograd.grad(y, (xt, gt_), torch.from_numpy(g))
+    _, rms = oracle.rms_norm_forward(x, gamma, 1e-5)
+    dx, terms = oracle.rms_norm_backward(g, gamma, x, rms)
+    _close(dx, dxr.numpy(), 1e-9, 1e-12, "dx")
+    _close(oracle.column_sums(terms), dgr.numpy(), 1e-11, 1e-12, "dgamma")
+    # sum_j dx_j x_j = (1/r) s C (1 - ms/r^2) = s C eps / r^3, with s = mean(g' x)
+    s = np.mean(g * gamma * x, axis=1)
+    ms = np.mean(x * x, axis=1)
+    _close((dx * x).sum(axis=1), s * 80 * 1e-5 / rms ** 3, 1e-6, 1e-12, "sum dx * x")
+
+
+def pin_column_sums():
+    rng = _rng(35)
+    m = rng.normal(0, 1, (37, 11))
+    _close(oracle.column_sums(m), [math.fsum(c) for c in m.T], 1e-15, 1e-15, "fsum")
+    prev = rng.normal(0, 1, 11)
+    _close(oracle.column_sums(m, prev, 0.5), 0.5 * prev + [math.fsum(c) for c in m.T], 1e-15, 1e-15, "beta")
+    nan_prev = np.full(11, np.nan)
+    assert not np.isnan(oracle.column_sums(m, nan_prev, 0.0)).any(), "beta = 0 does not read out"
+    assert np.array_equal(oracle.column_sums(np.zeros((0, 4))), np.zeros(4))
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

@@ -58,6 +58,13 @@ MUTANTS = [
     ("top_k_nan_below", "        a_above = na && !nb;\n        b_above = nb && !na;", "        a_above = nb && !na;\n        b_above = na && !nb;"),
     ("top_k_largest_flag_ignored", "        return largest ? a_above : b_above;", "        return a_above;"),
     ("top_k_index_column", "            indices[r * k + t] = (double)best;", "            indices[r * k + t] = (double)t;"),
+    ("rms_eps_outside_sqrt", "        const double rms = sqrt(ss / (double)cols + eps);", "        const double rms = sqrt(ss / (double)cols) + eps;"),
+    ("rms_mean_missing", "        const double rms = sqrt(ss / (double)cols + eps);", "        const double rms = sqrt(ss + eps);"),
+    ("rms_bwd_r_squared", "            dx[i * cols + j] = (gi[j] * gamma[j] - xi[j] * s / (r * r)) / r;", "            dx[i * cols + j] = (gi[j] * gamma[j] - xi[j] * s / r) / r;"),
+    ("rms_bwd_sign", "            dx[i * cols + j] = (gi[j] * gamma[j] - xi[j] * s / (r * r)) / r;", "            dx[i * cols + j] = (gi[j] * gamma[j] + xi[j] * s / (r * r)) / r;"),
+    ("rms_terms_gamma", "            gamma_terms[i * cols + j] = gi[j] * xi[j] / r;", "            gamma_terms[i * cols + j] = gi[j] * gamma[j] * xi[j] / r;"),
+    ("colsum_beta_dropped", "        out[j] = (beta == 0.0 ? 0.0 : beta * out[j]) + s;", "        out[j] = s;"),
+    ("colsum_beta_reads_out", "        out[j] = (beta == 0.0 ? 0.0 : beta * out[j]) + s;", "        out[j] = beta * out[j] + s;"),
     ("kept_larger_or_equal", "                const int larger = xr[j] > xr[i];", "                const int larger = xr[j] >= xr[i];"),
 ]
 
