@@ -69,7 +69,11 @@ def algorithmic_bytes():
 def next_bytes():
     """Algorithmic bytes of the ops reported beside the step."""
     r5, c5, k = 262144, 64, 2
+    r2, c2 = 4096, 768
     return {
+        "rmsnorm_fwd": (4 * (2 * r2 * c2 + c2 + r2), r2),         # x, gamma read; out, row_rms written
+        "rmsnorm_bwd": (4 * (4 * r2 * c2 + c2 + r2), r2),         # dy, x, gamma, row_rms; dx, terms
+        "column_sums": (4 * (r2 * c2 + c2), r2),                  # gamma_terms read; dgamma written
         "router_masked_topk": (13 * r5 * c5, r5),       # x, mask read; p, kept written
         "top_k_rows": (4 * r5 * c5 + 8 * r5 * k, r5),   # x read; values, indices written
     }
@@ -149,7 +153,17 @@ class Ops:
             shape = (self.rx.shape[0], self.k)
             self.tv = torch.empty(shape, device=self.rx.device)
             self.ti = torch.empty(shape, device=self.rx.device)
+        if not hasattr(self, "rms_out"):
+            import torch
+            self.rms_out, self.rms_r = torch.empty_like(self.lx), torch.empty(self.lx.shape[0], device=self.lx.device)
+            self.rms_dx, self.rms_t = torch.empty_like(self.lx), torch.empty_like(self.lx)
+            self.rms_dg = torch.empty_like(self.lg)
+            ro.rowops_rmsnorm_fwd(self.lx, self.lg, self.rms_out, self.rms_r, eps=self.eps)
         return [
+            ("rmsnorm_fwd", lambda: ro.rowops_rmsnorm_fwd(self.lx, self.lg, self.rms_out, self.rms_r, eps=self.eps)),
+            ("rmsnorm_bwd", lambda: ro.rowops_rmsnorm_bwd(self.ldy, self.lg, self.lx, self.rms_r, self.rms_dx,
+                                                          self.rms_t)),
+            ("column_sums", lambda: ro.rowops_column_sums(self.rms_t, self.rms_dg)),
             ("router_masked_topk", lambda: ro.rowops_router_masked_topk(self.rx, self.rm, self.k, self.fp, self.fk)),
             ("top_k_rows", lambda: ro.rowops_top_k_rows(self.rx, self.k, True, self.tv, self.ti)),
         ]

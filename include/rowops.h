@@ -16,7 +16,8 @@
  *     when an error is returned, except ROWOPS_ERR_CUDA, which reports a failed
  *     launch (the CUDA runtime's error after the launch).
  *   - rows == 0 is a successful no-op for every op (after the scalar
- *     parameters are checked).  Negative sizes, cols >= 2^31, and matrices of
+ *     parameters are checked), except rowops_column_sums, which still scales
+ *     its output by beta.  Negative sizes, cols >= 2^31, and matrices of
  *     more than 2^60 elements are ROWOPS_ERR_SHAPE.
  *   - A pointer may be NULL only when the buffer it names is empty.
  *   - Buffers must not overlap unless the entry point says so
@@ -269,6 +270,42 @@ int rowops_router_masked_topk(const float *x, const uint8_t *mask, float *p, flo
  */
 int rowops_top_k_rows(const float *x, float *values, float *indices, int64_t rows, int64_t cols,
                       int64_t k, int largest, rowops_stream stream);
+
+/*
+ * RMSNorm forward.  [P1] rms_norm_forward(in, gamma, out, row_rms, rows, cols, eps).
+ *   rms_i = sqrt(mean_j x_ij^2 + eps),  out_ij = gamma_j * x_ij / rms_i,
+ *   row_rms_i = rms_i (the cached statistic).
+ * x, out: rows x cols; gamma: cols; row_rms: rows.  cols == 0, eps < 0 or
+ * non-finite eps are ROWOPS_ERR_SHAPE.  Outputs must not overlap inputs or each
+ * other.
+ */
+int rowops_rmsnorm_fwd(const float *x, const float *gamma, float *out, float *row_rms, int64_t rows,
+                       int64_t cols, float eps, rowops_stream stream);
+
+/*
+ * RMSNorm backward.  [P1] rms_norm_backward(grad_out, gamma, in, row_rms,
+ * grad_in, gamma_terms, rows, cols).
+ *   g'_ij = dy_ij * gamma_j,  dx_ij = (g'_ij - x_ij * mean_k(g'_ik x_ik) / rms_i^2) / rms_i,
+ *   gamma_terms_ij = dy_ij * x_ij / rms_i
+ * (gamma's gradient is rowops_column_sums(gamma_terms), as [P1] intends).
+ * dy, x, dx, gamma_terms: rows x cols; gamma: cols; row_rms: rows.  cols == 0 is
+ * ROWOPS_ERR_SHAPE.  Outputs must not overlap inputs or each other.
+ */
+int rowops_rmsnorm_bwd(const float *dy, const float *gamma, const float *x, const float *row_rms,
+                       float *dx, float *gamma_terms, int64_t rows, int64_t cols,
+                       rowops_stream stream);
+
+/*
+ * Column sums.  [P1] column_sums(in, out, rows, cols, beta).
+ *   out_j = beta * out_j + sum_i in_ij;  beta == 0 does not read out.
+ * in: rows x cols; out: cols.  Deterministic: fixed blocks of consecutive rows
+ * are added in row order, then the blocks in block order (no workspace: a
+ * thread-block cluster per 32-column tile).  Exception to the common contract:
+ * rows == 0 still applies beta.  Non-finite beta is ROWOPS_ERR_SHAPE; out must not
+ * overlap in ([P1]).
+ */
+int rowops_column_sums(const float *in, float *out, int64_t rows, int64_t cols, float beta,
+                       rowops_stream stream);
 
 #ifdef __cplusplus
 }

@@ -11,12 +11,15 @@ from .binding import (  # noqa: F401
     library,
     rowops_attn_softmax_bwd,
     rowops_attn_softmax_fwd,
+    rowops_column_sums,
     rowops_kernel_launches,
     rowops_layernorm_bwd,
     rowops_layernorm_bwd_workspace,
     rowops_layernorm_fwd,
     rowops_logsumexp,
     rowops_masked_softmax,
+    rowops_rmsnorm_bwd,
+    rowops_rmsnorm_fwd,
     rowops_router_masked_topk,
     rowops_softmax_bwd,
     rowops_softmax_ce,

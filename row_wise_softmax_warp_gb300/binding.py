@@ -42,6 +42,9 @@ SIGNATURES = {
     "rowops_topk_kept": ([_P, _P, _I64, _I64, _I64, _P], ctypes.c_int),
     "rowops_router_masked_topk": ([_P, _P, _P, _P, _I64, _I64, _I64, _P], ctypes.c_int),
     "rowops_top_k_rows": ([_P, _P, _P, _I64, _I64, _I64, ctypes.c_int, _P], ctypes.c_int),
+    "rowops_rmsnorm_fwd": ([_P, _P, _P, _P, _I64, _I64, _F, _P], ctypes.c_int),
+    "rowops_rmsnorm_bwd": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _P], ctypes.c_int),
+    "rowops_column_sums": ([_P, _P, _I64, _I64, _F, _P], ctypes.c_int),
     "rowops_layernorm_bwd_noalloc": ([_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P], ctypes.c_int),
     "rowops_layernorm_bwd_noalloc_max_bytes": ([], ctypes.c_size_t),
 }
@@ -259,6 +262,39 @@ def rowops_top_k_rows(x, k, largest=True, values=None, indices=None, stream=None
     _check(library().rowops_top_k_rows(x.data_ptr(), values.data_ptr(), indices.data_ptr(), rows, cols, k,
                                        1 if largest else 0, _stream(x, stream)))
     return values, indices
+
+
+def rowops_rmsnorm_fwd(x, gamma, out=None, row_rms=None, eps=1e-5, stream=None):
+    """Returns (out, row_rms)."""
+    x, gamma = _mat(x, "x"), _mat(gamma, "gamma")
+    rows, cols = _shape(x)
+    out = _out(out, x, "out")
+    row_rms = _out(row_rms, x, "row_rms", shape=(rows,))
+    _check(library().rowops_rmsnorm_fwd(x.data_ptr(), gamma.data_ptr(), out.data_ptr(), row_rms.data_ptr(),
+                                        rows, cols, eps, _stream(x, stream)))
+    return out, row_rms
+
+
+def rowops_rmsnorm_bwd(dy, gamma, x, row_rms, dx=None, gamma_terms=None, stream=None):
+    """Returns (dx, gamma_terms); gamma's gradient is rowops_column_sums(gamma_terms)."""
+    dy, gamma, x, row_rms = _mat(dy, "dy"), _mat(gamma, "gamma"), _mat(x, "x"), _mat(row_rms, "row_rms")
+    rows, cols = _shape(dy)
+    dx = _out(dx, dy, "dx")
+    gamma_terms = _out(gamma_terms, dy, "gamma_terms")
+    _check(library().rowops_rmsnorm_bwd(dy.data_ptr(), gamma.data_ptr(), x.data_ptr(), row_rms.data_ptr(),
+                                        dx.data_ptr(), gamma_terms.data_ptr(), rows, cols, _stream(dy, stream)))
+    return dx, gamma_terms
+
+
+def rowops_column_sums(m, out=None, beta=0.0, stream=None):
+    """out_j = beta * out_j + sum_i m_ij (deterministic order)."""
+    m = _mat(m, "in")
+    rows, cols = _shape(m)
+    if out is None:
+        out = torch.zeros(cols, dtype=torch.float32, device=m.device)
+    out = _mat(out, "out")
+    _check(library().rowops_column_sums(m.data_ptr(), out.data_ptr(), rows, cols, beta, _stream(m, stream)))
+    return out
 
 
 def rowops_layernorm_bwd_noalloc(dy, gamma, xhat, inv_std, dx=None, dgamma=None, dbeta=None, stream=None):

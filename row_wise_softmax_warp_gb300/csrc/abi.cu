@@ -251,4 +251,50 @@ int rowops_top_k_rows(const float* x, float* values, float* indices, int64_t row
                                                st(stream)));
 }
 
+int rowops_rmsnorm_fwd(const float* x, const float* gamma, float* out, float* row_rms, int64_t rows,
+                       int64_t cols, float eps, rowops_stream stream) {
+    if (int e = check_dims(rows, cols)) return e;
+    if (cols == 0 || !std::isfinite(eps) || eps < 0.f) return ROWOPS_ERR_SHAPE;
+    if (rows == 0) return ROWOPS_OK;
+    if (!x || !gamma || !out || !row_rms) return ROWOPS_ERR_NULL;
+    const int64_t n = rows * cols * 4;
+    const Buf in[2] = {{x, n}, {gamma, cols * 4}};
+    const Buf o[2] = {{out, n}, {row_rms, rows * 4}};
+    for (int a = 0; a < 2; ++a)
+        for (int b = 0; b < 2; ++b)
+            if (overlap(o[a], in[b]) || (a != b && overlap(o[a], o[b]))) return ROWOPS_ERR_ALIAS;
+    const bool vec4 = cols % 4 == 0 && aligned(x, 16) && aligned(gamma, 16) && aligned(out, 16);
+    return to_status(rowops::launch_rmsnorm_fwd(x, gamma, out, row_rms, rows, cols, eps, vec4, st(stream)));
+}
+
+int rowops_rmsnorm_bwd(const float* dy, const float* gamma, const float* x, const float* row_rms, float* dx,
+                       float* gamma_terms, int64_t rows, int64_t cols, rowops_stream stream) {
+    if (int e = check_dims(rows, cols)) return e;
+    if (cols == 0) return ROWOPS_ERR_SHAPE;
+    if (rows == 0) return ROWOPS_OK;
+    if (!dy || !gamma || !x || !row_rms || !dx || !gamma_terms) return ROWOPS_ERR_NULL;
+    const int64_t n = rows * cols * 4;
+    const Buf in[4] = {{dy, n}, {gamma, cols * 4}, {x, n}, {row_rms, rows * 4}};
+    const Buf o[2] = {{dx, n}, {gamma_terms, n}};
+    for (int a = 0; a < 2; ++a) {
+        for (int b = 0; b < 4; ++b)
+            if (overlap(o[a], in[b])) return ROWOPS_ERR_ALIAS;
+    }
+    if (overlap(o[0], o[1])) return ROWOPS_ERR_ALIAS;
+    const bool vec4 = cols % 4 == 0 && aligned(dy, 16) && aligned(gamma, 16) && aligned(x, 16) &&
+                      aligned(dx, 16) && aligned(gamma_terms, 16);
+    return to_status(rowops::launch_rmsnorm_bwd(dy, gamma, x, row_rms, dx, gamma_terms, rows, cols, vec4,
+                                                st(stream)));
+}
+
+int rowops_column_sums(const float* in, float* out, int64_t rows, int64_t cols, float beta,
+                       rowops_stream stream) {
+    if (int e = check_dims(rows, cols)) return e;
+    if (!std::isfinite(beta)) return ROWOPS_ERR_SHAPE;
+    if (cols == 0) return ROWOPS_OK;
+    if (!out || (rows > 0 && !in)) return ROWOPS_ERR_NULL;
+    if (overlap({in, rows * cols * 4}, {out, cols * 4})) return ROWOPS_ERR_ALIAS;
+    return to_status(rowops::launch_column_sums(in, out, rows, cols, beta, st(stream)));
+}
+
 }  // extern "C"

@@ -114,6 +114,13 @@ cudaError_t launch_router(const float* x, const uint8_t* mask, float* p, float* 
                           int64_t cols, int64_t k, bool vec4, cudaStream_t stream);
 cudaError_t launch_top_k_rows(const float* x, float* values, float* indices, int64_t rows, int64_t cols,
                               int64_t k, bool largest, bool vec4, cudaStream_t stream);
+cudaError_t launch_rmsnorm_fwd(const float* x, const float* gamma, float* out, float* row_rms, int64_t rows,
+                               int64_t cols, float eps, bool vec4, cudaStream_t stream);
+cudaError_t launch_rmsnorm_bwd(const float* dy, const float* gamma, const float* x, const float* row_rms,
+                               float* dx, float* terms, int64_t rows, int64_t cols, bool vec4,
+                               cudaStream_t stream);
+cudaError_t launch_column_sums(const float* in, float* out, int64_t rows, int64_t cols, float beta,
+                               cudaStream_t stream);
 cudaError_t launch_topk_kept(const float* x, float* kept, int64_t rows, int64_t cols, int64_t k,
                              bool vec4, cudaStream_t stream);
 
