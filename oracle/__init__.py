@@ -58,6 +58,9 @@ _SIGNATURES = {
     "oracle_rms_norm_forward": [_D, _D, _D, _D, _I64, _I64, ctypes.c_double],
     "oracle_rms_norm_backward": [_D, _D, _D, _D, _D, _D, _I64, _I64],
     "oracle_column_sums": [_D, _D, _I64, _I64, ctypes.c_double],
+    "oracle_lrp_softmax_rows": [_D, _D, _D, _D, _I64, _I64],
+    "oracle_masked_softmax_fmask": [_D, _D, _D, _I64, _I64],
+    "oracle_argmax_onehot": [_D, _D, _I64, _I64],
 }
 
 
@@ -339,3 +342,33 @@ def column_sums(m, out=None, beta: float = 0.0):
     o = np.zeros(cols) if out is None else _f64(out).reshape(cols).copy()
     lib.oracle_column_sums(_p(m), _p(o), rows, cols, beta)
     return o
+
+
+def lrp_softmax_rows(x, y, r, n_threads=None) -> np.ndarray:
+    lib = _load()
+    x, y, r = _2d(x), _2d(y), _2d(r)
+    rows, cols = x.shape
+    out = np.empty_like(x)
+    _run(_row_blocks(rows, cols, n_threads),
+         lambda a, b: lib.oracle_lrp_softmax_rows(_p(x[a:b]), _p(y[a:b]), _p(r[a:b]), _p(out[a:b]), b - a, cols))
+    return out
+
+
+def masked_softmax_fmask(x, mask, n_threads=None) -> np.ndarray:
+    lib = _load()
+    x, m = _2d(x), _2d(mask)
+    rows, cols = x.shape
+    y = np.empty_like(x)
+    _run(_row_blocks(rows, cols, n_threads),
+         lambda a, b: lib.oracle_masked_softmax_fmask(_p(x[a:b]), _p(m[a:b]), _p(y[a:b]), b - a, cols))
+    return y
+
+
+def argmax_onehot(x, n_threads=None) -> np.ndarray:
+    lib = _load()
+    x = _2d(x)
+    rows, cols = x.shape
+    out = np.empty_like(x)
+    _run(_row_blocks(rows, cols * cols, n_threads),
+         lambda a, b: lib.oracle_argmax_onehot(_p(x[a:b]), _p(out[a:b]), b - a, cols))
+    return out

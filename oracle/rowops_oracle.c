@@ -450,3 +450,77 @@ void oracle_column_sums(const double *in, double *out, int64_t rows, int64_t col
         out[j] = (beta == 0.0 ? 0.0 : beta * out[j]) + s;
     }
 }
+
+/*
+ * [P1] lrp_softmax_rows(x, y, r, r_in, rows, cols): the SoftmaxModule relevance
+ * rule per row, r_in_j = x_j * (r_j - y_j * sum_k r_k).
+ */
+void oracle_lrp_softmax_rows(const double *x, const double *y, const double *r, double *r_in,
+                             int64_t rows, int64_t cols)
+{
+    for (int64_t i = 0; i < rows; ++i) {
+        const double *xi = x + i * cols, *yi = y + i * cols, *ri = r + i * cols;
+        double s = 0.0;
+        for (int64_t k = 0; k < cols; ++k)
+            s += ri[k];
+        for (int64_t j = 0; j < cols; ++j)
+            r_in[i * cols + j] = xi[j] * (ri[j] - yi[j] * s);
+    }
+}
+
+/*
+ * [P3] hard-masked softmax with a floating-point mask: an entry is allowed when
+ * its mask value is not zero (mask != 0.0; -0.0 blocks, NaN allows); otherwise
+ * as oracle_masked_softmax.
+ */
+void oracle_masked_softmax_fmask(const double *x, const double *mask, double *y, int64_t rows,
+                                 int64_t cols)
+{
+    for (int64_t i = 0; i < rows; ++i) {
+        const double *xi = x + i * cols, *mi = mask + i * cols;
+        double *yi = y + i * cols;
+        int64_t allowed = 0;
+        double m = -INFINITY;
+        for (int64_t j = 0; j < cols; ++j)
+            if (mi[j] != 0.0) {
+                m = fmax(m, xi[j]);
+                ++allowed;
+            }
+        if (allowed == 0) {
+            for (int64_t j = 0; j < cols; ++j)
+                yi[j] = 0.0;
+            continue;
+        }
+        double s = 0.0;
+        for (int64_t k = 0; k < cols; ++k)
+            if (mi[k] != 0.0)
+                s += exp(xi[k] - m);
+        for (int64_t j = 0; j < cols; ++j)
+            yi[j] = mi[j] != 0.0 ? exp(xi[j] - m) / s : 0.0;
+    }
+}
+
+/*
+ * [P3] first-max one-hot: 1 at the first maximal coordinate of each nonempty row,
+ * 0 elsewhere.  A coordinate is maximal when no entry of the row is larger than it
+ * (x_i > x_j holds for no i); the first maximal coordinate is the lowest such j.
+ * Without NaN this is the first index of the maximum; a NaN is never exceeded, so
+ * it is maximal too.
+ */
+void oracle_argmax_onehot(const double *x, double *out, int64_t rows, int64_t cols)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        const double *xr = x + r * cols;
+        int64_t first = -1;
+        for (int64_t j = 0; j < cols && first < 0; ++j) {
+            int exceeded = 0;
+            for (int64_t i = 0; i < cols; ++i)
+                if (xr[i] > xr[j])
+                    exceeded = 1;
+            if (!exceeded)
+                first = j;
+        }
+        for (int64_t j = 0; j < cols; ++j)
+            out[r * cols + j] = j == first ? 1.0 : 0.0;
+    }
+}

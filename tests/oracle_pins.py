@@ -651,4 +651,49 @@ def pin_column_sums():
     assert np.array_equal(oracle.column_sums(np.zeros((0, 4))), np.zeros(4))
 
 
+
+
+# ------------------------------------------- lrp softmax, float mask, argmax
+
+def pin_lrp_softmax_rows():
+    for c in _golden("row_op_examples.json")["lrp_softmax_rows"]["cases"]:
+        got = oracle.lrp_softmax_rows(_f(c["x"])[None], _f(c["y"])[None], _f(c["r"])[None])
+        _close(got[0], _f(c["r_in"]), 0, 1e-15, c["why"])
+    rng = _rng(36)
+    x = rng.normal(0, 1, (5, 9))
+    y = oracle.softmax_rows(rng.normal(0, 1, (5, 9)))
+    r1, r2 = rng.normal(0, 1, (5, 9)), rng.normal(0, 1, (5, 9))
+    _close(oracle.lrp_softmax_rows(x, y, 2 * r1 - 3 * r2),
+           2 * oracle.lrp_softmax_rows(x, y, r1) - 3 * oracle.lrp_softmax_rows(x, y, r2), 1e-13, 1e-13, "linear in r")
+    _close(oracle.lrp_softmax_rows(x, np.zeros_like(y), r1), x * r1, 1e-15, 0, "y = 0")
+    onehot = np.zeros((5, 9))
+    onehot[np.arange(5), [0, 3, 8, 2, 2]] = 1
+    _close(oracle.lrp_softmax_rows(np.ones((5, 9)), onehot, r1), r1 - onehot * r1.sum(axis=1, keepdims=True),
+           1e-14, 1e-14, "x = 1, one-hot y")
+
+
+def pin_masked_softmax_float_mask():
+    rng = _rng(37)
+    x = rng.integers(-16, 17, (30, 20)) / 4.0
+    mask = rng.choice([0.0, -0.0, 1.0, 0.25, -3.0, np.nan], size=(30, 20))
+    mask[4] = 0.0
+    y = oracle.masked_softmax_fmask(x, mask)
+    assert np.array_equal(y, oracle.masked_softmax(x, (mask != 0).astype(np.uint8)))
+    assert (y[4] == 0).all()
+
+
+def pin_argmax_onehot():
+    for c in _golden("row_op_examples.json")["argmax_onehot"]["cases"]:
+        got = oracle.argmax_onehot(_f(c["x"])[None])
+        assert np.array_equal(got[0], _f(c["out"])), c["why"]
+    rng = _rng(38)
+    x = rng.integers(-3, 4, (200, 17)) / 2.0
+    out = oracle.argmax_onehot(x)
+    ref = np.zeros_like(out)
+    ref[np.arange(200), np.argmax(x, axis=1)] = 1  # numpy: the first maximum
+    assert np.array_equal(out, ref)
+    assert np.array_equal(out, oracle.topk_kept(x, 1).astype(np.float64)), "k = 1 kept mask without NaN"
+    assert oracle.argmax_onehot(np.zeros((3, 0))).shape == (3, 0)
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

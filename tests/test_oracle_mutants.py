@@ -47,8 +47,8 @@ MUTANTS = [
     ("ln_dbeta_transposed", "            dbeta[j] += g[i * cols + j];", "            dbeta[j] += g[j * cols + i % cols];"),
     ("masked_max_over_all", "            if (mi[j] != 0) {\n                m = fmax(m, xi[j]);", "            if (1) {\n                m = fmax(m, xi[j]);"),
     ("masked_blocked_in_sum", "            if (mi[k] != 0)\n                s += exp(xi[k] - m);", "            s += exp(xi[k] - m);"),
-    ("masked_empty_row_nan", "            for (int64_t j = 0; j < cols; ++j)\n                yi[j] = 0.0;\n            continue;",
-     "            for (int64_t j = 0; j < cols; ++j)\n                yi[j] = NAN;\n            continue;"),
+    ("masked_empty_row_nan", "                ++allowed;\n            }\n        if (allowed == 0) {\n            for (int64_t j = 0; j < cols; ++j)\n                yi[j] = 0.0;\n            continue;\n        }\n        double s = 0.0;\n        for (int64_t k = 0; k < cols; ++k)\n            if (mi[k] != 0)\n",
+     "                ++allowed;\n            }\n        if (allowed == 0) {\n            for (int64_t j = 0; j < cols; ++j)\n                yi[j] = NAN;\n            continue;\n        }\n        double s = 0.0;\n        for (int64_t k = 0; k < cols; ++k)\n            if (mi[k] != 0)\n"),
     ("masked_blocked_negative_zero", "            yi[j] = mi[j] != 0 ? exp(xi[j] - m) / s : 0.0;",
      "            yi[j] = mi[j] != 0 ? exp(xi[j] - m) / s : -0.0;"),
     ("kept_tie_direction", "if (larger || (neither && j < i))", "if (larger || (neither && j > i))"),
@@ -65,6 +65,10 @@ MUTANTS = [
     ("rms_terms_gamma", "            gamma_terms[i * cols + j] = gi[j] * xi[j] / r;", "            gamma_terms[i * cols + j] = gi[j] * gamma[j] * xi[j] / r;"),
     ("colsum_beta_dropped", "        out[j] = (beta == 0.0 ? 0.0 : beta * out[j]) + s;", "        out[j] = s;"),
     ("colsum_beta_reads_out", "        out[j] = (beta == 0.0 ? 0.0 : beta * out[j]) + s;", "        out[j] = beta * out[j] + s;"),
+    ("lrp_sign", "            r_in[i * cols + j] = xi[j] * (ri[j] - yi[j] * s);", "            r_in[i * cols + j] = xi[j] * (ri[j] + yi[j] * s);"),
+    ("lrp_y_dropped", "            r_in[i * cols + j] = xi[j] * (ri[j] - yi[j] * s);", "            r_in[i * cols + j] = xi[j] * (ri[j] - s);"),
+    ("fmask_nonzero_test", "            if (mi[j] != 0.0) {\n                m = fmax(m, xi[j]);", "            if (mi[j] > 0.0) {\n                m = fmax(m, xi[j]);"),
+    ("argmax_last_max", "                if (xr[i] > xr[j])\n                    exceeded = 1;", "                if (xr[i] >= xr[j] && i != j)\n                    exceeded = 1;"),
     ("kept_larger_or_equal", "                const int larger = xr[j] > xr[i];", "                const int larger = xr[j] >= xr[i];"),
 ]
 
