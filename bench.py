@@ -74,6 +74,7 @@ def next_bytes():
         "rmsnorm_fwd": (4 * (2 * r2 * c2 + c2 + r2), r2),         # x, gamma read; out, row_rms written
         "rmsnorm_bwd": (4 * (4 * r2 * c2 + c2 + r2), r2),         # dy, x, gamma, row_rms; dx, terms
         "column_sums": (4 * (r2 * c2 + c2), r2),                  # gamma_terms read; dgamma written
+        "argmax_onehot": (8 * r5 * c5, r5),             # x read; one-hot written
         "router_masked_topk": (13 * r5 * c5, r5),       # x, mask read; p, kept written
         "top_k_rows": (4 * r5 * c5 + 8 * r5 * k, r5),   # x read; values, indices written
     }
@@ -164,6 +165,7 @@ class Ops:
             ("rmsnorm_bwd", lambda: ro.rowops_rmsnorm_bwd(self.ldy, self.lg, self.lx, self.rms_r, self.rms_dx,
                                                           self.rms_t)),
             ("column_sums", lambda: ro.rowops_column_sums(self.rms_t, self.rms_dg)),
+            ("argmax_onehot", lambda: ro.rowops_argmax_onehot(self.rx, self.fk)),
             ("router_masked_topk", lambda: ro.rowops_router_masked_topk(self.rx, self.rm, self.k, self.fp, self.fk)),
             ("top_k_rows", lambda: ro.rowops_top_k_rows(self.rx, self.k, True, self.tv, self.ti)),
         ]

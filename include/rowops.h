@@ -307,6 +307,34 @@ int rowops_rmsnorm_bwd(const float *dy, const float *gamma, const float *x, cons
 int rowops_column_sums(const float *in, float *out, int64_t rows, int64_t cols, float beta,
                        rowops_stream stream);
 
+/*
+ * Hard-masked softmax with a floating-point mask.  [P3] hard-masked softmax: an
+ * entry is allowed when its mask value is not zero (mask != 0.0f: -0.0 blocks,
+ * NaN allows); otherwise exactly rowops_masked_softmax.  mask: rows x cols fp32.
+ * y may be exactly x; any other overlap is ROWOPS_ERR_ALIAS.
+ */
+int rowops_masked_softmax_fmask(const float *x, const float *mask, float *y, int64_t rows,
+                                int64_t cols, rowops_stream stream);
+
+/*
+ * Softmax relevance rule.  [P1] lrp_softmax_rows(x, y, r, r_in, rows, cols):
+ *   r_in_ij = x_ij * (r_ij - y_ij * sum_k r_ik).
+ * x, y, r, r_in: rows x cols (y is the softmax output).  r_in must not overlap the
+ * inputs.  cols == 0 is a no-op.
+ */
+int rowops_lrp_softmax_rows(const float *x, const float *y, const float *r, float *r_in,
+                            int64_t rows, int64_t cols, rowops_stream stream);
+
+/*
+ * First-max one-hot.  [P3]: 1.0f at the first maximal coordinate of each
+ * nonempty row and 0.0f elsewhere (the input dtype).  A coordinate is maximal
+ * when no entry is larger than it, so a NaN is maximal and, without NaN, this is
+ * the first index of the maximum.  x, out: rows x cols; out must not overlap x.
+ * cols == 0 is a no-op (empty rows give an empty result).
+ */
+int rowops_argmax_onehot(const float *x, float *out, int64_t rows, int64_t cols,
+                         rowops_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

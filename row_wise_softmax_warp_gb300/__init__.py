@@ -9,6 +9,7 @@ seeded synthetic workloads and ``build`` compiles the library.
 from .binding import (  # noqa: F401
     RowopsError,
     library,
+    rowops_argmax_onehot,
     rowops_attn_softmax_bwd,
     rowops_attn_softmax_fwd,
     rowops_column_sums,
@@ -17,7 +18,9 @@ from .binding import (  # noqa: F401
     rowops_layernorm_bwd_workspace,
     rowops_layernorm_fwd,
     rowops_logsumexp,
+    rowops_lrp_softmax_rows,
     rowops_masked_softmax,
+    rowops_masked_softmax_fmask,
     rowops_rmsnorm_bwd,
     rowops_rmsnorm_fwd,
     rowops_router_masked_topk,

@@ -45,6 +45,9 @@ SIGNATURES = {
     "rowops_rmsnorm_fwd": ([_P, _P, _P, _P, _I64, _I64, _F, _P], ctypes.c_int),
     "rowops_rmsnorm_bwd": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _P], ctypes.c_int),
     "rowops_column_sums": ([_P, _P, _I64, _I64, _F, _P], ctypes.c_int),
+    "rowops_masked_softmax_fmask": ([_P, _P, _P, _I64, _I64, _P], ctypes.c_int),
+    "rowops_lrp_softmax_rows": ([_P, _P, _P, _P, _I64, _I64, _P], ctypes.c_int),
+    "rowops_argmax_onehot": ([_P, _P, _I64, _I64, _P], ctypes.c_int),
     "rowops_layernorm_bwd_noalloc": ([_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P], ctypes.c_int),
     "rowops_layernorm_bwd_noalloc_max_bytes": ([], ctypes.c_size_t),
 }
@@ -294,6 +297,35 @@ def rowops_column_sums(m, out=None, beta=0.0, stream=None):
         out = torch.zeros(cols, dtype=torch.float32, device=m.device)
     out = _mat(out, "out")
     _check(library().rowops_column_sums(m.data_ptr(), out.data_ptr(), rows, cols, beta, _stream(m, stream)))
+    return out
+
+
+def rowops_masked_softmax_fmask(x, mask, y=None, stream=None):
+    """Masked softmax with an fp32 mask (allowed where mask != 0)."""
+    x, mask = _mat(x, "x"), _mat(mask, "mask")
+    y = _out(y, x, "y")
+    rows, cols = _shape(x)
+    _check(library().rowops_masked_softmax_fmask(x.data_ptr(), mask.data_ptr(), y.data_ptr(), rows, cols,
+                                                 _stream(x, stream)))
+    return y
+
+
+def rowops_lrp_softmax_rows(x, y, r, r_in=None, stream=None):
+    """r_in = x * (r - y * sum(r)) per row."""
+    x, y, r = _mat(x, "x"), _mat(y, "y"), _mat(r, "r")
+    r_in = _out(r_in, x, "r_in")
+    rows, cols = _shape(x)
+    _check(library().rowops_lrp_softmax_rows(x.data_ptr(), y.data_ptr(), r.data_ptr(), r_in.data_ptr(), rows,
+                                             cols, _stream(x, stream)))
+    return r_in
+
+
+def rowops_argmax_onehot(x, out=None, stream=None):
+    """1.0 at the first maximal coordinate of each row, 0.0 elsewhere."""
+    x = _mat(x, "x")
+    out = _out(out, x, "out")
+    rows, cols = _shape(x)
+    _check(library().rowops_argmax_onehot(x.data_ptr(), out.data_ptr(), rows, cols, _stream(x, stream)))
     return out
 
 

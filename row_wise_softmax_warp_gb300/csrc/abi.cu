@@ -297,4 +297,39 @@ int rowops_column_sums(const float* in, float* out, int64_t rows, int64_t cols, 
     return to_status(rowops::launch_column_sums(in, out, rows, cols, beta, st(stream)));
 }
 
+int rowops_masked_softmax_fmask(const float* x, const float* mask, float* y, int64_t rows, int64_t cols,
+                                rowops_stream stream) {
+    if (int e = check_dims(rows, cols)) return e;
+    if (rows == 0 || cols == 0) return ROWOPS_OK;
+    if (!x || !mask || !y) return ROWOPS_ERR_NULL;
+    const int64_t n = rows * cols * 4;
+    if (static_cast<const void*>(x) != y && overlap({x, n}, {y, n})) return ROWOPS_ERR_ALIAS;
+    if (overlap({mask, n}, {y, n}) || overlap({mask, n}, {x, n})) return ROWOPS_ERR_ALIAS;
+    const bool vec4 = cols % 4 == 0 && aligned(x, 16) && aligned(y, 16) && aligned(mask, 16);
+    return to_status(rowops::launch_masked_softmax_fmask(x, mask, y, rows, cols, vec4, st(stream)));
+}
+
+int rowops_lrp_softmax_rows(const float* x, const float* y, const float* r, float* r_in, int64_t rows,
+                            int64_t cols, rowops_stream stream) {
+    if (int e = check_dims(rows, cols)) return e;
+    if (rows == 0 || cols == 0) return ROWOPS_OK;
+    if (!x || !y || !r || !r_in) return ROWOPS_ERR_NULL;
+    const int64_t n = rows * cols * 4;
+    if (overlap({r_in, n}, {x, n}) || overlap({r_in, n}, {y, n}) || overlap({r_in, n}, {r, n}))
+        return ROWOPS_ERR_ALIAS;
+    const bool vec4 = cols % 4 == 0 && aligned(x, 16) && aligned(y, 16) && aligned(r, 16) &&
+                      aligned(r_in, 16);
+    return to_status(rowops::launch_lrp_softmax(x, y, r, r_in, rows, cols, vec4, st(stream)));
+}
+
+int rowops_argmax_onehot(const float* x, float* out, int64_t rows, int64_t cols, rowops_stream stream) {
+    if (int e = check_dims(rows, cols)) return e;
+    if (rows == 0 || cols == 0) return ROWOPS_OK;
+    if (!x || !out) return ROWOPS_ERR_NULL;
+    const int64_t n = rows * cols * 4;
+    if (overlap({x, n}, {out, n})) return ROWOPS_ERR_ALIAS;
+    const bool vec4 = cols % 4 == 0 && aligned(x, 16) && aligned(out, 16);
+    return to_status(rowops::launch_argmax_onehot(x, out, rows, cols, vec4, st(stream)));
+}
+
 }  // extern "C"

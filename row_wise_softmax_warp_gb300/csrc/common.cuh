@@ -89,6 +89,15 @@ __device__ __forceinline__ void ld_mask(const uint8_t* p, bool (&a)[VEC]) {
     }
 }
 
+// VEC float mask values; an entry is allowed when its mask value is not 0.0.
+template <int VEC>
+__device__ __forceinline__ void ld_mask(const float* p, bool (&a)[VEC]) {
+    float m[VEC];
+    ld_chunk<VEC>(p, m);
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) a[e] = m[e] != 0.0f;
+}
+
 // ----------------------------------------------------------- group reductions
 
 template <int LANES>

@@ -121,6 +121,12 @@ cudaError_t launch_rmsnorm_bwd(const float* dy, const float* gamma, const float*
                                cudaStream_t stream);
 cudaError_t launch_column_sums(const float* in, float* out, int64_t rows, int64_t cols, float beta,
                                cudaStream_t stream);
+cudaError_t launch_masked_softmax_fmask(const float* x, const float* mask, float* y, int64_t rows,
+                                        int64_t cols, bool vec4, cudaStream_t stream);
+cudaError_t launch_lrp_softmax(const float* x, const float* y, const float* r, float* r_in, int64_t rows,
+                               int64_t cols, bool vec4, cudaStream_t stream);
+cudaError_t launch_argmax_onehot(const float* x, float* out, int64_t rows, int64_t cols, bool vec4,
+                                 cudaStream_t stream);
 cudaError_t launch_topk_kept(const float* x, float* kept, int64_t rows, int64_t cols, int64_t k,
                              bool vec4, cudaStream_t stream);
 

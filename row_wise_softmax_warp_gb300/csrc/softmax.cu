@@ -370,11 +370,12 @@ attn_bwd_rowblock(const float* __restrict__ p, const float* __restrict__ dp,
 
 // ------------------------------------------------------ hard-masked softmax
 // TorchLean hard-masked softmax: max and denominator over allowed entries
-// (mask byte != 0); blocked entries +0; a row with nothing allowed is all +0.
+// (mask value != 0: a byte mask, or a float mask where -0.0 blocks and NaN
+// allows); blocked entries +0; a row with nothing allowed is all +0.
 
-template <int LANES, int NV, int VEC>
+template <typename MaskT, int LANES, int NV, int VEC>
 __global__ void __launch_bounds__(kBlockThreads)
-masked_group(const float* x, const uint8_t* __restrict__ mask, float* y, int64_t rows, int cols) {
+masked_group(const float* x, const MaskT* __restrict__ mask, float* y, int64_t rows, int cols) {
     constexpr int GPB = kBlockThreads / LANES;
     const int g = threadIdx.x % LANES;
     const int grp = threadIdx.x / LANES;
@@ -431,9 +432,9 @@ masked_group(const float* x, const uint8_t* __restrict__ mask, float* y, int64_t
     }
 }
 
-template <int VEC>
+template <typename MaskT, int VEC>
 __global__ void __launch_bounds__(kBlockThreads)
-masked_rowblock(const float* x, const uint8_t* __restrict__ mask, float* y, int64_t rows,
+masked_rowblock(const float* x, const MaskT* __restrict__ mask, float* y, int64_t rows,
                 int64_t cols) {
     __shared__ float scratch[2 * kBlockThreads / 32];
     __shared__ int iscratch[kBlockThreads / 32];
@@ -551,21 +552,32 @@ cudaError_t launch_attn_bwd(const float* p, const float* dp, float* ds, int64_t 
     return cudaGetLastError();
 }
 
-cudaError_t launch_masked_softmax(const float* x, const uint8_t* mask, float* y, int64_t rows,
-                                  int64_t cols, bool vec4, cudaStream_t stream) {
+template <typename MaskT>
+cudaError_t launch_masked_impl(const float* x, const MaskT* mask, float* y, int64_t rows, int64_t cols,
+                               bool vec4, cudaStream_t stream) {
     const bool done = with_geometry(vec4, cols, [&](auto geo) {
         using G = decltype(geo);
-        masked_group<G::LANES, G::NV, G::VEC>
+        masked_group<MaskT, G::LANES, G::NV, G::VEC>
             <<<group_grid(rows, G::LANES), kBlockThreads, 0, stream>>>(x, mask, y, rows, int(cols));
     });
     if (!done) {
         if (vec4)
-            masked_rowblock<4><<<row_grid(rows), kBlockThreads, 0, stream>>>(x, mask, y, rows, cols);
+            masked_rowblock<MaskT, 4><<<row_grid(rows), kBlockThreads, 0, stream>>>(x, mask, y, rows, cols);
         else
-            masked_rowblock<1><<<row_grid(rows), kBlockThreads, 0, stream>>>(x, mask, y, rows, cols);
+            masked_rowblock<MaskT, 1><<<row_grid(rows), kBlockThreads, 0, stream>>>(x, mask, y, rows, cols);
     }
     note_launches(1);
     return cudaGetLastError();
+}
+
+cudaError_t launch_masked_softmax(const float* x, const uint8_t* mask, float* y, int64_t rows,
+                                  int64_t cols, bool vec4, cudaStream_t stream) {
+    return launch_masked_impl(x, mask, y, rows, cols, vec4, stream);
+}
+
+cudaError_t launch_masked_softmax_fmask(const float* x, const float* mask, float* y, int64_t rows,
+                                        int64_t cols, bool vec4, cudaStream_t stream) {
+    return launch_masked_impl(x, mask, y, rows, cols, vec4, stream);
 }
 
 }  // namespace rowops

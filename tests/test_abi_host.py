@@ -141,6 +141,19 @@ def test_router_and_top_k_rules(lib):
     assert lib.rowops_top_k_rows(A, B, C, 0, 8, 2, 0, None) == OK
 
 
+def test_misc_rules(lib):
+    assert lib.rowops_masked_softmax_fmask(A, A + 64, C, 4, 64, None) == ALIAS
+    assert lib.rowops_masked_softmax_fmask(A, B, None, 4, 64, None) == NULL
+    assert lib.rowops_lrp_softmax_rows(A, B, C, C, 4, 8, None) == ALIAS
+    assert lib.rowops_lrp_softmax_rows(A, B, None, D, 4, 8, None) == NULL
+    assert lib.rowops_argmax_onehot(A, A, 4, 8, None) == ALIAS
+    assert lib.rowops_argmax_onehot(A, B, 4, 0, None) == OK
+    assert lib.rowops_rmsnorm_fwd(A, B, C, D, 4, 8, -1.0, None) == SHAPE
+    assert lib.rowops_rmsnorm_bwd(A, B, C, D, A, F, 4, 8, None) == ALIAS
+    assert lib.rowops_column_sums(A, A + 16, 4, 8, 0.0, None) == ALIAS
+    assert lib.rowops_column_sums(A, B, 4, 8, float("inf"), None) == SHAPE
+
+
 def test_rejected_calls_launch_nothing(lib):
     n0 = lib.rowops_kernel_launches()
     lib.rowops_topk_kept(A, A, 16, 64, 2, None)
