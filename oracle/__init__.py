@@ -61,6 +61,8 @@ _SIGNATURES = {
     "oracle_lrp_softmax_rows": [_D, _D, _D, _D, _I64, _I64],
     "oracle_masked_softmax_fmask": [_D, _D, _D, _I64, _I64],
     "oracle_argmax_onehot": [_D, _D, _I64, _I64],
+    "oracle_soft_ce": [_D, _D, _D, _D, _I64, _I64, ctypes.c_double],
+    "oracle_teacher_ce": [_D, _D, _D, _D, _I64, _I64, ctypes.c_double],
 }
 
 
@@ -372,3 +374,25 @@ def argmax_onehot(x, n_threads=None) -> np.ndarray:
     _run(_row_blocks(rows, cols * cols, n_threads),
          lambda a, b: lib.oracle_argmax_onehot(_p(x[a:b]), _p(out[a:b]), b - a, cols))
     return out
+
+
+def _two_input_ce(fn_name, a, b, grad_scale, n_threads):
+    lib = _load()
+    a, b = _2d(a), _2d(b)
+    rows, cols = a.shape
+    grad, loss = np.empty_like(a), np.empty(rows)
+    fn = getattr(lib, fn_name)
+    _run(_row_blocks(rows, cols, n_threads),
+         lambda i0, i1: fn(_p(a[i0:i1]), _p(b[i0:i1]), _p(grad[i0:i1]), _p(loss[i0:i1]), i1 - i0, cols, grad_scale))
+    mean_loss = lib.oracle_mean(_p(loss), rows) if rows else float("nan")
+    return grad, loss, mean_loss
+
+
+def soft_ce(logits, weights, grad_scale: float, n_threads=None):
+    """Weighted-logits (soft-target) cross-entropy: returns (grad, row_loss, mean_loss)."""
+    return _two_input_ce("oracle_soft_ce", logits, weights, grad_scale, n_threads)
+
+
+def teacher_ce(student, teacher, grad_scale: float, n_threads=None):
+    """Fixed-teacher cross-entropy: returns (student grad, row_loss, mean_loss)."""
+    return _two_input_ce("oracle_teacher_ce", student, teacher, grad_scale, n_threads)

@@ -524,3 +524,60 @@ void oracle_argmax_onehot(const double *x, double *out, int64_t rows, int64_t co
             out[r * cols + j] = j == first ? 1.0 : 0.0;
     }
 }
+
+/*
+ * [P3] mean weighted-logits cross-entropy, read as cross-entropy against a
+ * weight (soft-target) row: every term is weighted, and its log-probability is
+ * taken from the original logits as x_j - lse, so a term whose probability
+ * underflows still has a finite log-probability.
+ *   lse_i = m + log sum_j exp(x_ij - m),  loss_i = sum_j w_ij * (lse_i - x_ij),
+ *   g_ij = grad_scale * (p_ij * sum_k w_ik - w_ij),  p = softmax(x_i).
+ * With a one-hot w this is oracle_softmax_cross_entropy.
+ */
+void oracle_soft_ce(const double *x, const double *w, double *grad, double *row_loss,
+                    int64_t rows, int64_t cols, double grad_scale)
+{
+    for (int64_t i = 0; i < rows; ++i) {
+        const double *xi = x + i * cols, *wi = w + i * cols;
+        const double m = row_max(xi, cols);
+        double s = 0.0, wsum = 0.0;
+        for (int64_t j = 0; j < cols; ++j) {
+            s += exp(xi[j] - m);
+            wsum += wi[j];
+        }
+        const double lse = m + log(s);
+        double loss = 0.0;
+        for (int64_t j = 0; j < cols; ++j)
+            loss += wi[j] * (lse - xi[j]);
+        row_loss[i] = loss;
+        for (int64_t j = 0; j < cols; ++j)
+            grad[i * cols + j] = grad_scale * (exp(xi[j] - m) / s * wsum - wi[j]);
+    }
+}
+
+/*
+ * [P3] fixed-teacher mean cross-entropy and its student gradient: the teacher
+ * distribution q = softmax(t) is a constant, and with p = softmax(s)
+ *   loss_i = -sum_j q_ij log p_ij = sum_j q_ij (lse(s_i) - s_ij),
+ *   g_ij = grad_scale * (p_ij - q_ij)        (gradient with respect to s).
+ */
+void oracle_teacher_ce(const double *s, const double *t, double *grad, double *row_loss,
+                       int64_t rows, int64_t cols, double grad_scale)
+{
+    for (int64_t i = 0; i < rows; ++i) {
+        const double *si = s + i * cols, *ti = t + i * cols;
+        const double ms = row_max(si, cols), mt = row_max(ti, cols);
+        double ss = 0.0, st = 0.0;
+        for (int64_t j = 0; j < cols; ++j) {
+            ss += exp(si[j] - ms);
+            st += exp(ti[j] - mt);
+        }
+        const double lse = ms + log(ss);
+        double loss = 0.0;
+        for (int64_t j = 0; j < cols; ++j)
+            loss += exp(ti[j] - mt) / st * (lse - si[j]);
+        row_loss[i] = loss;
+        for (int64_t j = 0; j < cols; ++j)
+            grad[i * cols + j] = grad_scale * (exp(si[j] - ms) / ss - exp(ti[j] - mt) / st);
+    }
+}

@@ -696,4 +696,64 @@ def pin_argmax_onehot():
     assert oracle.argmax_onehot(np.zeros((3, 0))).shape == (3, 0)
 
 
+
+
+# ------------------------------------------------------ soft / teacher CE
+
+def pin_soft_ce():
+    rng = _rng(39)
+    R, C = 7, 30
+    x = rng.normal(0, 2, (R, C))
+    t = rng.integers(0, C, R).astype(np.int32)
+    onehot = np.zeros((R, C))
+    onehot[np.arange(R), t] = 1
+    g1, l1, m1 = oracle.soft_ce(x, onehot, 1 / R)
+    g2, l2, m2 = oracle.softmax_cross_entropy(x, t, 1 / R)
+    _close(l1, l2, 1e-13, 1e-14, "one-hot weights = integer targets")
+    _close(g1, g2, 1e-13, 1e-16, "gradient")
+    w = rng.random((R, C))
+    w /= w.sum(axis=1, keepdims=True)
+    g, loss, mean = oracle.soft_ce(x, w, 1 / R)
+    xt = torch.from_numpy(x).requires_grad_(True)
+    ref = torch.nn.functional.cross_entropy(xt, torch.from_numpy(w), reduction="none")
+    _close(loss, ref.detach().numpy(), 1e-13, 1e-14, "torch soft-target cross_entropy")
+    (gx,) = torch.autograd.grad(ref.mean(), xt)
+    _close(g, gx.numpy(), 1e-12, 1e-16, "torch gradient")
+    # unnormalised weights: gradient of the mean loss by finite differences
+    w2 = rng.random((3, 5)) * 3
+    x2 = rng.normal(0, 1, (3, 5))
+    g3, _, _ = oracle.soft_ce(x2, w2, 1 / 3)
+    h = 1e-6
+    fd = np.zeros_like(x2)
+    for i in range(3):
+        for j in range(5):
+            xp, xm = x2.copy(), x2.copy()
+            xp[i, j] += h
+            xm[i, j] -= h
+            fd[i, j] = (oracle.soft_ce(xp, w2, 1.0)[2] - oracle.soft_ce(xm, w2, 1.0)[2]) / (2 * h)
+    _close(g3, fd, 1e-7, 1e-10, "finite differences")
+    # a zero weight on an underflowing probability contributes 0, not NaN
+    _, l4, _ = oracle.soft_ce(np.array([[0.0, -2000.0]]), np.array([[1.0, 0.0]]), 1.0)
+    assert np.isfinite(l4).all()
+
+
+def pin_teacher_ce():
+    rng = _rng(40)
+    R, C = 6, 25
+    s = rng.normal(0, 2, (R, C))
+    t = rng.normal(0, 2, (R, C))
+    q = oracle.softmax_rows(t)
+    g, loss, mean = oracle.teacher_ce(s, t, 1 / R)
+    gs, ls, ms = oracle.soft_ce(s, q, 1 / R)
+    _close(loss, ls, 1e-13, 1e-14, "teacher CE = soft CE with softmax(t)")
+    _close(g, (oracle.softmax_rows(s) - q) / R, 1e-13, 1e-17, "student gradient")
+    st = torch.from_numpy(s).requires_grad_(True)
+    ref = torch.nn.functional.cross_entropy(st, torch.softmax(torch.from_numpy(t), 1), reduction="none")
+    _close(loss, ref.detach().numpy(), 1e-13, 1e-14, "torch")
+    entropy = -(q * np.log(q)).sum(axis=1)
+    assert (loss - entropy >= -1e-12).all(), "cross-entropy >= entropy (KL >= 0)"
+    _close(oracle.teacher_ce(s, s, 1.0)[1], -(oracle.softmax_rows(s) * np.log(oracle.softmax_rows(s))).sum(1),
+           1e-12, 1e-14, "teacher = student gives the entropy")
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

@@ -69,6 +69,10 @@ MUTANTS = [
     ("lrp_y_dropped", "            r_in[i * cols + j] = xi[j] * (ri[j] - yi[j] * s);", "            r_in[i * cols + j] = xi[j] * (ri[j] - s);"),
     ("fmask_nonzero_test", "            if (mi[j] != 0.0) {\n                m = fmax(m, xi[j]);", "            if (mi[j] > 0.0) {\n                m = fmax(m, xi[j]);"),
     ("argmax_last_max", "                if (xr[i] > xr[j])\n                    exceeded = 1;", "                if (xr[i] >= xr[j] && i != j)\n                    exceeded = 1;"),
+    ("softce_wsum_dropped", "            grad[i * cols + j] = grad_scale * (exp(xi[j] - m) / s * wsum - wi[j]);", "            grad[i * cols + j] = grad_scale * (exp(xi[j] - m) / s - wi[j]);"),
+    ("softce_loss_sign", "            loss += wi[j] * (lse - xi[j]);", "            loss += wi[j] * (xi[j] - lse);"),
+    ("teacher_swapped", "            grad[i * cols + j] = grad_scale * (exp(si[j] - ms) / ss - exp(ti[j] - mt) / st);", "            grad[i * cols + j] = grad_scale * (exp(ti[j] - mt) / st - exp(si[j] - ms) / ss);"),
+    ("teacher_loss_student_weights", "            loss += exp(ti[j] - mt) / st * (lse - si[j]);", "            loss += exp(si[j] - ms) / ss * (lse - si[j]);"),
     ("kept_larger_or_equal", "                const int larger = xr[j] > xr[i];", "                const int larger = xr[j] >= xr[i];"),
 ]
 
