@@ -75,6 +75,8 @@ def next_bytes():
         "rmsnorm_bwd": (4 * (4 * r2 * c2 + c2 + r2), r2),         # dy, x, gamma, row_rms; dx, terms
         "column_sums": (4 * (r2 * c2 + c2), r2),                  # gamma_terms read; dgamma written
         "argmax_onehot": (8 * r5 * c5, r5),             # x read; one-hot written
+        "soft_ce": (4 * (3 * r2 * c2 + r2) + 8, r2),    # logits, weights read; grad, row loss, mean
+        "teacher_ce": (4 * (3 * r2 * c2 + r2) + 8, r2),  # student, teacher read; grad, row loss, mean
         "router_masked_topk": (13 * r5 * c5, r5),       # x, mask read; p, kept written
         "top_k_rows": (4 * r5 * c5 + 8 * r5 * k, r5),   # x read; values, indices written
     }
@@ -160,12 +162,15 @@ class Ops:
             self.rms_dx, self.rms_t = torch.empty_like(self.lx), torch.empty_like(self.lx)
             self.rms_dg = torch.empty_like(self.lg)
             ro.rowops_rmsnorm_fwd(self.lx, self.lg, self.rms_out, self.rms_r, eps=self.eps)
+            self.ldy_soft = torch.softmax(self.ldy, dim=1)  # soft targets for the weighted-logits CE
         return [
             ("rmsnorm_fwd", lambda: ro.rowops_rmsnorm_fwd(self.lx, self.lg, self.rms_out, self.rms_r, eps=self.eps)),
             ("rmsnorm_bwd", lambda: ro.rowops_rmsnorm_bwd(self.ldy, self.lg, self.lx, self.rms_r, self.rms_dx,
                                                           self.rms_t)),
             ("column_sums", lambda: ro.rowops_column_sums(self.rms_t, self.rms_dg)),
             ("argmax_onehot", lambda: ro.rowops_argmax_onehot(self.rx, self.fk)),
+            ("soft_ce", lambda: ro.rowops_soft_ce(self.lx, self.ldy_soft, self.rms_dx, self.rms_r, self.cml)),
+            ("teacher_ce", lambda: ro.rowops_teacher_ce(self.lx, self.ldy, self.rms_dx, self.rms_r, self.cml)),
             ("router_masked_topk", lambda: ro.rowops_router_masked_topk(self.rx, self.rm, self.k, self.fp, self.fk)),
             ("top_k_rows", lambda: ro.rowops_top_k_rows(self.rx, self.k, True, self.tv, self.ti)),
         ]

@@ -335,6 +335,32 @@ int rowops_lrp_softmax_rows(const float *x, const float *y, const float *r, floa
 int rowops_argmax_onehot(const float *x, float *out, int64_t rows, int64_t cols,
                          rowops_stream stream);
 
+/*
+ * Weighted-logits (soft-target) cross-entropy.  [P3] mean weighted-logits
+ * cross-entropy, read as cross-entropy against a weight row, with every
+ * log-probability taken from the original logits (x - lse) so that a weighted
+ * term whose probability underflows stays finite:
+ *   loss_i = sum_j w_ij (lse_i - x_ij),  *mean_loss = (1/rows) sum_i loss_i,
+ *   grad_ij = grad_scale * (softmax(x_i)_j * sum_k w_ik - w_ij).
+ * A one-hot w gives rowops_softmax_ce.  logits, weights, grad: rows x cols;
+ * row_loss: rows; mean_loss: one device double.  cols == 0 or non-finite
+ * grad_scale is ROWOPS_ERR_SHAPE; outputs must not overlap inputs or each other.
+ */
+int rowops_soft_ce(const float *logits, const float *weights, float *grad, float *row_loss,
+                   double *mean_loss, int64_t rows, int64_t cols, float grad_scale,
+                   rowops_stream stream);
+
+/*
+ * Fixed-teacher cross-entropy and the student gradient.  [P3] fixed-teacher mean
+ * cross-entropy, or its student gradient: q = softmax(teacher) is a constant,
+ *   loss_i = sum_j q_ij (lse(student)_i - student_ij),  mean over rows,
+ *   grad_ij = grad_scale * (softmax(student_i)_j - q_ij)   (written when grad != NULL).
+ * Shapes and rules as rowops_soft_ce; grad may be NULL (loss only).
+ */
+int rowops_teacher_ce(const float *student, const float *teacher, float *grad, float *row_loss,
+                      double *mean_loss, int64_t rows, int64_t cols, float grad_scale,
+                      rowops_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -26,7 +26,9 @@ from .binding import (  # noqa: F401
     rowops_router_masked_topk,
     rowops_softmax_bwd,
     rowops_softmax_ce,
+    rowops_soft_ce,
     rowops_softmax_fwd,
+    rowops_teacher_ce,
     rowops_top_k_rows,
     rowops_topk_kept,
 )

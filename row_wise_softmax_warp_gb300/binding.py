@@ -48,6 +48,8 @@ SIGNATURES = {
     "rowops_masked_softmax_fmask": ([_P, _P, _P, _I64, _I64, _P], ctypes.c_int),
     "rowops_lrp_softmax_rows": ([_P, _P, _P, _P, _I64, _I64, _P], ctypes.c_int),
     "rowops_argmax_onehot": ([_P, _P, _I64, _I64, _P], ctypes.c_int),
+    "rowops_soft_ce": ([_P, _P, _P, _P, _P, _I64, _I64, _F, _P], ctypes.c_int),
+    "rowops_teacher_ce": ([_P, _P, _P, _P, _P, _I64, _I64, _F, _P], ctypes.c_int),
     "rowops_layernorm_bwd_noalloc": ([_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P], ctypes.c_int),
     "rowops_layernorm_bwd_noalloc_max_bytes": ([], ctypes.c_size_t),
 }
@@ -327,6 +329,32 @@ def rowops_argmax_onehot(x, out=None, stream=None):
     rows, cols = _shape(x)
     _check(library().rowops_argmax_onehot(x.data_ptr(), out.data_ptr(), rows, cols, _stream(x, stream)))
     return out
+
+
+def _ce2(fn, x, w, grad, row_loss, mean_loss, grad_scale, stream, want_grad=True):
+    x, w = _mat(x, "logits"), _mat(w, "weights")
+    rows, cols = _shape(x)
+    if want_grad:
+        grad = _out(grad, x, "grad")
+    row_loss = _out(row_loss, x, "row_loss", shape=(rows,))
+    mean_loss = _out(mean_loss, x, "mean_loss", shape=(1,), dtype=torch.float64)
+    if grad_scale is None:
+        grad_scale = 1.0 / rows if rows else 1.0
+    _check(fn(x.data_ptr(), w.data_ptr(), grad.data_ptr() if grad is not None else None, row_loss.data_ptr(),
+              mean_loss.data_ptr(), rows, cols, grad_scale, _stream(x, stream)))
+    return grad, row_loss, mean_loss
+
+
+def rowops_soft_ce(logits, weights, grad=None, row_loss=None, mean_loss=None, grad_scale=None, stream=None):
+    """Weighted-logits (soft-target) CE: returns (grad, row_loss, mean_loss)."""
+    return _ce2(library().rowops_soft_ce, logits, weights, grad, row_loss, mean_loss, grad_scale, stream)
+
+
+def rowops_teacher_ce(student, teacher, grad=None, row_loss=None, mean_loss=None, grad_scale=None,
+                      with_grad=True, stream=None):
+    """Fixed-teacher CE: returns (student grad or None, row_loss, mean_loss)."""
+    return _ce2(library().rowops_teacher_ce, student, teacher, grad, row_loss, mean_loss, grad_scale, stream,
+                want_grad=with_grad)
 
 
 def rowops_layernorm_bwd_noalloc(dy, gamma, xhat, inv_std, dx=None, dgamma=None, dbeta=None, stream=None):

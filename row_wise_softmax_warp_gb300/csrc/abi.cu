@@ -332,4 +332,41 @@ int rowops_argmax_onehot(const float* x, float* out, int64_t rows, int64_t cols,
     return to_status(rowops::launch_argmax_onehot(x, out, rows, cols, vec4, st(stream)));
 }
 
+static int ce2_checks(const float* x, const float* w, float* grad, float* row_loss, double* mean_loss,
+                      int64_t rows, int64_t cols, float grad_scale, bool grad_required) {
+    if (int e = check_dims(rows, cols)) return e;
+    if (cols == 0 || !std::isfinite(grad_scale)) return ROWOPS_ERR_SHAPE;
+    if (rows == 0) return -1;  // nothing to do
+    if (!x || !w || !row_loss || !mean_loss || (grad_required && !grad)) return ROWOPS_ERR_NULL;
+    const int64_t n = rows * cols * 4;
+    const Buf in[2] = {{x, n}, {w, n}};
+    const Buf out[3] = {{grad, grad ? n : 0}, {row_loss, rows * 4}, {mean_loss, 8}};
+    for (const Buf& o : out) {
+        for (const Buf& i : in)
+            if (overlap(o, i)) return ROWOPS_ERR_ALIAS;
+        for (const Buf& o2 : out)
+            if (&o != &o2 && overlap(o, o2)) return ROWOPS_ERR_ALIAS;
+    }
+    return ROWOPS_OK;
+}
+
+int rowops_soft_ce(const float* logits, const float* weights, float* grad, float* row_loss, double* mean_loss,
+                   int64_t rows, int64_t cols, float grad_scale, rowops_stream stream) {
+    const int e = ce2_checks(logits, weights, grad, row_loss, mean_loss, rows, cols, grad_scale, true);
+    if (e != ROWOPS_OK) return e < 0 ? ROWOPS_OK : e;
+    const bool vec4 = cols % 4 == 0 && aligned(logits, 16) && aligned(weights, 16) && aligned(grad, 16);
+    return to_status(rowops::launch_soft_ce(logits, weights, grad, row_loss, mean_loss, rows, cols, grad_scale,
+                                            vec4, st(stream)));
+}
+
+int rowops_teacher_ce(const float* student, const float* teacher, float* grad, float* row_loss,
+                      double* mean_loss, int64_t rows, int64_t cols, float grad_scale, rowops_stream stream) {
+    const int e = ce2_checks(student, teacher, grad, row_loss, mean_loss, rows, cols, grad_scale, false);
+    if (e != ROWOPS_OK) return e < 0 ? ROWOPS_OK : e;
+    const bool vec4 = cols % 4 == 0 && aligned(student, 16) && aligned(teacher, 16) &&
+                      (grad == nullptr || aligned(grad, 16));
+    return to_status(rowops::launch_teacher_ce(student, teacher, grad, row_loss, mean_loss, rows, cols,
+                                               grad_scale, vec4, st(stream)));
+}
+
 }  // extern "C"

@@ -127,6 +127,12 @@ cudaError_t launch_lrp_softmax(const float* x, const float* y, const float* r, f
                                int64_t cols, bool vec4, cudaStream_t stream);
 cudaError_t launch_argmax_onehot(const float* x, float* out, int64_t rows, int64_t cols, bool vec4,
                                  cudaStream_t stream);
+// Fixed-order mean of the row losses into one double (programmatic dependent).
+cudaError_t launch_row_mean(const float* row_loss, int64_t rows, double* mean_loss, cudaStream_t stream);
+cudaError_t launch_soft_ce(const float* x, const float* w, float* grad, float* row_loss, double* mean_loss,
+                           int64_t rows, int64_t cols, float grad_scale, bool vec4, cudaStream_t stream);
+cudaError_t launch_teacher_ce(const float* s, const float* t, float* grad, float* row_loss, double* mean_loss,
+                              int64_t rows, int64_t cols, float grad_scale, bool vec4, cudaStream_t stream);
 cudaError_t launch_topk_kept(const float* x, float* kept, int64_t rows, int64_t cols, int64_t k,
                              bool vec4, cudaStream_t stream);
 

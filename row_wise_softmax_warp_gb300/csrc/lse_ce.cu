@@ -428,6 +428,11 @@ cudaError_t launch_softmax_ce(const float* logits, const int32_t* targets, float
     }
     if (err == cudaSuccess) err = cudaGetLastError();
     if (err != cudaSuccess) return err;
+    note_launches(1);
+    return launch_row_mean(row_loss, rows, mean_loss, stream);
+}
+
+cudaError_t launch_row_mean(const float* row_loss, int64_t rows, double* mean_loss, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1);
     cfg.blockDim = dim3(1024);
@@ -437,8 +442,8 @@ cudaError_t launch_softmax_ce(const float* logits, const int32_t* targets, float
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    err = cudaLaunchKernelEx(&cfg, ce_mean, static_cast<const float*>(row_loss), rows, mean_loss);
-    note_launches(2);
+    const cudaError_t err = cudaLaunchKernelEx(&cfg, ce_mean, row_loss, rows, mean_loss);
+    note_launches(1);
     return err != cudaSuccess ? err : cudaGetLastError();
 }
 

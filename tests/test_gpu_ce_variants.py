@@ -1,0 +1,62 @@
+"""GPU parity: weighted-logits (soft-target) and fixed-teacher cross-entropy."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity_util import check_abs, check_rel, gpu, host
+
+pytestmark = pytest.mark.gpu
+
+COLS = [1, 3, 4, 16, 64, 256, 1000, 1024, 1028, 8192, 50304]
+
+
+def _inputs(rows, cols, seed):
+    rng = np.random.default_rng(seed)
+    x = (rng.normal(0, 2, (rows, cols))).astype(np.float32)
+    x[rng.random(x.shape) < 1e-3] = 30.0
+    w = rng.random((rows, cols)).astype(np.float32)
+    w[rng.random(w.shape) < 0.5] = 0.0
+    t = (rng.normal(0, 2, (rows, cols))).astype(np.float32)
+    return x, w, t
+
+
+@pytest.mark.parametrize("cols", COLS)
+@pytest.mark.parametrize("misalign", [False, True])
+def test_soft_ce(ro, cols, misalign):
+    rows = 5 if cols > 4096 else 33
+    x, w, _ = _inputs(rows, cols, cols)
+    g, rl, ml = ro.rowops_soft_ce(gpu(x, misalign), gpu(w, misalign), grad_scale=1.0 / rows)
+    gr, rlr, mlr = oracle.soft_ce(x, w, 1.0 / rows)
+    wsum = np.abs(w.astype(np.float64)).sum(axis=1, keepdims=True)
+    check_abs(host(g), gr, 2e-6 * (1.0 / rows) * np.maximum(1.0, wsum), f"soft ce grad cols={cols}")
+    scale = np.maximum(1.0, np.abs(w.astype(np.float64)).sum(axis=1) * (np.abs(x).max(axis=1) + 10))
+    check_abs(host(rl), rlr, 1e-5 * scale, f"soft ce loss cols={cols}")
+    check_abs(host(ml), [mlr], 1e-5 * scale.max(), "soft ce mean")
+
+
+@pytest.mark.parametrize("cols", COLS)
+@pytest.mark.parametrize("misalign", [False, True])
+def test_teacher_ce(ro, cols, misalign):
+    rows = 5 if cols > 4096 else 33
+    s, _, t = _inputs(rows, cols, cols + 1)
+    sg, tg = gpu(s, misalign), gpu(t, misalign)
+    g, rl, ml = ro.rowops_teacher_ce(sg, tg, grad_scale=1.0 / rows)
+    gr, rlr, mlr = oracle.teacher_ce(s, t, 1.0 / rows)
+    check_abs(host(g), gr, 4e-6 / rows, f"teacher grad cols={cols}")
+    check_rel(host(rl), rlr, f"teacher loss cols={cols}")
+    check_rel(host(ml), [mlr], "teacher mean")
+    _, rl2, ml2 = ro.rowops_teacher_ce(sg, tg, with_grad=False)
+    assert torch.equal(rl2, rl)
+
+
+def test_soft_ce_one_hot_matches_integer_targets(ro):
+    rng = np.random.default_rng(9)
+    x = rng.normal(0, 2, (64, 50304)).astype(np.float32)
+    t = rng.integers(0, 50304, 64).astype(np.int32)
+    w = np.zeros_like(x)
+    w[np.arange(64), t] = 1
+    g1, l1, _ = ro.rowops_soft_ce(gpu(x), gpu(w))
+    g2, l2, _ = ro.rowops_softmax_ce(gpu(x), gpu(t))
+    check_abs(host(g1), host(g2), 2e-6 / 64, "one-hot grad")
+    check_rel(host(l1), host(l2).astype(np.float64), "one-hot loss")
