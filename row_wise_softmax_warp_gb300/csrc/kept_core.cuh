@@ -88,9 +88,10 @@ __device__ __forceinline__ void kept_select(const float (&v)[NV][VEC], const boo
             for (int e = 0; e < VEC; ++e) keep[kk][e] = cnt[kk][e] < k;
     } else if (k <= 2) {
         // Top two in one pass: each lane keeps its best two (value, column)
-        // pairs in the rule's order (its columns arrive in increasing order),
-        // then the group merges the pairs with a butterfly; every lane ends
-        // with the row's best two.
+        // pairs; its columns arrive in increasing order, so a later entry only
+        // displaces on a strictly larger value (or an empty place).  The group
+        // then merges the pairs with a butterfly under the full rule; every lane
+        // ends with the row's best two.
         float m1 = -INFINITY, m2 = -INFINITY;
         int i1 = INT_MAX, i2 = INT_MAX;
 #pragma unroll
@@ -100,9 +101,9 @@ __device__ __forceinline__ void kept_select(const float (&v)[NV][VEC], const boo
                 const float xv = v[kk][e];
                 const int c = (g + kk * LANES) * VEC + e;
                 if (valid[kk][e]) {
-                    if (beats(xv, c, m1, i1)) {
+                    if (xv > m1 || i1 == INT_MAX) {
                         m2 = m1; i2 = i1; m1 = xv; i1 = c;
-                    } else if (beats(xv, c, m2, i2)) {
+                    } else if (xv > m2 || i2 == INT_MAX) {
                         m2 = xv; i2 = c;
                     }
                 }

@@ -69,20 +69,21 @@ router_group(const float* x, const uint8_t* __restrict__ mask, float* p, float* 
             }
         s = group_sum<LANES>(s);
         const float inv = n_allowed > 0 ? 1.0f / s : 0.f;
-        bool has_nan = false;
+        float probe = 0.f;  // probabilities sum to at most 1; NaN makes the sum NaN
 #pragma unroll
         for (int kk = 0; kk < NV; ++kk) {
 #pragma unroll
             for (int e = 0; e < VEC; ++e) {
                 v[kk][e] = al[kk][e] ? v[kk][e] * inv : 0.f;  // the stored probabilities
-                has_nan |= valid[kk][e] && isnan(v[kk][e]);
+                probe += v[kk][e];
             }
             const int c = g + kk * LANES;
             if (live && c < nch) st_chunk<VEC>(p + off + c * VEC, v[kk]);
         }
         // Top-k kept mask of those probabilities.
         bool keep[NV][VEC];
-        kept_select<LANES, NV, VEC>(v, valid, __any_sync(kFullMask, has_nan), cols, k, keep);
+        kept_select<LANES, NV, VEC>(v, valid, __any_sync(kFullMask, !(fabsf(probe) <= 3.402823466e38f)), cols,
+                                    k, keep);
 #pragma unroll
         for (int kk = 0; kk < NV; ++kk) {
             const int c = g + kk * LANES;

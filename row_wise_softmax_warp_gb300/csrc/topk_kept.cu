@@ -28,14 +28,14 @@ kept_group(const float* __restrict__ x, float* __restrict__ kept, int64_t rows, 
         const int64_t off = (live ? row : 0) * int64_t(cols);
         float v[NV][VEC];
         bool valid[NV][VEC];
-        bool has_nan = false;
+        float probe = 0.f;  // a NaN anywhere makes the sum non-finite
 #pragma unroll
         for (int kk = 0; kk < NV; ++kk) {
             const int c = g + kk * LANES;
             if (live && c < nch) {
                 ld_chunk<VEC>(x + off + c * VEC, v[kk]);
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) has_nan |= isnan(v[kk][e]);
+                for (int e = 0; e < VEC; ++e) probe += v[kk][e];
             } else {
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) v[kk][e] = 0.f;
@@ -44,7 +44,10 @@ kept_group(const float* __restrict__ x, float* __restrict__ kept, int64_t rows, 
             for (int e = 0; e < VEC; ++e) valid[kk][e] = live && c < nch;
         }
         bool keep[NV][VEC];
-        kept_select<LANES, NV, VEC>(v, valid, __any_sync(kFullMask, has_nan), cols, k, keep);
+        // A non-finite sum (NaN, or infinities / overflow) sends the warp to the
+        // literal count, which is exact for every input.
+        kept_select<LANES, NV, VEC>(v, valid, __any_sync(kFullMask, !(fabsf(probe) <= 3.402823466e38f)), cols,
+                                    k, keep);
 #pragma unroll
         for (int kk = 0; kk < NV; ++kk) {
             const int c = g + kk * LANES;
