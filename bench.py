@@ -495,7 +495,7 @@ def gpu_leg(args):
                 "ms_per_step": round(e2e_ms, 3), "steps": ke},
         "clocks": clocks.summary(),
     }
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and world == 1:  # the CPU baseline belongs to the N = 1 line
         line["cpu_baseline"] = cpu_leg(data, budget_s=args.cpu_seconds)
     print(json.dumps(line), flush=True)
     if dist is not None:
