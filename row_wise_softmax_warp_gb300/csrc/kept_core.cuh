@@ -45,6 +45,27 @@ __device__ __forceinline__ int low_bits(int cols) { return cols <= 1 ? 0 : 32 - 
 
 }  // namespace kept_detail
 
+// Loads row `row` into a group's registers (zeros outside the row or past the
+// last row); read-only input.
+template <int LANES, int NV, int VEC>
+__device__ __forceinline__ void kept_load_row(const float* __restrict__ x, int64_t row, int64_t rows, int cols,
+                                              float (&v)[NV][VEC]) {
+    const int g = threadIdx.x % LANES;
+    const int nch = cols / VEC;
+    const bool live = row < rows;
+    const int64_t off = (live ? row : 0) * int64_t(cols);
+#pragma unroll
+    for (int kk = 0; kk < NV; ++kk) {
+        const int c = g + kk * LANES;
+        if (live && c < nch) {
+            ld_chunk<VEC>(x + off + c * VEC, v[kk]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) v[kk][e] = 0.f;
+        }
+    }
+}
+
 // Sets keep[kk][e] for this lane's entries of the row its group holds.  `valid`
 // marks entries inside the row; any_nan must be warp-uniform (true when any
 // group of the warp has a NaN in its row).  Every lane of the warp must call it.

@@ -17,6 +17,7 @@ namespace rowops {
 // ------------------------------------------------------------ bookkeeping
 
 void note_launches(int n);  // counts kernels queued (rowops_kernel_launches)
+int sm_count();             // SMs of the current device (cached; 0 if unknown)
 
 template <int L, int N, int V>
 struct Geom {
@@ -61,6 +62,16 @@ inline unsigned group_grid(int64_t rows, int lanes) {
     int64_t b = (rows + groups_per_block - 1) / groups_per_block;
     if (b > (1 << 20)) b = 1 << 20;
     return static_cast<unsigned>(b < 1 ? 1 : b);
+}
+
+// Blocks for a group kernel whose loop loads the next rows while it works on
+// the current ones: at most `per_sm` blocks per SM, so each group walks several
+// rows and its loads stay in flight across the selection work.
+inline unsigned stream_grid(int64_t rows, int lanes, int per_sm = 8) {
+    const unsigned g = group_grid(rows, lanes);
+    const int sms = sm_count();
+    const int64_t cap = int64_t(sms > 0 ? sms : 132) * per_sm;
+    return int64_t(g) > cap ? static_cast<unsigned>(cap) : g;
 }
 
 // Blocks for a one-row-per-block (or per-cluster) kernel.

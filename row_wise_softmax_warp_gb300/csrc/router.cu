@@ -10,8 +10,9 @@
 //
 // top_k_rows: the order is a strict total order on (key, column) with key the
 // order-preserving uint32 of the value, NaN mapped above +inf and -0 onto +0;
-// k rounds each pick the best remaining key (max for largest, min for
-// smallest) and the lowest column holding it.
+// k <= 2 takes one pass of per-lane best pairs and a butterfly merge, larger k
+// takes k rounds that each pick the best remaining key (max for largest, min
+// for smallest) and the lowest column holding it.
 #include "common.cuh"
 #include "kept_core.cuh"
 #include "launch.h"
@@ -126,27 +127,92 @@ top_k_rows_group(const float* __restrict__ x, float* __restrict__ values, float*
     const int grp = threadIdx.x / LANES;
     const int leader = (threadIdx.x & 31) - g;
     const int nch = cols / VEC;
-    for (int64_t base = int64_t(blockIdx.x) * GPB; base < rows; base += int64_t(gridDim.x) * GPB) {
+    const int64_t stride = int64_t(gridDim.x) * GPB;
+    float nv[NV][VEC];
+    kept_load_row<LANES, NV, VEC>(x, int64_t(blockIdx.x) * GPB + grp, rows, cols, nv);
+    for (int64_t base = int64_t(blockIdx.x) * GPB; base < rows; base += stride) {  // block-uniform
+        float v[NV][VEC];
+#pragma unroll
+        for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) v[kk][e] = nv[kk][e];
+        if (base + stride < rows) kept_load_row<LANES, NV, VEC>(x, base + stride + grp, rows, cols, nv);
         const int64_t row = base + grp;
         const bool live = row < rows;
-        const int64_t off = (live ? row : 0) * int64_t(cols);
-        float v[NV][VEC];
         uint32_t key[NV][VEC];
         bool avail[NV][VEC];
 #pragma unroll
         for (int kk = 0; kk < NV; ++kk) {
             const int c = g + kk * LANES;
-            if (live && c < nch) {
-                ld_chunk<VEC>(x + off + c * VEC, v[kk]);
-            } else {
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) v[kk][e] = 0.f;
-            }
 #pragma unroll
             for (int e = 0; e < VEC; ++e) {
                 key[kk][e] = rank_key(v[kk][e]);
                 avail[kk][e] = live && c < nch;
             }
+        }
+        if (k <= 2) {
+            // One pass keeps each lane's best two (key, column) pairs, in the
+            // order "larger key first, then lower column" (keys complemented for
+            // smallest-first); a butterfly merge of the pairs leaves the row's
+            // best two in every lane of the group.  Columns are visited in
+            // increasing order, so a strict comparison keeps the lower column
+            // of equal keys.
+            const uint32_t flip = largest ? 0u : 0xffffffffu;
+            uint32_t m1 = 0, m2 = 0;
+            int i1 = INT_MAX, i2 = INT_MAX;  // INT_MAX: empty slot
+#pragma unroll
+            for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    const uint32_t kx = key[kk][e] ^ flip;
+                    const int c = (g + kk * LANES) * VEC + e;
+                    if (avail[kk][e]) {
+                        if (kx > m1 || i1 == INT_MAX) {
+                            m2 = m1; i2 = i1; m1 = kx; i1 = c;
+                        } else if (kx > m2 || i2 == INT_MAX) {
+                            m2 = kx; i2 = c;
+                        }
+                    }
+                }
+            auto before = [](uint32_t ak, int ac, uint32_t bk, int bc) {
+                return ak > bk || (ak == bk && ac < bc);
+            };
+#pragma unroll
+            for (int o = LANES / 2; o > 0; o >>= 1) {
+                const uint32_t om1 = __shfl_xor_sync(kFullMask, m1, o), om2 = __shfl_xor_sync(kFullMask, m2, o);
+                const int oi1 = __shfl_xor_sync(kFullMask, i1, o), oi2 = __shfl_xor_sync(kFullMask, i2, o);
+                if (before(om1, oi1, m1, i1)) {
+                    if (before(om2, oi2, m1, i1)) {
+                        m2 = om2; i2 = oi2;
+                    } else {
+                        m2 = m1; i2 = i1;
+                    }
+                    m1 = om1; i1 = oi1;
+                } else if (before(om1, oi1, m2, i2)) {
+                    m2 = om1; i2 = oi1;
+                }
+            }
+            // The lanes holding the two columns pass their values to the group.
+            float v1 = 0.f, v2 = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    const int c = (g + kk * LANES) * VEC + e;
+                    if (c == i1) v1 = v[kk][e];
+                    if (c == i2) v2 = v[kk][e];
+                }
+            v1 = __shfl_sync(kFullMask, v1, leader + (i1 / VEC) % LANES);
+            v2 = __shfl_sync(kFullMask, v2, leader + (k == 2 ? (i2 / VEC) % LANES : 0));
+            if (live && g == 0) {
+                values[row * int64_t(k)] = v1;
+                indices[row * int64_t(k)] = float(i1);
+                if (k == 2) {
+                    values[row * int64_t(k) + 1] = v2;
+                    indices[row * int64_t(k) + 1] = float(i2);
+                }
+            }
+            continue;
         }
         for (int r = 0; r < k; ++r) {
             uint32_t best = largest ? 0u : 0xffffffffu;
@@ -289,7 +355,7 @@ cudaError_t launch_top_k_rows(const float* x, float* values, float* indices, int
                               int64_t k, bool largest, bool vec4, cudaStream_t stream) {
     const bool done = with_geometry(vec4, cols, [&](auto geo) {
         using G = decltype(geo);
-        top_k_rows_group<G::LANES, G::NV, G::VEC><<<group_grid(rows, G::LANES), kBlockThreads, 0, stream>>>(
+        top_k_rows_group<G::LANES, G::NV, G::VEC><<<stream_grid(rows, G::LANES), kBlockThreads, 0, stream>>>(
             x, values, indices, rows, int(cols), int(k), largest ? 1 : 0);
     });
     if (!done) {

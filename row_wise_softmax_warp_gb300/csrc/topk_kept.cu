@@ -15,6 +15,8 @@ using kept_detail::low_bits;
 using kept_detail::make_key;
 
 // Group kernel (geometry of common.cuh): a group of LANES lanes owns a row.
+// Blocks walk the rows in a grid-stride loop and load a group's next row
+// before selecting in the current one, so that load is in flight meanwhile.
 template <int LANES, int NV, int VEC>
 __global__ void __launch_bounds__(kBlockThreads)
 kept_group(const float* __restrict__ x, float* __restrict__ kept, int64_t rows, int cols, int k) {
@@ -22,27 +24,28 @@ kept_group(const float* __restrict__ x, float* __restrict__ kept, int64_t rows, 
     const int g = threadIdx.x % LANES;
     const int grp = threadIdx.x / LANES;
     const int nch = cols / VEC;
-    for (int64_t base = int64_t(blockIdx.x) * GPB; base < rows; base += int64_t(gridDim.x) * GPB) {
+    const int64_t stride = int64_t(gridDim.x) * GPB;
+    float next[NV][VEC];
+    kept_load_row<LANES, NV, VEC>(x, int64_t(blockIdx.x) * GPB + grp, rows, cols, next);
+    for (int64_t base = int64_t(blockIdx.x) * GPB; base < rows; base += stride) {  // block-uniform
+        float v[NV][VEC];
+#pragma unroll
+        for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) v[kk][e] = next[kk][e];
+        if (base + stride < rows) kept_load_row<LANES, NV, VEC>(x, base + stride + grp, rows, cols, next);
         const int64_t row = base + grp;
         const bool live = row < rows;
         const int64_t off = (live ? row : 0) * int64_t(cols);
-        float v[NV][VEC];
         bool valid[NV][VEC];
         float probe = 0.f;  // a NaN anywhere makes the sum non-finite
 #pragma unroll
-        for (int kk = 0; kk < NV; ++kk) {
-            const int c = g + kk * LANES;
-            if (live && c < nch) {
-                ld_chunk<VEC>(x + off + c * VEC, v[kk]);
+        for (int kk = 0; kk < NV; ++kk)
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) probe += v[kk][e];
-            } else {
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) v[kk][e] = 0.f;
+            for (int e = 0; e < VEC; ++e) {
+                valid[kk][e] = live && g + kk * LANES < nch;
+                probe += v[kk][e];
             }
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) valid[kk][e] = live && c < nch;
-        }
         bool keep[NV][VEC];
         // A non-finite sum (NaN, or infinities / overflow) sends the warp to the
         // literal count, which is exact for every input.
@@ -129,7 +132,7 @@ cudaError_t launch_topk_kept(const float* x, float* kept, int64_t rows, int64_t 
                              bool vec4, cudaStream_t stream) {
     const bool done = with_geometry(vec4, cols, [&](auto geo) {
         using G = decltype(geo);
-        kept_group<G::LANES, G::NV, G::VEC><<<group_grid(rows, G::LANES), kBlockThreads, 0, stream>>>(
+        kept_group<G::LANES, G::NV, G::VEC><<<stream_grid(rows, G::LANES), kBlockThreads, 0, stream>>>(
             x, kept, rows, int(cols), int(k));
     });
     if (!done) {

@@ -3,7 +3,8 @@
     python -m row_wise_softmax_warp_gb300.run_op --op softmax_ce --rows 1024 --cols 50304 --reps 3
 
 Ops: softmax_fwd, softmax_bwd, attn_fwd, attn_bwd (cols = seq_len), logsumexp,
-softmax_ce, layernorm_fwd, layernorm_bwd, masked_softmax, topk_kept.  Inputs
+softmax_ce, layernorm_fwd, layernorm_bwd, masked_softmax, topk_kept,
+router_masked_topk, top_k_rows, argmax_onehot.  Inputs
 follow the workload distributions of ``inputs``; the L2 is flushed (512 MiB
 write) before every call.  Prints the median CUDA-event time per call.
 """
@@ -67,6 +68,18 @@ def make(op: str, rows: int, cols: int, dev):
             return lambda: ro.rowops_masked_softmax(x, m, p)
         kept = torch.empty_like(p)
         return lambda: ro.rowops_topk_kept(p, r["k"], kept)
+    if op in ("router_masked_topk", "top_k_rows", "argmax_onehot"):
+        r = inputs.router(0, rows=rows, cols=cols)
+        x, m = t(r["x"]), t(r["mask"])
+        if op == "router_masked_topk":
+            p, kept = torch.empty_like(x), torch.empty_like(x)
+            return lambda: ro.rowops_router_masked_topk(x, m, r["k"], p, kept)
+        if op == "top_k_rows":
+            vals = torch.empty((rows, r["k"]), device=dev)
+            idx = torch.empty_like(vals)
+            return lambda: ro.rowops_top_k_rows(x, r["k"], True, vals, idx)
+        oh = torch.empty_like(x)
+        return lambda: ro.rowops_argmax_onehot(x, oh)
     raise SystemExit(f"unknown op {op}")
 
 
