@@ -260,10 +260,17 @@ def peaks():
     return 6800.0, "fallback"
 
 
-def kernel_fingerprint():
+# Sources each recorded kernel is compiled from (its kernels, their launchers
+# and the shared device helpers); a change to any of them voids the record.
+KERNEL_SOURCES = {
+    "softmax_ce": ("common.cuh", "launch.h", "lse_ce.cu", "tma_rows.cu"),
+}
+
+
+def kernel_fingerprint(op="softmax_ce"):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "row_wise_softmax_warp_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in sorted(KERNEL_SOURCES[op]):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -275,7 +282,9 @@ def recorded_traffic(op):
     p = os.path.join(ROOT, "profiles", "dram_traffic.md")
     if not os.path.exists(p):
         return None
-    fp = kernel_fingerprint()
+    if op not in KERNEL_SOURCES:
+        return None
+    fp = kernel_fingerprint(op)
     for line in open(p):
         cells = [c.strip() for c in line.strip().strip("|").split("|")]
         if len(cells) == 3 and cells[0] == op and cells[1].isdigit():

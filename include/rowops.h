@@ -139,7 +139,9 @@ int rowops_logsumexp(const float *x, float *lse, int64_t rows, int64_t cols,
  * [P2] fused_softmax_ce_grad(logits, targets) -> (Float64 loss, grad).
  *   loss_i = lse_i - x_{i,t_i}
  *   grad_ij = grad_scale * (softmax(x_i)_j - [j == t_i])
- *   *mean_loss = (1/rows) * sum_i loss_i   (double, fixed summation order)
+ *   *mean_loss = (1/rows) * sum_i loss_i   (fixed summation order; summed as a
+ *   double-word fp32 value, about 48 significant bits, and returned as a double;
+ *   a sum that is not finite in that form is redone in double)
  * logits, grad: rows x cols fp32; targets: rows int32; row_loss: rows fp32
  * (written, then reduced into the mean); mean_loss: ONE double in device memory.
  * grad_scale = 1/rows gives the gradient of the mean loss.  A target outside

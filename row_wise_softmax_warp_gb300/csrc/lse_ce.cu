@@ -333,31 +333,99 @@ ce_rowblock(const float* __restrict__ x, const int32_t* __restrict__ targets,
     }
 }
 
-// Mean of the row losses in double.  Launched as a programmatic dependent of
-// the loss kernel: it waits here for that grid.  Thread t adds rows t, t+1024,
-// ... in order (eight loads in flight), warps reduce with a fixed xor
-// butterfly and warp 0 adds the 32 warp sums in order: one block, fixed order.
+// Mean of the row losses.  Launched as a programmatic dependent of the loss
+// kernel: it waits here for that grid.  One block, fixed order: thread t adds
+// rows t, t+1024, ... in order (eight loads in flight), warps combine with a
+// fixed xor butterfly, then warp 0 combines the 32 warp sums the same way.
+//
+// The sum is carried as a double-word fp32 value hi + lo (about 48 significant
+// bits), whose additions use only the fp32 pipes: a single block spends about
+// 8 us on GB300's narrow fp64 pipe converting and adding 8192 losses in
+// double, against about 1 us this way.  Error-free transformations:
+//   TwoSum(a, b)   (Knuth): s = fl(a + b) and e with a + b = s + e exactly;
+//   Fast2Sum(a, b) (Dekker, |a| >= |b|): the same with three operations;
+// word + float and word + word follow the double-word additions of Joldes,
+// Muller and Popescu (2017) ("DWPlusFP" and "AccurateDWPlusDW"), each with a
+// relative error of order u^2, u = 2^-24.  A sum that is not finite in
+// this form (an infinite or NaN loss, or fp32 overflow) is recomputed in double
+// in the same fixed order, so such means are IEEE double sums as before.
+struct DWord {
+    float hi, lo;
+};
+
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+    s = a + b;
+    const float bv = s - a;
+    e = (a - (s - bv)) + (b - bv);
+}
+
+__device__ __forceinline__ void fast_two_sum(float a, float b, float& s, float& e) {
+    s = a + b;
+    e = b - (s - a);
+}
+
+__device__ __forceinline__ DWord dw_add(DWord x, float y) {
+    float sh, sl, zh, zl;
+    two_sum(x.hi, y, sh, sl);
+    fast_two_sum(sh, x.lo + sl, zh, zl);
+    return {zh, zl};
+}
+
+__device__ __forceinline__ DWord dw_add(DWord x, DWord y) {
+    float sh, sl, th, tl, vh, vl, zh, zl;
+    two_sum(x.hi, y.hi, sh, sl);
+    two_sum(x.lo, y.lo, th, tl);
+    fast_two_sum(sh, sl + th, vh, vl);
+    fast_two_sum(vh, tl + vl, zh, zl);
+    return {zh, zl};
+}
+
+__device__ __forceinline__ DWord dw_shfl_xor(DWord v, int o) {
+    return {__shfl_xor_sync(kFullMask, v.hi, o), __shfl_xor_sync(kFullMask, v.lo, o)};
+}
+
 __global__ void __launch_bounds__(1024)
 ce_mean(const float* row_loss, int64_t rows, double* __restrict__ mean) {
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
-    __shared__ double part[32];
-    double s = 0.0;
+    __shared__ DWord part[32];
+    __shared__ double dpart[32];
+    __shared__ int redo;
+    DWord s{0.f, 0.f};
     int64_t i = threadIdx.x;
     for (; i + 7 * 1024 < rows; i += 8 * 1024) {
         float v[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) v[u] = row_loss[i + u * 1024];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) s += double(v[u]);
+        for (int u = 0; u < 8; ++u) s = dw_add(s, v[u]);
     }
-    for (; i < rows; i += 1024) s += double(row_loss[i]);
+    for (; i < rows; i += 1024) s = dw_add(s, row_loss[i]);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFullMask, s, o);
+    for (int o = 16; o > 0; o >>= 1) s = dw_add(s, dw_shfl_xor(s, o));
     if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = s;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        DWord t = part[threadIdx.x];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) t = dw_add(t, dw_shfl_xor(t, o));
+        if (threadIdx.x == 0) {
+            const bool finite = isfinite(t.hi) && isfinite(t.lo);
+            redo = finite ? 0 : 1;
+            if (finite) *mean = (double(t.hi) + double(t.lo)) / double(rows);
+        }
+    }
+    __syncthreads();
+    if (!redo) return;  // block-uniform
+    // Non-finite in fp32: the same fixed order in double.
+    double d = 0.0;
+    for (i = threadIdx.x; i < rows; i += 1024) d += double(row_loss[i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(kFullMask, d, o);
+    if ((threadIdx.x & 31) == 0) dpart[threadIdx.x >> 5] = d;
     __syncthreads();
     if (threadIdx.x == 0) {
         double t = 0.0;
-        for (int w = 0; w < 32; ++w) t += part[w];
+        for (int w = 0; w < 32; ++w) t += dpart[w];
         *mean = t / double(rows);
     }
 }

@@ -85,3 +85,39 @@ def test_long_rows_many_rows_per_cta(ro, cols):
     y = host(ro.rowops_softmax_fwd(xg))
     check_abs(y[idx], oracle.softmax_rows(x[idx]), 2e-6, "softmax long rows")
     assert ro.library().rowops_pipeline_timeouts() == 0
+
+
+def _exact_mean(rl):
+    import math
+    rl = np.asarray(rl, np.float64)
+    return math.fsum(rl.tolist()) / rl.size
+
+
+@pytest.mark.parametrize("rows", [1, 1000, 8192, 20001])
+def test_ce_mean_of_row_losses(ro, rows):
+    # the mean kernel alone: its result against the exactly rounded mean of the
+    # row losses the GPU wrote (independent of the row losses' own fp32 error)
+    c = inputs.cross_entropy(rows, rows=rows, cols=64)
+    _, rl, ml = ro.rowops_softmax_ce(gpu(c["logits"]), gpu(c["targets"]))
+    rl = host(rl)
+    ref = _exact_mean(rl)
+    assert abs(float(host(ml)[0]) - ref) <= 1e-12 * np.abs(rl.astype(np.float64)).mean()
+
+
+def test_ce_mean_non_finite_and_fp32_overflow(ro):
+    # an infinite row loss: the mean is +inf, as a double sum gives
+    x = np.zeros((3, 8), np.float32)
+    x[1, 2] = -np.inf
+    t = np.array([0, 2, 5], np.int32)
+    _, rl, ml = ro.rowops_softmax_ce(gpu(x), gpu(t))
+    assert np.isinf(host(rl)[1]) and host(ml)[0] == np.inf
+    assert oracle.softmax_cross_entropy(x, t, 1.0)[2] == np.inf
+    # finite losses of 1e37 whose sum overflows fp32: the mean stays finite
+    x = np.zeros((8192, 8), np.float32)
+    x[:, 3] = -1e37
+    t = np.full(8192, 3, np.int32)
+    _, rl, ml = ro.rowops_softmax_ce(gpu(x), gpu(t))
+    rl = host(rl)
+    got = float(host(ml)[0])
+    assert np.isfinite(got) and abs(got - _exact_mean(rl)) <= 1e-12 * abs(_exact_mean(rl))
+    assert abs(got - oracle.softmax_cross_entropy(x, t, 1.0)[2]) <= 1e-6 * 1e37
