@@ -18,6 +18,21 @@ static std::atomic<uint64_t> g_launches{0};
 
 void note_launches(int n) { g_launches.fetch_add(uint64_t(n), std::memory_order_relaxed); }
 
+int sm_count() {
+    // Per-device cache; concurrent first calls store the same value.
+    static std::atomic<int> cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+    if (dev < 64) {
+        const int c = cached[dev].load(std::memory_order_relaxed);
+        if (c) return c;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev < 64) cached[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
 }  // namespace rowops
 
 namespace {

@@ -311,16 +311,6 @@ bool launch_tma(const float* x, float* out, const int32_t* targets, float* aux, 
 
 }  // namespace
 
-int sm_count() {
-    static int cached[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
-    if (dev < 64 && cached[dev]) return cached[dev];
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    if (dev < 64) cached[dev] = n;
-    return n;
-}
 
 bool launch_lse_tma(const float* x, float* lse, int64_t rows, int64_t cols, cudaStream_t stream,
                     cudaError_t* err) {
