@@ -159,3 +159,35 @@ def test_rejected_calls_launch_nothing(lib):
     lib.rowops_topk_kept(A, A, 16, 64, 2, None)
     lib.rowops_softmax_ce(A, B, C, D, E, 4, 0, 0.25, None)
     assert lib.rowops_kernel_launches() == n0
+
+
+def test_header_is_plain_c(lib, tmp_path):
+    # include/rowops.h compiles as strict C99 and a C program links against the
+    # library and gets the documented answers (no call here reaches the GPU)
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    src = tmp_path / "abi_c.c"
+    src.write_text(r"""
+#include <stdio.h>
+#include <string.h>
+#include "rowops.h"
+int main(void) {
+    rowops_stream s = NULL;
+    if (strncmp(rowops_status_string(ROWOPS_ERR_SHAPE), "ROWOPS_ERR_SHAPE", 16) != 0) return 1;
+    if (rowops_softmax_fwd(NULL, NULL, -1, 4, s) != ROWOPS_ERR_SHAPE) return 2;
+    if (rowops_softmax_fwd(NULL, NULL, 0, 4, s) != ROWOPS_OK) return 3;
+    if (rowops_topk_kept(NULL, NULL, 4, 8, 9, s) != ROWOPS_ERR_SHAPE) return 4;
+    if (rowops_layernorm_bwd_workspace(0, 768) != 0) return 5;
+    puts("ok");
+    return 0;
+}
+""")
+    exe = tmp_path / "abi_c"
+    libpath = binding.LIB_PATH
+    subprocess.check_call(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                           "-I", os.path.join(ROOT, "include"), str(src), libpath,
+                           "-Wl,-rpath," + os.path.dirname(libpath), "-o", str(exe)])
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert out.returncode == 0 and out.stdout.strip() == "ok", (out.returncode, out.stdout, out.stderr)
