@@ -190,6 +190,7 @@ rms_bwd_rowblock(const float* __restrict__ dy, const float* __restrict__ gamma, 
 constexpr int kColTile = 32;
 constexpr int kColCluster = 8;
 constexpr int kColWarps = 16;
+constexpr int kColInFlight = 16;  // loads per thread in flight
 
 __device__ __forceinline__ void csum_arrive() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
@@ -215,16 +216,14 @@ column_sums_cluster(const float* __restrict__ in, float* __restrict__ out, int64
     float s = 0.f;
     if (col < cols) {
         int64_t i = r0 + w;
-        // four independent loads in flight, added in row order
-        for (; i + 3 * kColWarps < r1; i += 4 * kColWarps) {
-            const float a = __ldg(in + i * cols + col);
-            const float b = __ldg(in + (i + kColWarps) * cols + col);
-            const float c = __ldg(in + (i + 2 * kColWarps) * cols + col);
-            const float d = __ldg(in + (i + 3 * kColWarps) * cols + col);
-            s += a;
-            s += b;
-            s += c;
-            s += d;
+        // kColInFlight independent loads in flight (a warp reads one 128-byte
+        // row segment per load), added in row order
+        for (; i + (kColInFlight - 1) * kColWarps < r1; i += kColInFlight * kColWarps) {
+            float v[kColInFlight];
+#pragma unroll
+            for (int u = 0; u < kColInFlight; ++u) v[u] = __ldg(in + (i + u * kColWarps) * cols + col);
+#pragma unroll
+            for (int u = 0; u < kColInFlight; ++u) s += v[u];
         }
         for (; i < r1; i += kColWarps) s += __ldg(in + i * cols + col);
     }
