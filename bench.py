@@ -277,9 +277,9 @@ def kernel_fingerprint(op="softmax_ce"):
 
 
 def recorded_traffic(op):
-    """DRAM bytes per launch from the committed ncu summary (profiles/dram_traffic.md),
+    """DRAM bytes per launch from the committed ncu summary (profiles/tma_rows_ce_8192x50304_dram.md),
     if it was taken on the current kernel sources; else None."""
-    p = os.path.join(ROOT, "profiles", "dram_traffic.md")
+    p = os.path.join(ROOT, "profiles", "tma_rows_ce_8192x50304_dram.md")
     if not os.path.exists(p):
         return None
     if op not in KERNEL_SOURCES:
