@@ -28,7 +28,9 @@ struct Geom {
 
 // Calls f(Geom<LANES, NV, VEC>{}) with the group geometry for rows of `cols`
 // floats (see common.cuh), or returns false when a row is longer than one
-// warp can hold in registers (1024 floats vectorised, 256 scalar).
+// warp holds in registers (1024 floats, vectorised or scalar).  Scalar rows
+// keep the same registers per lane as vectorised ones (NV = 32 scalars against
+// NV = 8 float4s) and still coalesce: a warp's 32 consecutive floats per load.
 template <typename F>
 bool with_geometry(bool vec4, int64_t cols, F&& f) {
     if (vec4) {
@@ -50,6 +52,9 @@ bool with_geometry(bool vec4, int64_t cols, F&& f) {
         else if (cols <= 64) f(Geom<32, 2, 1>{});
         else if (cols <= 128) f(Geom<32, 4, 1>{});
         else if (cols <= 256) f(Geom<32, 8, 1>{});
+        else if (cols <= 512) f(Geom<32, 16, 1>{});
+        else if (cols <= 768) f(Geom<32, 24, 1>{});
+        else if (cols <= 1024) f(Geom<32, 32, 1>{});
         else return false;
     }
     return true;
@@ -86,13 +91,16 @@ inline unsigned row_grid(int64_t rows, int per_row = 1) {
 
 cudaError_t launch_softmax_fwd(const float* x, float* y, int64_t rows, int64_t cols, bool vec4,
                                cudaStream_t stream);
-// Vectorised rows too long for one warp: the cluster kernel of lse_ce.cu.
-// Returns false (nothing launched) when the row exceeds its capacity.
-bool launch_softmax_fwd_long(const float* x, float* y, int64_t rows, int64_t cols,
+// Rows too long for one warp: the TMA kernel (any 4-byte aligned rows), else
+// for vectorised rows the cluster kernel of lse_ce.cu.  Returns false
+// (nothing launched) when neither applies.
+bool launch_softmax_fwd_long(const float* x, float* y, int64_t rows, int64_t cols, bool vec4,
                              cudaStream_t stream, cudaError_t* err);
-// TMA-streamed long rows (tma_rows.cu): vectorised rows only; each returns
-// false, launching nothing, when the shape does not suit it (too short, or the
-// row does not fit in shared memory where it must stay resident).
+// TMA-streamed long rows (tma_rows.cu): rows of more than 1024 floats from
+// 4-byte aligned buffers (an output row must share its input row's alignment
+// modulo 16 bytes); each returns false, launching nothing, when the shape does
+// not suit it (the row does not fit in shared memory where it must stay
+// resident, or the alignments differ).
 bool launch_lse_tma(const float* x, float* lse, int64_t rows, int64_t cols, cudaStream_t stream,
                     cudaError_t* err);
 bool launch_ce_tma(const float* x, const int32_t* targets, float* grad, float* row_loss, int64_t rows,

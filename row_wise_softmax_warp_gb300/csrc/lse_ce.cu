@@ -456,7 +456,7 @@ cudaError_t launch_logsumexp(const float* x, float* lse, int64_t rows, int64_t c
     int nv = 0, cl = 0;
     cudaError_t err = cudaSuccess;
     if (!done) {
-        if (vec4 && launch_lse_tma(x, lse, rows, cols, stream, &err)) {
+        if (launch_lse_tma(x, lse, rows, cols, stream, &err)) {
         } else if (vec4 && long_row_config(cols / 4, &nv, &cl))
             err = launch_long<LongOp::kLse>(nv, cl, x, lse, nullptr, nullptr, rows, int(cols), 1.f,
                                             stream);
@@ -481,7 +481,7 @@ cudaError_t launch_softmax_ce(const float* logits, const int32_t* targets, float
     int nv = 0, cl = 0;
     cudaError_t err = cudaSuccess;
     if (!done) {
-        if (vec4 && launch_ce_tma(logits, targets, grad, row_loss, rows, cols, grad_scale, stream, &err)) {
+        if (launch_ce_tma(logits, targets, grad, row_loss, rows, cols, grad_scale, stream, &err)) {
         } else if (vec4 && long_row_config(cols / 4, &nv, &cl))
             err = launch_long<LongOp::kCe>(nv, cl, logits, grad, targets, row_loss, rows, int(cols),
                                            grad_scale, stream);
@@ -517,9 +517,10 @@ cudaError_t launch_row_mean(const float* row_loss, int64_t rows, double* mean_lo
 
 // Long vectorised rows of softmax_fwd use the cluster kernel; called from
 // softmax.cu's dispatcher through this hook.
-bool launch_softmax_fwd_long(const float* x, float* y, int64_t rows, int64_t cols,
+bool launch_softmax_fwd_long(const float* x, float* y, int64_t rows, int64_t cols, bool vec4,
                              cudaStream_t stream, cudaError_t* err) {
     if (launch_softmax_tma(x, y, rows, cols, stream, err)) return true;
+    if (!vec4) return false;
     int nv = 0, cl = 0;
     if (!long_row_config(cols / 4, &nv, &cl)) return false;
     *err = launch_long<LongOp::kSoftmax>(nv, cl, x, y, nullptr, nullptr, rows, int(cols), 1.f, stream);

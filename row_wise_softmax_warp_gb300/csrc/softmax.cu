@@ -563,7 +563,7 @@ cudaError_t launch_softmax_fwd(const float* x, float* y, int64_t rows, int64_t c
     });
     cudaError_t err = cudaSuccess;
     if (!done) {
-        if (vec4 && launch_softmax_fwd_long(x, y, rows, cols, stream, &err)) {
+        if (launch_softmax_fwd_long(x, y, rows, cols, vec4, stream, &err)) {
         } else if (vec4) {
             softmax_fwd_rowblock<4><<<row_grid(rows), kBlockThreads, 0, stream>>>(x, y, rows, cols);
         } else {

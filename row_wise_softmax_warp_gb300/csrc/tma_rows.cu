@@ -17,6 +17,14 @@
 // current row's gradient has been written from them.  HBM sees exactly one read
 // of every input element and one write of every output element.
 //
+// Rows need not start on a 16-byte boundary (cols % 4 != 0, or an offset
+// base): the row's first boundary splits off a head of h < 4 floats, the body
+// (a multiple of 4 floats) goes through the bulk copies, and the tail of
+// t < 4 floats after it is read with plain loads by consumer lanes, which also
+// write the head and tail outputs.  The output row must have the same
+// alignment modulo 16 bytes as the input row, so that the body's stores stay
+// 128-bit.
+//
 // exp(x - m) is evaluated as 2^((x - m)*log2(e)) with the ex2.approx
 // instruction.
 //
@@ -105,6 +113,26 @@ __device__ __forceinline__ void push4(float& m, float& s, const float4 v) {
          ex2((v.w - m) * kLog2e);
 }
 
+// Running (max, sum) over one value (head and tail floats of a row).
+__device__ __forceinline__ void push1(float& m, float& s, const float v) {
+    if (v > m) {
+        s *= ex2((m - v) * kLog2e);
+        m = v;
+    }
+    s += ex2((v - m) * kLog2e);
+}
+
+// Split of a row at its first 16-byte boundary: `head` floats before it
+// (0..3), then `body` floats (a multiple of 4) for the bulk copies; the
+// remaining cols - head - body (0..3) floats are the tail.  `src` is 4-byte
+// aligned (checked by the launcher).
+__device__ __forceinline__ void row_split(const float* src, int cols, int& head, int& body) {
+    const int mis = int((reinterpret_cast<uintptr_t>(src) >> 2) & 3);
+    head = (4 - mis) & 3;
+    if (head > cols) head = cols;
+    body = (cols - head) & ~3;
+}
+
 __device__ __forceinline__ void merge2(float& m, float& s, float m2, float s2) {
     const float mm = fmaxf(m, m2);
     if (mm == -INFINITY) return;
@@ -134,7 +162,6 @@ tma_rows(const float* x, float* out, const int32_t* __restrict__ targets, float*
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    const int nch = (cols + chunk - 1) / chunk;
     if constexpr (OP == RowOp::kCe) {
         // The mean-loss kernel may be scheduled now; it waits for this grid.
         asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
@@ -159,6 +186,10 @@ tma_rows(const float* x, float* out, const int32_t* __restrict__ targets, float*
         bool ok = true;
         for (int64_t row = blockIdx.x; ok && row < rows; row += gridDim.x) {
             const float* src = x + row * int64_t(cols);
+            int head, body;
+            row_split(src, cols, head, body);
+            src += head;
+            const int nch = (body + chunk - 1) / chunk;
             for (int k = 0; k < nch; ++k, ++n) {
                 const int s = int(n % nslot);
                 const uint64_t use = n / nslot;
@@ -167,7 +198,7 @@ tma_rows(const float* x, float* out, const int32_t* __restrict__ targets, float*
                     ok = false;
                     break;
                 }
-                const int cnt = min(chunk, cols - k * chunk);
+                const int cnt = min(chunk, body - k * chunk);
                 mbar_arrive_expect_tx(&full[s], uint32_t(cnt) * 4u);
                 bulk_load(buf + size_t(s) * chunk, src + size_t(k) * chunk, uint32_t(cnt) * 4u, &full[s]);
             }
@@ -189,7 +220,18 @@ tma_rows(const float* x, float* out, const int32_t* __restrict__ targets, float*
     uint64_t n = 0;
     int it = 0;
     for (int64_t row = blockIdx.x; row < rows; row += gridDim.x, ++it) {
+        const float* src = x + row * int64_t(cols);
+        int head, body;
+        row_split(src, cols, head, body);
+        const int nch = (body + chunk - 1) / chunk;
+        // Lanes 0..head-1 of consumer warp 0 own the head floats, lanes
+        // 0..tail-1 of consumer warp 1 the tail floats; `ej` is the column.
+        int ej = -1;
+        if (ct < head) ej = ct;
+        else if (ct >= 32 && ct - 32 < cols - head - body) ej = head + body + (ct - 32);
+        const float xe = ej >= 0 ? src[ej] : -INFINITY;  // coherent: softmax may run in place
         float m = -INFINITY, s = 0.f;
+        if (ej >= 0) push1(m, s, xe);
         for (int k = 0; k < nch; ++k) {
             const uint64_t q = n + k;
             const int slot = int(q % nslot);
@@ -197,7 +239,7 @@ tma_rows(const float* x, float* out, const int32_t* __restrict__ targets, float*
                 raise_abort(&abort_flag);
                 return;
             }
-            const int cnt4 = min(chunk, cols - k * chunk) >> 2;
+            const int cnt4 = min(chunk, body - k * chunk) >> 2;
             const float4* c4 = reinterpret_cast<const float4*>(buf + size_t(slot) * chunk);
             for (int i = ct; i < cnt4; i += kConsumers) push4(m, s, c4[i]);
             if constexpr (OP == RowOp::kLse) {
@@ -233,16 +275,27 @@ tma_rows(const float* x, float* out, const int32_t* __restrict__ targets, float*
                 if (ct == 0) {
                     float loss = __int_as_float(0x7fc00000);
                     if (t >= 0 && t < cols) {
-                        const uint64_t qt = n + t / chunk;
-                        loss = lse - buf[size_t(qt % nslot) * chunk + t % chunk];
+                        const int tb = t - head;  // position in the body
+                        if (tb >= 0 && tb < body) {
+                            const uint64_t qt = n + tb / chunk;
+                            loss = lse - buf[size_t(qt % nslot) * chunk + tb % chunk];
+                        } else {
+                            loss = lse - __ldg(src + t);
+                        }
                     }
                     aux[row] = loss;
                 }
             }
             float* dst = out + row * int64_t(cols);
+            if (ej >= 0) {
+                float p = ex2((xe - M) * kLog2e) * inv;
+                if constexpr (OP == RowOp::kCe) p = grad_scale * (p - (ej == t ? 1.f : 0.f));
+                dst[ej] = p;
+            }
+            dst += head;
             for (int k = 0; k < nch; ++k) {
                 const int slot = int((n + k) % nslot);
-                const int cnt4 = min(chunk, cols - k * chunk) >> 2;
+                const int cnt4 = min(chunk, body - k * chunk) >> 2;
                 const float4* c4 = reinterpret_cast<const float4*>(buf + size_t(slot) * chunk);
                 float4* d4 = reinterpret_cast<float4*>(dst + size_t(k) * chunk);
                 for (int i = ct; i < cnt4; i += kConsumers) {
@@ -253,7 +306,7 @@ tma_rows(const float* x, float* out, const int32_t* __restrict__ targets, float*
                     p.z = ex2((v.z - M) * kLog2e) * inv;
                     p.w = ex2((v.w - M) * kLog2e) * inv;
                     if constexpr (OP == RowOp::kCe) {
-                        const int j = k * chunk + 4 * i;
+                        const int j = head + k * chunk + 4 * i;
                         p.x = grad_scale * (p.x - (j == t ? 1.f : 0.f));
                         p.y = grad_scale * (p.y - (j + 1 == t ? 1.f : 0.f));
                         p.z = grad_scale * (p.z - (j + 2 == t ? 1.f : 0.f));
@@ -279,7 +332,12 @@ constexpr size_t kMaxDynSmem = 226 * 1024;  // 227 KB per block, less room for s
 template <RowOp OP>
 bool launch_tma(const float* x, float* out, const int32_t* targets, float* aux, int64_t rows,
                 int64_t cols, float grad_scale, cudaStream_t stream, cudaError_t* err) {
-    if (cols < 4 || cols % 4 != 0 || cols > INT32_MAX / 2) return false;
+    // Long rows only; 4-byte aligned buffers; for the ops that write rows, the
+    // output row has the input row's alignment modulo 16 bytes.
+    if (cols < 1024 || cols > INT32_MAX / 2) return false;
+    const uintptr_t xa = reinterpret_cast<uintptr_t>(x);
+    if ((xa & 3) != 0) return false;
+    if (OP != RowOp::kLse && ((reinterpret_cast<uintptr_t>(out) & 15) != (xa & 15))) return false;
     // A row is cut into equal chunks of at most kMaxChunk floats: every chunk
     // costs the pipeline a fixed ~0.5 us per SM, so chunks are kept large (on
     // GB300, 16 KB chunks left logsumexp at 0.70 of the HBM copy rate, 48-64 KB

@@ -121,3 +121,43 @@ def test_ce_mean_non_finite_and_fp32_overflow(ro):
     got = float(host(ml)[0])
     assert np.isfinite(got) and abs(got - _exact_mean(rl)) <= 1e-12 * abs(_exact_mean(rl))
     assert abs(got - oracle.softmax_cross_entropy(x, t, 1.0)[2]) <= 1e-6 * 1e37
+
+
+def _at_offset(a: np.ndarray, off: int) -> torch.Tensor:
+    """Device copy of `a` whose data starts `off` floats past a 256-byte boundary."""
+    a = np.ascontiguousarray(a, np.float32)
+    flat = torch.zeros(a.size + 8, dtype=torch.float32, device="cuda")
+    view = flat[off:off + a.size].view(a.shape)
+    view.copy_(torch.from_numpy(a).cuda())
+    return view
+
+
+@pytest.mark.parametrize("cols", [1025, 3001, 50257, 50258, 50259])
+@pytest.mark.parametrize("off", [0, 1, 3])
+def test_long_rows_not_on_16_byte_boundaries(ro, cols, off):
+    # rows of cols % 4 != 0 (and buffers offset by `off` floats) start at every
+    # position modulo 16 bytes: the long-row kernels split each row into a head,
+    # a bulk-copied body and a tail; 300 rows make every CTA walk several rows
+    rows = 300
+    c = inputs.cross_entropy(cols + off, rows=rows, cols=cols, outlier_frac=1e-3)
+    x, t = c["logits"], c["targets"]
+    # targets in the first and last four columns hit the head and tail floats
+    t[:8] = [0, 1, 2, 3, cols - 1, cols - 2, cols - 3, cols - 4]
+    xg = _at_offset(x, off)
+    idx = np.r_[0:12, 151:156, rows - 4:rows]
+    check_rel(host(ro.rowops_logsumexp(xg)), oracle.logsumexp_rows(x), f"lse {rows}x{cols}+{off}")
+    g = _at_offset(np.zeros_like(x), off)
+    rl = torch.empty(rows, device="cuda")
+    ml = torch.empty(1, dtype=torch.float64, device="cuda")
+    ro.rowops_softmax_ce(xg, gpu(t), g, rl, ml, grad_scale=c["grad_scale"])
+    gr, rlr, mlr = oracle.softmax_cross_entropy(x, t, c["grad_scale"])
+    check_abs(host(g)[idx], gr[idx], 2e-6 * c["grad_scale"], "ce grad")
+    check_rel(host(rl), rlr, "ce row loss")
+    check_rel(host(ml), [mlr], "ce mean loss")
+    ref = oracle.softmax_rows(x[idx])
+    y = _at_offset(np.zeros_like(x), off)
+    ro.rowops_softmax_fwd(xg, y)
+    check_abs(host(y)[idx], ref, 2e-6, "softmax")
+    ro.rowops_softmax_fwd(xg, xg)  # in place
+    check_abs(host(xg)[idx], ref, 2e-6, "softmax in place")
+    assert ro.library().rowops_pipeline_timeouts() == 0
