@@ -29,8 +29,9 @@ struct Geom {
 // Calls f(Geom<LANES, NV, VEC>{}) with the group geometry for rows of `cols`
 // floats (see common.cuh), or returns false when a row is longer than one
 // warp holds in registers (1024 floats, vectorised or scalar).  Scalar rows
-// keep the same registers per lane as vectorised ones (NV = 32 scalars against
-// NV = 8 float4s) and still coalesce: a warp's 32 consecutive floats per load.
+// keep the floats per lane of vectorised rows of the same length (NV = 32
+// scalars against NV = 8 float4s); groups of at least 8 lanes make each row's
+// share of a warp load one full 32-byte sector.
 template <typename F>
 bool with_geometry(bool vec4, int64_t cols, F&& f) {
     if (vec4) {
@@ -48,9 +49,9 @@ bool with_geometry(bool vec4, int64_t cols, F&& f) {
         if (cols <= 4) f(Geom<4, 1, 1>{});
         else if (cols <= 8) f(Geom<8, 1, 1>{});
         else if (cols <= 16) f(Geom<8, 2, 1>{});
-        else if (cols <= 32) f(Geom<16, 2, 1>{});
-        else if (cols <= 64) f(Geom<32, 2, 1>{});
-        else if (cols <= 128) f(Geom<32, 4, 1>{});
+        else if (cols <= 32) f(Geom<8, 4, 1>{});
+        else if (cols <= 64) f(Geom<8, 8, 1>{});
+        else if (cols <= 128) f(Geom<16, 8, 1>{});
         else if (cols <= 256) f(Geom<32, 8, 1>{});
         else if (cols <= 512) f(Geom<32, 16, 1>{});
         else if (cols <= 768) f(Geom<32, 24, 1>{});

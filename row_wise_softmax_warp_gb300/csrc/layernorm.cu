@@ -14,6 +14,10 @@
 //     partial per cluster to the workspace;
 //   stage 2 (ln_params_reduce): one thread per output column adds the
 //     cluster partials in increasing order.
+// Rows of 1025..8192 floats take a block-row stage 1 instead (ln_bwd_brow):
+// one CTA per row at a time, each thread keeping its columns' partials in
+// registers across the CTA's block of rows, one workspace slot per CTA.
+#include "block_rows.cuh"
 #include "common.cuh"
 #include "launch.h"
 
@@ -333,6 +337,168 @@ ln_bwd_rowblock(const float* __restrict__ dy, const float* __restrict__ gamma,
     }
 }
 
+// ------------------------------------------------------ block-row kernels
+// Rows of 1025..16384 floats (forward) or 1025..8192 floats (backward), one
+// CTA per row in registers (block_rows.cuh); the arithmetic of the group
+// kernels with block reductions.
+
+template <int NT, int NV, int VEC>
+__global__ void __launch_bounds__(NT)
+ln_fwd_brow(const float* __restrict__ x, const float* __restrict__ gamma, const float* __restrict__ beta,
+            float* __restrict__ out, float* __restrict__ xhat, float* __restrict__ inv_std, int64_t rows,
+            int cols, float eps) {
+    __shared__ float sc[4 * (NT / 32)];
+    BlockReduce<NT> red(sc);
+    const int nch = cols / VEC;
+    const float inv_cols = 1.0f / float(cols);
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const int64_t off = row * int64_t(cols);
+        const float shift = __ldg(x + off);  // the row's first entry
+        float v[NV][VEC];
+        float s = 0.f;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c = int(threadIdx.x) + k * NT;
+            if (c < nch) {
+                ld_chunk<VEC>(x + off + c * VEC, v[k]);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) s += v[k][e] - shift;
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) v[k][e] = 0.f;
+            }
+        }
+        const float mean = shift + red.sum(s) * inv_cols;
+        float q = 0.f;
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+            if (int(threadIdx.x) + k * NT < nch)
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    v[k][e] -= mean;
+                    q = fmaf(v[k][e], v[k][e], q);
+                }
+        const float r = 1.0f / sqrtf(red.sum(q) * inv_cols + eps);
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c = int(threadIdx.x) + k * NT;
+            if (c < nch) {
+                float gm[VEC], bt[VEC], h[VEC], o[VEC];
+                ld_chunk<VEC>(gamma + c * VEC, gm);
+                ld_chunk<VEC>(beta + c * VEC, bt);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    h[e] = v[k][e] * r;
+                    o[e] = fmaf(gm[e], h[e], bt[e]);
+                }
+                st_chunk<VEC>(xhat + off + c * VEC, h);
+                st_chunk<VEC>(out + off + c * VEC, o);
+            }
+        }
+        if (threadIdx.x == 0) inv_std[row] = r;
+    }
+}
+
+// Backward: the CTA walks a fixed block of rows; each thread keeps the
+// column partials of dgamma and dbeta for its own columns in registers and
+// writes them to the CTA's workspace slot at the end (stage 2,
+// ln_params_reduce, adds the slots in order).  8 floats of the row per thread.
+constexpr int64_t kLnBwdBrowMax = 8192;
+
+inline int ln_bwd_brow_threads(int64_t cols) { return cols <= 2048 ? 256 : (cols <= 4096 ? 512 : 1024); }
+
+template <typename F>
+bool with_ln_bwd_brow_geometry(bool vec4, int64_t cols, F&& f) {
+    if (cols <= 1024 || cols > kLnBwdBrowMax) return false;
+    if (vec4) {
+        if (cols <= 2048) f(BGeom<256, 2, 4>{});
+        else if (cols <= 4096) f(BGeom<512, 2, 4>{});
+        else f(BGeom<1024, 2, 4>{});
+    } else {
+        if (cols <= 2048) f(BGeom<256, 8, 1>{});
+        else if (cols <= 4096) f(BGeom<512, 8, 1>{});
+        else f(BGeom<1024, 8, 1>{});
+    }
+    return true;
+}
+
+template <int NT, int NV, int VEC>
+__global__ void __launch_bounds__(NT, 1024 / NT)
+ln_bwd_brow(const float* __restrict__ dy, const float* __restrict__ gamma, const float* __restrict__ xhat,
+            const float* __restrict__ inv_std, float* __restrict__ dx, float* __restrict__ ws, int64_t rows,
+            int cols, int64_t rows_per_cta) {
+    // Let the dependent stage-2 kernel be scheduled now; it waits for this
+    // grid's completion before reading the workspace.
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    __shared__ float sc[4 * (NT / 32)];
+    BlockReduce<NT> red(sc);
+    const int nch = cols / VEC;
+    const float inv_cols = 1.0f / float(cols);
+    const int64_t r_begin = int64_t(blockIdx.x) * rows_per_cta;
+    int64_t r_end = r_begin + rows_per_cta;
+    if (r_end > rows) r_end = rows;
+    float pg[NV][VEC], pb[NV][VEC];
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) pg[k][e] = pb[k][e] = 0.f;
+    for (int64_t row = r_begin; row < r_end; ++row) {  // block-uniform
+        const int64_t off = row * int64_t(cols);
+        float a[NV][VEC], h[NV][VEC];
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c = int(threadIdx.x) + k * NT;
+            if (c < nch) {
+                ld_chunk<VEC>(dy + off + c * VEC, a[k]);
+                ld_chunk<VEC>(xhat + off + c * VEC, h[k]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) a[k][e] = h[k][e] = 0.f;
+            }
+        }
+        const float r = __ldg(inv_std + row);
+        float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c = int(threadIdx.x) + k * NT;
+            if (c < nch) {
+                float gm[VEC];
+                ld_chunk<VEC>(gamma + c * VEC, gm);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    pg[k][e] = fmaf(a[k][e], h[k][e], pg[k][e]);
+                    pb[k][e] += a[k][e];
+                    a[k][e] *= gm[e];  // g' = dy * gamma
+                    s1 += a[k][e];
+                    s2 = fmaf(a[k][e], h[k][e], s2);
+                }
+            }
+        }
+        red.sum2(s1, s2);
+        s1 *= inv_cols;
+        s2 *= inv_cols;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c = int(threadIdx.x) + k * NT;
+            if (c < nch) {
+                float o[VEC];
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) o[e] = r * (a[k][e] - s1 - h[k][e] * s2);
+                st_chunk<VEC>(dx + off + c * VEC, o);
+            }
+        }
+    }
+    float* wg = ws + int64_t(blockIdx.x) * 2 * cols;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const int c = int(threadIdx.x) + k * NT;
+        if (c < nch) {
+            st_chunk<VEC>(wg + c * VEC, pg[k]);
+            st_chunk<VEC>(wg + cols + c * VEC, pb[k]);
+        }
+    }
+}
+
 // Stage 2: out[i] = sum_p ws[p][i] for i in [0, 2*cols).  A block covers 32
 // outputs with 8 warps: warp j adds partials j, j+8, j+16, ... in order (loads
 // coalesced across the 32 outputs), then thread i adds the 8 warp sums in warp
@@ -386,7 +552,12 @@ cudaError_t launch_layernorm_fwd(const float* x, const float* gamma, const float
             x, gamma, beta, out, xhat, inv_std, rows, int(cols), eps);
     });
     if (!done) {
-        if (vec4)
+        if (with_block_geometry(vec4, cols, kBlockRowMax, [&](auto geo) {
+                using G = decltype(geo);
+                ln_fwd_brow<G::NT, G::NV, G::VEC><<<block_row_grid(rows), G::NT, 0, stream>>>(
+                    x, gamma, beta, out, xhat, inv_std, rows, int(cols), eps);
+            })) {
+        } else if (vec4)
             ln_fwd_rowblock<4><<<row_grid(rows), kBlockThreads, 0, stream>>>(x, gamma, beta, out, xhat,
                                                                              inv_std, rows, cols, eps);
         else
@@ -397,18 +568,36 @@ cudaError_t launch_layernorm_fwd(const float* x, const float* gamma, const float
     return cudaGetLastError();
 }
 
+// Column partials of the backward: one per cluster of the group kernel, one
+// per resident CTA of the block-row kernel (1024 threads per SM), one
+// per block of the streaming kernel.
+int64_t ln_bwd_slots(int64_t rows, int64_t cols) {
+    if (cols > 1024 && cols <= kLnBwdBrowMax) {
+        const int sms = sm_count();
+        const int64_t p = int64_t(sms > 0 ? sms : 1) * (1024 / ln_bwd_brow_threads(cols));
+        return rows < p ? rows : p;
+    }
+    return ln_bwd_partials(rows);
+}
+
 size_t layernorm_bwd_workspace(int64_t rows, int64_t cols) {
     if (rows <= 0 || cols <= 0) return 0;
-    return size_t(ln_bwd_partials(rows)) * 2 * size_t(cols) * sizeof(float);
+    return size_t(ln_bwd_slots(rows, cols)) * 2 * size_t(cols) * sizeof(float);
 }
 
 cudaError_t launch_layernorm_bwd(const float* dy, const float* gamma, const float* xhat,
                                  const float* inv_std, float* dx, float* dgamma, float* dbeta,
                                  int64_t rows, int64_t cols, float* ws, bool vec4,
                                  cudaStream_t stream) {
-    const int64_t partials = ln_bwd_partials(rows);
+    const int64_t partials = ln_bwd_slots(rows, cols);
     cudaError_t err = cudaSuccess;
-    const bool done = with_geometry(vec4, cols, [&](auto geo) {
+    bool done = with_ln_bwd_brow_geometry(vec4, cols, [&](auto geo) {
+        using G = decltype(geo);
+        const int64_t per_cta = (rows + partials - 1) / partials;
+        ln_bwd_brow<G::NT, G::NV, G::VEC><<<unsigned(partials), G::NT, 0, stream>>>(
+            dy, gamma, xhat, inv_std, dx, ws, rows, int(cols), per_cta);
+    });
+    if (!done) done = with_geometry(vec4, cols, [&](auto geo) {
         using G = decltype(geo);
         constexpr int MAXC = G::LANES * G::NV * G::VEC;
         constexpr int GPB = kBlockThreads / G::LANES;

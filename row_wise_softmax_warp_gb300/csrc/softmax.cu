@@ -1,12 +1,15 @@
 // softmax.cu - softmax forward/backward, scaled causal attention softmax
 // forward/backward and hard-masked softmax.
 //
-// Two kernel shapes per op:
-//   *_group    : rows of up to 1024 floats (256 unaligned) held in registers by
-//                a group of LANES lanes (geometry in common.cuh); one HBM read
-//                and one HBM write per element.
+// Kernel shapes per op:
+//   *_group    : rows of up to 1024 floats held in registers by a group of
+//                LANES lanes (geometry in common.cuh); one HBM read and one
+//                HBM write per element.
+//   *_brow     : rows of 1025..16384 floats held in registers by one CTA
+//                (block_rows.cuh); one HBM read and one HBM write per element.
 //   *_rowblock : any row length and alignment; one 256-thread block per row,
 //                streaming the row from global memory once per pass.
+#include "block_rows.cuh"
 #include "common.cuh"
 #include "launch.h"
 
@@ -550,6 +553,256 @@ masked_rowblock(const float* x, const MaskT* __restrict__ mask, float* y, int64_
     }
 }
 
+// ------------------------------------------------------ block-row kernels
+// Rows of 1025..16384 floats, one CTA per row in registers (block_rows.cuh);
+// the same arithmetic as the group kernels above, with block reductions.
+
+// Loads the thread's NV chunks of a row (fill for chunks past the row).
+template <int NT, int NV, int VEC, bool COHERENT>
+__device__ __forceinline__ void brow_load(const float* r, int nch, float (&v)[NV][VEC], float fill) {
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const int c = int(threadIdx.x) + k * NT;
+        if (c < nch) {
+            if constexpr (COHERENT)
+                ld_chunk_coherent<VEC>(r + c * VEC, v[k]);
+            else
+                ld_chunk<VEC>(r + c * VEC, v[k]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) v[k][e] = fill;
+        }
+    }
+}
+
+template <int NT, int NV, int VEC>
+__global__ void __launch_bounds__(NT)
+softmax_fwd_brow(const float* x, float* y, int64_t rows, int cols) {
+    __shared__ float sc[4 * (NT / 32)];
+    BlockReduce<NT> red(sc);
+    const int nch = cols / VEC;
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const int64_t off = row * int64_t(cols);
+        float v[NV][VEC];
+        brow_load<NT, NV, VEC, true>(x + off, nch, v, -INFINITY);  // y may be x
+        float m = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) m = fmaxf(m, v[k][e]);
+        m = red.max(m);
+        float s = 0.f;
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                v[k][e] = exp_shifted(v[k][e], m);
+                s += v[k][e];
+            }
+        s = red.sum(s);
+        const float inv = 1.0f / s;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c = int(threadIdx.x) + k * NT;
+            if (c < nch) {
+                float o[VEC];
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) o[e] = v[k][e] * inv;
+                st_chunk<VEC>(y + off + c * VEC, o);
+            }
+        }
+    }
+}
+
+template <int NT, int NV, int VEC>
+__global__ void __launch_bounds__(NT)
+softmax_bwd_brow(const float* __restrict__ y, const float* __restrict__ dy, float* __restrict__ dx,
+                 int64_t rows, int cols) {
+    __shared__ float sc[4 * (NT / 32)];
+    BlockReduce<NT> red(sc);
+    const int nch = cols / VEC;
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const int64_t off = row * int64_t(cols);
+        float a[NV][VEC], b[NV][VEC];
+        brow_load<NT, NV, VEC, false>(y + off, nch, a, 0.f);
+        brow_load<NT, NV, VEC, false>(dy + off, nch, b, 0.f);
+        float dot = 0.f;
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) dot = fmaf(a[k][e], b[k][e], dot);
+        dot = red.sum(dot);
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c = int(threadIdx.x) + k * NT;
+            if (c < nch) {
+                float o[VEC];
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) o[e] = a[k][e] * (b[k][e] - dot);
+                st_chunk<VEC>(dx + off + c * VEC, o);
+            }
+        }
+    }
+}
+
+// Causal attention forward: only the visible prefix (keys 0..q) is read.
+template <int NT, int NV, int VEC>
+__global__ void __launch_bounds__(NT)
+attn_fwd_brow(const float* __restrict__ s, float* __restrict__ p, int64_t rows, int cols, int64_t seq_len,
+              float scale) {
+    __shared__ float sc[4 * (NT / 32)];
+    BlockReduce<NT> red(sc);
+    const int nch = cols / VEC;
+    const float sl = scale * kLog2e;
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const int64_t off = row * int64_t(cols);
+        const int q = int(row % seq_len);
+        const int nvis = q + 1 < cols ? q + 1 : cols;
+        float v[NV][VEC];
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c0 = (int(threadIdx.x) + k * NT) * VEC;
+            if (c0 < nvis) {
+                ld_chunk<VEC>(s + off + c0, v[k]);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) v[k][e] = (c0 + e < nvis) ? v[k][e] : -INFINITY;
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) v[k][e] = -INFINITY;
+            }
+        }
+        float m = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) m = fmaxf(m, v[k][e]);
+        m = red.max(m);
+        float sum = 0.f;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c0 = (int(threadIdx.x) + k * NT) * VEC;
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                v[k][e] = (c0 + e < nvis) ? ex2_approx((v[k][e] - m) * sl) : 0.f;
+                sum += v[k][e];
+            }
+        }
+        sum = red.sum(sum);
+        const float inv = 1.0f / sum;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c = int(threadIdx.x) + k * NT;
+            if (c < nch) {
+                float o[VEC];
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) o[e] = v[k][e] * inv;
+                st_chunk<VEC>(p + off + c * VEC, o);
+            }
+        }
+    }
+}
+
+template <int NT, int NV, int VEC>
+__global__ void __launch_bounds__(NT)
+attn_bwd_brow(const float* __restrict__ p, const float* __restrict__ dp, float* __restrict__ ds, int64_t rows,
+              int cols, int64_t seq_len, float scale) {
+    __shared__ float sc[4 * (NT / 32)];
+    BlockReduce<NT> red(sc);
+    const int nch = cols / VEC;
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const int64_t off = row * int64_t(cols);
+        const int q = int(row % seq_len);
+        const int nvis = q + 1 < cols ? q + 1 : cols;
+        float a[NV][VEC], b[NV][VEC];
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c0 = (int(threadIdx.x) + k * NT) * VEC;
+            if (c0 < nvis) {
+                ld_chunk<VEC>(p + off + c0, a[k]);
+                ld_chunk<VEC>(dp + off + c0, b[k]);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e)
+                    if (c0 + e >= nvis) a[k][e] = b[k][e] = 0.f;
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) a[k][e] = b[k][e] = 0.f;
+            }
+        }
+        float dot = 0.f;
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) dot = fmaf(a[k][e], b[k][e], dot);
+        dot = red.sum(dot);
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c = int(threadIdx.x) + k * NT;
+            if (c < nch) {
+                const int c0 = c * VEC;
+                float o[VEC];
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) o[e] = (c0 + e < nvis) ? scale * a[k][e] * (b[k][e] - dot) : 0.f;
+                st_chunk<VEC>(ds + off + c0, o);
+            }
+        }
+    }
+}
+
+template <typename MaskT, int NT, int NV, int VEC>
+__global__ void __launch_bounds__(NT)
+masked_brow(const float* x, const MaskT* __restrict__ mask, float* y, int64_t rows, int cols) {
+    __shared__ float sc[4 * (NT / 32)];
+    BlockReduce<NT> red(sc);
+    const int nch = cols / VEC;
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const int64_t off = row * int64_t(cols);
+        float v[NV][VEC];
+        bool al[NV][VEC];
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c = int(threadIdx.x) + k * NT;
+            if (c < nch) {
+                ld_chunk_coherent<VEC>(x + off + c * VEC, v[k]);  // y may be x
+                ld_mask<VEC>(mask + off + c * VEC, al[k]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) al[k][e] = false;
+            }
+        }
+        float m = -INFINITY;
+        int n_allowed = 0;
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e)
+                if (al[k][e]) {
+                    m = fmaxf(m, v[k][e]);
+                    ++n_allowed;
+                }
+        red.max_count(m, n_allowed);
+        float s = 0.f;
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                v[k][e] = al[k][e] ? exp_shifted(v[k][e], m) : 0.f;
+                s += v[k][e];
+            }
+        s = red.sum(s);
+        const float inv = n_allowed > 0 ? 1.0f / s : 0.f;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c = int(threadIdx.x) + k * NT;
+            if (c < nch) {
+                float o[VEC];
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) o[e] = al[k][e] ? v[k][e] * inv : 0.f;
+                st_chunk<VEC>(y + off + c * VEC, o);
+            }
+        }
+    }
+}
+
 }  // namespace
 
 // ------------------------------------------------------------ launchers
@@ -563,7 +816,15 @@ cudaError_t launch_softmax_fwd(const float* x, float* y, int64_t rows, int64_t c
     });
     cudaError_t err = cudaSuccess;
     if (!done) {
-        if (launch_softmax_fwd_long(x, y, rows, cols, vec4, stream, &err)) {
+        // Up to 8192 floats: on GB300 the TMA kernel is ahead at 16384 (51.8
+        // against 64.2 us on 2048 rows), the block-row kernel below (45.7
+        // against 66.2 us on 4096 x 8192, 45.8 against 195 us on 16384 x 2048).
+        if (with_block_geometry(vec4, cols, 8192, [&](auto geo) {
+                using G = decltype(geo);
+                softmax_fwd_brow<G::NT, G::NV, G::VEC>
+                    <<<block_row_grid(rows), G::NT, 0, stream>>>(x, y, rows, int(cols));
+            })) {
+        } else if (launch_softmax_fwd_long(x, y, rows, cols, vec4, stream, &err)) {
         } else if (vec4) {
             softmax_fwd_rowblock<4><<<row_grid(rows), kBlockThreads, 0, stream>>>(x, y, rows, cols);
         } else {
@@ -583,7 +844,12 @@ cudaError_t launch_softmax_bwd(const float* y, const float* dy, float* dx, int64
             <<<group_grid(rows, G::LANES), kBlockThreads, 0, stream>>>(y, dy, dx, rows, int(cols));
     });
     if (!done) {
-        if (vec4)
+        if (with_block_geometry(vec4, cols, kBlockRowMax, [&](auto geo) {
+                using G = decltype(geo);
+                softmax_bwd_brow<G::NT, G::NV, G::VEC>
+                    <<<block_row_grid(rows), G::NT, 0, stream>>>(y, dy, dx, rows, int(cols));
+            })) {
+        } else if (vec4)
             softmax_bwd_rowblock<4><<<row_grid(rows), kBlockThreads, 0, stream>>>(y, dy, dx, rows, cols);
         else
             softmax_bwd_rowblock<1><<<row_grid(rows), kBlockThreads, 0, stream>>>(y, dy, dx, rows, cols);
@@ -618,7 +884,12 @@ cudaError_t launch_attn_fwd(const float* s, float* p, int64_t rows, int64_t cols
                                                   stream>>>(s, p, rows, int(cols), seq_len, scale);
     });
     if (!done) {
-        if (vec4)
+        if (with_block_geometry(vec4, cols, kBlockRowMax, [&](auto geo) {
+                using G = decltype(geo);
+                attn_fwd_brow<G::NT, G::NV, G::VEC>
+                    <<<block_row_grid(rows), G::NT, 0, stream>>>(s, p, rows, int(cols), seq_len, scale);
+            })) {
+        } else if (vec4)
             attn_fwd_rowblock<4><<<row_grid(rows), kBlockThreads, 0, stream>>>(s, p, rows, cols,
                                                                                seq_len, scale);
         else
@@ -639,7 +910,12 @@ cudaError_t launch_attn_bwd(const float* p, const float* dp, float* ds, int64_t 
                                                             scale);
     });
     if (!done) {
-        if (vec4)
+        if (with_block_geometry(vec4, cols, kBlockRowMax, [&](auto geo) {
+                using G = decltype(geo);
+                attn_bwd_brow<G::NT, G::NV, G::VEC>
+                    <<<block_row_grid(rows), G::NT, 0, stream>>>(p, dp, ds, rows, int(cols), seq_len, scale);
+            })) {
+        } else if (vec4)
             attn_bwd_rowblock<4><<<row_grid(rows), kBlockThreads, 0, stream>>>(p, dp, ds, rows, cols,
                                                                                seq_len, scale);
         else
@@ -659,7 +935,12 @@ cudaError_t launch_masked_impl(const float* x, const MaskT* mask, float* y, int6
             <<<group_grid(rows, G::LANES), kBlockThreads, 0, stream>>>(x, mask, y, rows, int(cols));
     });
     if (!done) {
-        if (vec4)
+        if (with_block_geometry(vec4, cols, kBlockRowMax, [&](auto geo) {
+                using G = decltype(geo);
+                masked_brow<MaskT, G::NT, G::NV, G::VEC>
+                    <<<block_row_grid(rows), G::NT, 0, stream>>>(x, mask, y, rows, int(cols));
+            })) {
+        } else if (vec4)
             masked_rowblock<MaskT, 4><<<row_grid(rows), kBlockThreads, 0, stream>>>(x, mask, y, rows, cols);
         else
             masked_rowblock<MaskT, 1><<<row_grid(rows), kBlockThreads, 0, stream>>>(x, mask, y, rows, cols);

@@ -15,7 +15,8 @@ def _upper(rows, seq):
     return np.arange(seq)[None, :] > q[:, None]
 
 
-@pytest.mark.parametrize("seq", [1, 2, 3, 5, 8, 31, 64, 100, 256, 516, 600, 768, 1020, 1024, 1028, 1500, 2048])
+@pytest.mark.parametrize("seq", [1, 2, 3, 5, 8, 31, 64, 100, 256, 516, 600, 768, 1020, 1024, 1028, 1500, 2048,
+                                 3001, 4096])
 @pytest.mark.parametrize("misalign", [False, True])
 def test_attention_shapes(ro, seq, misalign):
     heads = 3 if seq <= 256 else 1

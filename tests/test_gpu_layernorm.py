@@ -33,7 +33,7 @@ def test_layernorm_workload_4096x768(ro):
 
 
 @pytest.mark.parametrize("cols", [1, 2, 3, 4, 7, 16, 33, 64, 127, 128, 256, 257, 768, 1000, 1024, 1028,
-                                  3000, 4096])
+                                  1536, 2049, 3000, 4096, 8192, 8193, 12000, 16384, 16388])
 @pytest.mark.parametrize("misalign", [False, True])
 def test_layernorm_shapes(ro, cols, misalign):
     _run(ro, inputs.layernorm(cols, rows=45, cols=cols), misalign)
@@ -43,6 +43,14 @@ def test_layernorm_shapes(ro, cols, misalign):
 def test_layernorm_row_counts(ro, rows):
     # covers empty CTAs and clusters, ragged last blocks and the capped partial count
     _run(ro, inputs.layernorm(rows, rows=rows, cols=256))
+
+
+@pytest.mark.parametrize("rows,cols", [(2000, 2048), (700, 4100), (333, 8192)])
+@pytest.mark.parametrize("misalign", [False, True])
+def test_layernorm_block_rows_many_rows_per_cta(ro, rows, cols, misalign):
+    # rows of 1025..8192 floats: each CTA of the block-row backward walks
+    # several rows and carries its column partials across them
+    _run(ro, inputs.layernorm(rows + cols, rows=rows, cols=cols), misalign)
 
 
 def test_layernorm_eps_zero_and_constant_rows(ro):

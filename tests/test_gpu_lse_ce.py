@@ -10,7 +10,8 @@ from row_wise_softmax_warp_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
 
-COLS = [1, 3, 4, 7, 32, 64, 129, 256, 1000, 1024, 1028, 3001, 4096, 8192, 50304, 50305, 131072, 140000]
+COLS = [1, 3, 4, 7, 32, 64, 129, 256, 1000, 1024, 1028, 1536, 3001, 4096, 8192, 16384, 16385, 50304, 50305,
+        131072, 140000]
 
 
 @pytest.mark.parametrize("cols", COLS)

@@ -25,7 +25,7 @@ def test_router_workload_scaled(ro):
     assert np.array_equal(kept_x, oracle.topk_kept(x, 2).astype(np.float32))
 
 
-MASK_COLS = [1, 2, 3, 4, 7, 8, 16, 33, 64, 128, 255, 256, 1024, 1028, 5000]
+MASK_COLS = [1, 2, 3, 4, 7, 8, 16, 33, 64, 128, 255, 256, 1024, 1028, 2048, 5000, 16384, 16385]
 
 
 @pytest.mark.parametrize("cols", MASK_COLS)

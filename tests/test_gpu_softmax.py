@@ -13,7 +13,7 @@ from row_wise_softmax_warp_gb300 import inputs
 pytestmark = pytest.mark.gpu
 
 COLS = [1, 2, 3, 4, 5, 8, 12, 16, 31, 32, 33, 64, 100, 127, 128, 129, 255, 256, 257, 768, 1000,
-        1024, 1028, 2048, 4097, 8192, 50304, 140000]
+        1024, 1028, 1536, 2048, 3000, 4097, 8192, 12000, 16384, 16385, 50304, 140000]
 
 
 def _x(rows, cols, seed):
