@@ -22,9 +22,11 @@
  *   - A pointer may be NULL only when the buffer it names is empty.
  *   - Buffers must not overlap unless the entry point says so
  *     (ROWOPS_ERR_ALIAS); overlap is checked by address range.
- *   - Any alignment is accepted.  16-byte aligned buffers with cols % 4 == 0
- *     take the 128-bit vector path; others take a scalar path with the same
- *     results up to fp32 rounding order.
+ *   - Every pointer must be aligned to its element type (4 bytes for float
+ *     and int32_t, 8 for double, any for uint8_t); a pointer that is not is
+ *     ROWOPS_ERR_ALIGN.  Beyond that any alignment is accepted: 16-byte
+ *     aligned buffers with cols % 4 == 0 take the 128-bit vector path; others
+ *     take scalar paths with the same results up to fp32 rounding order.
  *   - Reductions use a fixed order: repeated calls on the same inputs give
  *     bit-identical outputs.
  *
@@ -50,7 +52,8 @@ typedef enum {
     ROWOPS_ERR_SHAPE = 2,     /* bad size, k, seq_len, scale, eps or grad_scale */
     ROWOPS_ERR_ALIAS = 3,     /* buffers overlap where the op forbids it */
     ROWOPS_ERR_WORKSPACE = 4, /* workspace missing, misaligned or too small */
-    ROWOPS_ERR_CUDA = 5       /* the CUDA runtime reported an error at launch */
+    ROWOPS_ERR_CUDA = 5,      /* the CUDA runtime reported an error at launch */
+    ROWOPS_ERR_ALIGN = 6      /* a pointer is not aligned to its element type */
 } rowops_status;
 
 /* Same object as cudaStream_t. */

@@ -9,6 +9,9 @@
 #include <cmath>
 #include <cstdint>
 
+#include <initializer_list>
+#include <utility>
+
 #include "rowops.h"
 #include "launch.h"
 
@@ -52,6 +55,15 @@ bool overlap(Buf a, Buf b) {
 
 bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) & (n - 1)) == 0; }
 
+// Every pointer aligned to its element type (4 bytes for float and int32, 8 for
+// double): the scalar paths need no more, and less would make the kernels'
+// accesses misaligned on the GPU.
+bool elems_aligned(std::initializer_list<std::pair<const void*, uintptr_t>> ps) {
+    for (const auto& p : ps)
+        if (!aligned(p.first, p.second)) return false;
+    return true;
+}
+
 // rows, cols >= 0; cols < 2^31; rows*cols*8 bytes fits in int64.
 int check_dims(int64_t rows, int64_t cols) {
     if (rows < 0 || cols < 0 || cols > INT32_MAX) return ROWOPS_ERR_SHAPE;
@@ -75,6 +87,7 @@ const char* rowops_status_string(int status) {
         case ROWOPS_ERR_ALIAS: return "ROWOPS_ERR_ALIAS: buffers overlap where the op forbids it";
         case ROWOPS_ERR_WORKSPACE: return "ROWOPS_ERR_WORKSPACE: workspace missing, misaligned or too small";
         case ROWOPS_ERR_CUDA: return "ROWOPS_ERR_CUDA: the CUDA runtime reported a launch error";
+        case ROWOPS_ERR_ALIGN: return "ROWOPS_ERR_ALIGN: a pointer is not aligned to its element type";
         default: return "ROWOPS: unknown status";
     }
 }
@@ -85,6 +98,7 @@ int rowops_softmax_fwd(const float* x, float* y, int64_t rows, int64_t cols, row
     if (int e = check_dims(rows, cols)) return e;
     if (rows == 0 || cols == 0) return ROWOPS_OK;
     if (!x || !y) return ROWOPS_ERR_NULL;
+    if (!elems_aligned({{x, 4}, {y, 4}})) return ROWOPS_ERR_ALIGN;
     const int64_t n = rows * cols * 4;
     if (static_cast<const void*>(x) != y && overlap({x, n}, {y, n})) return ROWOPS_ERR_ALIAS;
     const bool vec4 = cols % 4 == 0 && aligned(x, 16) && aligned(y, 16);
@@ -96,6 +110,7 @@ int rowops_softmax_bwd(const float* y, const float* dy, float* dx, int64_t rows,
     if (int e = check_dims(rows, cols)) return e;
     if (rows == 0 || cols == 0) return ROWOPS_OK;
     if (!y || !dy || !dx) return ROWOPS_ERR_NULL;
+    if (!elems_aligned({{y, 4}, {dy, 4}, {dx, 4}})) return ROWOPS_ERR_ALIGN;
     const int64_t n = rows * cols * 4;
     if (overlap({dx, n}, {y, n}) || overlap({dx, n}, {dy, n})) return ROWOPS_ERR_ALIAS;
     const bool vec4 = cols % 4 == 0 && aligned(y, 16) && aligned(dy, 16) && aligned(dx, 16);
@@ -114,6 +129,7 @@ int rowops_attn_softmax_fwd(const float* scores, float* p, int64_t rows, int64_t
     if (int e = check_attn(rows, cols, seq_len, scale)) return e;
     if (rows == 0) return ROWOPS_OK;
     if (!scores || !p) return ROWOPS_ERR_NULL;
+    if (!elems_aligned({{scores, 4}, {p, 4}})) return ROWOPS_ERR_ALIGN;
     const int64_t n = rows * cols * 4;
     if (overlap({scores, n}, {p, n})) return ROWOPS_ERR_ALIAS;
     const bool vec4 = cols % 4 == 0 && aligned(scores, 16) && aligned(p, 16);
@@ -125,6 +141,7 @@ int rowops_attn_softmax_bwd(const float* p, const float* dp, float* ds, int64_t 
     if (int e = check_attn(rows, cols, seq_len, scale)) return e;
     if (rows == 0) return ROWOPS_OK;
     if (!p || !dp || !ds) return ROWOPS_ERR_NULL;
+    if (!elems_aligned({{p, 4}, {dp, 4}, {ds, 4}})) return ROWOPS_ERR_ALIGN;
     const int64_t n = rows * cols * 4;
     if (overlap({ds, n}, {p, n}) || overlap({ds, n}, {dp, n})) return ROWOPS_ERR_ALIAS;
     const bool vec4 = cols % 4 == 0 && aligned(p, 16) && aligned(dp, 16) && aligned(ds, 16);
@@ -136,6 +153,7 @@ int rowops_masked_softmax(const float* x, const uint8_t* mask, float* y, int64_t
     if (int e = check_dims(rows, cols)) return e;
     if (rows == 0 || cols == 0) return ROWOPS_OK;
     if (!x || !mask || !y) return ROWOPS_ERR_NULL;
+    if (!elems_aligned({{x, 4}, {y, 4}})) return ROWOPS_ERR_ALIGN;
     const int64_t n = rows * cols * 4;
     if (static_cast<const void*>(x) != y && overlap({x, n}, {y, n})) return ROWOPS_ERR_ALIAS;
     if (overlap({mask, rows * cols}, {y, n}) || overlap({mask, rows * cols}, {x, n}))
@@ -148,6 +166,7 @@ int rowops_logsumexp(const float* x, float* lse, int64_t rows, int64_t cols, row
     if (int e = check_dims(rows, cols)) return e;
     if (rows == 0) return ROWOPS_OK;
     if (!lse || (cols > 0 && !x)) return ROWOPS_ERR_NULL;
+    if (!elems_aligned({{x, 4}, {lse, 4}})) return ROWOPS_ERR_ALIGN;
     if (overlap({x, rows * cols * 4}, {lse, rows * 4})) return ROWOPS_ERR_ALIAS;
     const bool vec4 = cols % 4 == 0 && aligned(x, 16);
     return to_status(rowops::launch_logsumexp(x, lse, rows, cols, vec4, st(stream)));
@@ -160,6 +179,7 @@ int rowops_softmax_ce(const float* logits, const int32_t* targets, float* grad, 
     if (cols == 0 || !std::isfinite(grad_scale)) return ROWOPS_ERR_SHAPE;
     if (rows == 0) return ROWOPS_OK;
     if (!logits || !targets || !grad || !row_loss || !mean_loss) return ROWOPS_ERR_NULL;
+    if (!elems_aligned({{logits, 4}, {targets, 4}, {grad, 4}, {row_loss, 4}, {mean_loss, 8}})) return ROWOPS_ERR_ALIGN;
     const int64_t n = rows * cols * 4;
     const Buf in[2] = {{logits, n}, {targets, rows * 4}};
     const Buf out[3] = {{grad, n}, {row_loss, rows * 4}, {mean_loss, 8}};
@@ -181,6 +201,7 @@ int rowops_layernorm_fwd(const float* x, const float* gamma, const float* beta, 
     if (cols == 0 || !std::isfinite(eps) || eps < 0.f) return ROWOPS_ERR_SHAPE;
     if (rows == 0) return ROWOPS_OK;
     if (!x || !gamma || !beta || !out || !xhat || !inv_std) return ROWOPS_ERR_NULL;
+    if (!elems_aligned({{x, 4}, {gamma, 4}, {beta, 4}, {out, 4}, {xhat, 4}, {inv_std, 4}})) return ROWOPS_ERR_ALIGN;
     const int64_t n = rows * cols * 4;
     const Buf in[3] = {{x, n}, {gamma, cols * 4}, {beta, cols * 4}};
     const Buf o[3] = {{out, n}, {xhat, n}, {inv_std, rows * 4}};
@@ -207,6 +228,7 @@ int rowops_layernorm_bwd(const float* dy, const float* gamma, const float* xhat,
     if (cols == 0) return ROWOPS_ERR_SHAPE;
     if (rows == 0) return ROWOPS_OK;
     if (!dy || !gamma || !xhat || !inv_std || !dx || !dgamma || !dbeta) return ROWOPS_ERR_NULL;
+    if (!elems_aligned({{dy, 4}, {gamma, 4}, {xhat, 4}, {inv_std, 4}, {dx, 4}, {dgamma, 4}, {dbeta, 4}})) return ROWOPS_ERR_ALIGN;
     const size_t need = rowops::layernorm_bwd_workspace(rows, cols);
     if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return ROWOPS_ERR_WORKSPACE;
     const int64_t n = rows * cols * 4;
@@ -229,6 +251,7 @@ int rowops_topk_kept(const float* x, float* kept, int64_t rows, int64_t cols, in
     if (k < 1 || k > cols) return ROWOPS_ERR_SHAPE;
     if (rows == 0) return ROWOPS_OK;
     if (!x || !kept) return ROWOPS_ERR_NULL;
+    if (!elems_aligned({{x, 4}, {kept, 4}})) return ROWOPS_ERR_ALIGN;
     const int64_t n = rows * cols * 4;
     if (overlap({x, n}, {kept, n})) return ROWOPS_ERR_ALIAS;
     const bool vec4 = cols % 4 == 0 && aligned(x, 16) && aligned(kept, 16);
@@ -241,6 +264,7 @@ int rowops_router_masked_topk(const float* x, const uint8_t* mask, float* p, flo
     if (k < 1 || k > cols) return ROWOPS_ERR_SHAPE;
     if (rows == 0) return ROWOPS_OK;
     if (!x || !mask || !p || !kept) return ROWOPS_ERR_NULL;
+    if (!elems_aligned({{x, 4}, {p, 4}, {kept, 4}})) return ROWOPS_ERR_ALIGN;
     const int64_t n = rows * cols * 4;
     if (static_cast<const void*>(x) != p && overlap({x, n}, {p, n})) return ROWOPS_ERR_ALIAS;
     if (overlap({mask, rows * cols}, {p, n}) || overlap({mask, rows * cols}, {x, n}) ||
@@ -257,6 +281,7 @@ int rowops_top_k_rows(const float* x, float* values, float* indices, int64_t row
     if (k < 1 || k > cols || cols > (int64_t(1) << 24)) return ROWOPS_ERR_SHAPE;
     if (rows == 0) return ROWOPS_OK;
     if (!x || !values || !indices) return ROWOPS_ERR_NULL;
+    if (!elems_aligned({{x, 4}, {values, 4}, {indices, 4}})) return ROWOPS_ERR_ALIGN;
     const int64_t n = rows * cols * 4, nk = rows * k * 4;
     if (overlap({values, nk}, {x, n}) || overlap({indices, nk}, {x, n}) ||
         overlap({values, nk}, {indices, nk}))
@@ -272,6 +297,7 @@ int rowops_rmsnorm_fwd(const float* x, const float* gamma, float* out, float* ro
     if (cols == 0 || !std::isfinite(eps) || eps < 0.f) return ROWOPS_ERR_SHAPE;
     if (rows == 0) return ROWOPS_OK;
     if (!x || !gamma || !out || !row_rms) return ROWOPS_ERR_NULL;
+    if (!elems_aligned({{x, 4}, {gamma, 4}, {out, 4}, {row_rms, 4}})) return ROWOPS_ERR_ALIGN;
     const int64_t n = rows * cols * 4;
     const Buf in[2] = {{x, n}, {gamma, cols * 4}};
     const Buf o[2] = {{out, n}, {row_rms, rows * 4}};
@@ -288,6 +314,7 @@ int rowops_rmsnorm_bwd(const float* dy, const float* gamma, const float* x, cons
     if (cols == 0) return ROWOPS_ERR_SHAPE;
     if (rows == 0) return ROWOPS_OK;
     if (!dy || !gamma || !x || !row_rms || !dx || !gamma_terms) return ROWOPS_ERR_NULL;
+    if (!elems_aligned({{dy, 4}, {gamma, 4}, {x, 4}, {row_rms, 4}, {dx, 4}, {gamma_terms, 4}})) return ROWOPS_ERR_ALIGN;
     const int64_t n = rows * cols * 4;
     const Buf in[4] = {{dy, n}, {gamma, cols * 4}, {x, n}, {row_rms, rows * 4}};
     const Buf o[2] = {{dx, n}, {gamma_terms, n}};
@@ -308,6 +335,7 @@ int rowops_column_sums(const float* in, float* out, int64_t rows, int64_t cols, 
     if (!std::isfinite(beta)) return ROWOPS_ERR_SHAPE;
     if (cols == 0) return ROWOPS_OK;
     if (!out || (rows > 0 && !in)) return ROWOPS_ERR_NULL;
+    if (!elems_aligned({{in, 4}, {out, 4}})) return ROWOPS_ERR_ALIGN;
     if (overlap({in, rows * cols * 4}, {out, cols * 4})) return ROWOPS_ERR_ALIAS;
     return to_status(rowops::launch_column_sums(in, out, rows, cols, beta, st(stream)));
 }
@@ -317,6 +345,7 @@ int rowops_masked_softmax_fmask(const float* x, const float* mask, float* y, int
     if (int e = check_dims(rows, cols)) return e;
     if (rows == 0 || cols == 0) return ROWOPS_OK;
     if (!x || !mask || !y) return ROWOPS_ERR_NULL;
+    if (!elems_aligned({{x, 4}, {mask, 4}, {y, 4}})) return ROWOPS_ERR_ALIGN;
     const int64_t n = rows * cols * 4;
     if (static_cast<const void*>(x) != y && overlap({x, n}, {y, n})) return ROWOPS_ERR_ALIAS;
     if (overlap({mask, n}, {y, n}) || overlap({mask, n}, {x, n})) return ROWOPS_ERR_ALIAS;
@@ -329,6 +358,7 @@ int rowops_lrp_softmax_rows(const float* x, const float* y, const float* r, floa
     if (int e = check_dims(rows, cols)) return e;
     if (rows == 0 || cols == 0) return ROWOPS_OK;
     if (!x || !y || !r || !r_in) return ROWOPS_ERR_NULL;
+    if (!elems_aligned({{x, 4}, {y, 4}, {r, 4}, {r_in, 4}})) return ROWOPS_ERR_ALIGN;
     const int64_t n = rows * cols * 4;
     if (overlap({r_in, n}, {x, n}) || overlap({r_in, n}, {y, n}) || overlap({r_in, n}, {r, n}))
         return ROWOPS_ERR_ALIAS;
@@ -341,6 +371,7 @@ int rowops_argmax_onehot(const float* x, float* out, int64_t rows, int64_t cols,
     if (int e = check_dims(rows, cols)) return e;
     if (rows == 0 || cols == 0) return ROWOPS_OK;
     if (!x || !out) return ROWOPS_ERR_NULL;
+    if (!elems_aligned({{x, 4}, {out, 4}})) return ROWOPS_ERR_ALIGN;
     const int64_t n = rows * cols * 4;
     if (overlap({x, n}, {out, n})) return ROWOPS_ERR_ALIAS;
     const bool vec4 = cols % 4 == 0 && aligned(x, 16) && aligned(out, 16);
@@ -353,6 +384,7 @@ static int ce2_checks(const float* x, const float* w, float* grad, float* row_lo
     if (cols == 0 || !std::isfinite(grad_scale)) return ROWOPS_ERR_SHAPE;
     if (rows == 0) return -1;  // nothing to do
     if (!x || !w || !row_loss || !mean_loss || (grad_required && !grad)) return ROWOPS_ERR_NULL;
+    if (!elems_aligned({{x, 4}, {w, 4}, {grad, 4}, {row_loss, 4}, {mean_loss, 8}})) return ROWOPS_ERR_ALIGN;
     const int64_t n = rows * cols * 4;
     const Buf in[2] = {{x, n}, {w, n}};
     const Buf out[3] = {{grad, grad ? n : 0}, {row_loss, rows * 4}, {mean_loss, 8}};

@@ -11,7 +11,7 @@ import __graft_entry__
 from row_wise_softmax_warp_gb300 import binding
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-OK, NULL, SHAPE, ALIAS, WORKSPACE, CUDA = 0, 1, 2, 3, 4, 5
+OK, NULL, SHAPE, ALIAS, WORKSPACE, CUDA, ALIGN = 0, 1, 2, 3, 4, 5, 6
 
 A = 0x7000_0000_0000  # fake, 256-byte aligned device addresses far apart
 B = 0x7100_0000_0000
@@ -40,7 +40,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for s in range(6):
+    for s in range(7):
         assert lib.rowops_status_string(s).startswith(b"ROWOPS")
     assert b"unknown" in lib.rowops_status_string(99)
 
@@ -72,6 +72,28 @@ def test_null_pointers(lib):
     assert lib.rowops_topk_kept(None, B, 2, 4, 1, None) == NULL
 
 
+def test_element_alignment(lib):
+    # a float pointer that is not 4-byte aligned (or a double that is not
+    # 8-byte aligned) is refused before any launch; byte masks may sit anywhere
+    n0 = lib.rowops_kernel_launches()
+    assert lib.rowops_softmax_fwd(A + 2, B, 2, 4, None) == ALIGN
+    assert lib.rowops_softmax_fwd(A, B + 1, 2, 4, None) == ALIGN
+    assert lib.rowops_softmax_bwd(A, B, C + 2, 2, 4, None) == ALIGN
+    assert lib.rowops_attn_softmax_fwd(A + 2, B, 8, 8, 8, 0.5, None) == ALIGN
+    assert lib.rowops_attn_softmax_bwd(A, B + 2, C, 8, 8, 8, 0.5, None) == ALIGN
+    assert lib.rowops_logsumexp(A, B + 2, 2, 4, None) == ALIGN
+    assert lib.rowops_softmax_ce(A, B + 2, C, D, E, 2, 4, 0.5, None) == ALIGN  # int32 targets
+    assert lib.rowops_softmax_ce(A, B, C, D, E + 4, 2, 4, 0.5, None) == ALIGN  # double mean
+    assert lib.rowops_layernorm_fwd(A, B, C + 2, D, E, F, 2, 4, 1e-5, None) == ALIGN
+    assert lib.rowops_layernorm_bwd(A, B, C, D + 2, E, F, G, 2, 4, W, 1 << 20, None) == ALIGN
+    assert lib.rowops_topk_kept(A, B + 2, 2, 4, 1, None) == ALIGN
+    assert lib.rowops_masked_softmax_fmask(A, B + 2, C, 2, 4, None) == ALIGN
+    assert lib.rowops_soft_ce(A, B, C, D + 2, E, 2, 4, 0.5, None) == ALIGN
+    assert lib.rowops_teacher_ce(A, B, C, D, E + 4, 2, 4, 0.5, None) == ALIGN
+    assert lib.rowops_masked_softmax(A + 2, B + 1, C, 2, 4, None) == ALIGN
+    assert lib.rowops_kernel_launches() == n0
+
+
 def test_aliasing(lib):
     n = 16 * 64 * 4
     assert lib.rowops_softmax_fwd(A, A + 64, 16, 64, None) == ALIAS       # partial overlap
@@ -82,7 +104,7 @@ def test_aliasing(lib):
     assert lib.rowops_masked_softmax(A, A + 128, B, 16, 64, None) == ALIAS  # mask inside x
     assert lib.rowops_logsumexp(A, A + 8, 16, 64, None) == ALIAS
     assert lib.rowops_softmax_ce(A, B, A, D, E, 16, 64, 0.1, None) == ALIAS        # grad == logits
-    assert lib.rowops_softmax_ce(A, B, C, D, D + 4, 16, 64, 0.1, None) == ALIAS    # mean in row_loss
+    assert lib.rowops_softmax_ce(A, B, C, D, D + 8, 16, 64, 0.1, None) == ALIAS    # mean in row_loss
     assert lib.rowops_layernorm_fwd(A, B, C, D, D, E, 16, 64, 1e-5, None) == ALIAS  # out == xhat
     assert lib.rowops_layernorm_bwd(A, B, C, D, A, F, G, 16, 64, W, 1 << 20, None) == ALIAS
     assert lib.rowops_layernorm_bwd(A, B, C, D, E, F, F, 16, 64, W, 1 << 20, None) == ALIAS
