@@ -6,13 +6,15 @@
 //             gamma_terms_ij = g_ij x_ij / rms_i   (per-row gamma contributions)
 //   column sums  out_j = beta * out_j + sum_i in_ij
 //
-// Forward and backward are group kernels (geometry of common.cuh) with a
-// streaming fallback.  Column sums need no workspace: a cluster of 8 CTAs owns a
+// Forward and backward are group kernels (geometry of common.cuh), block-row
+// kernels for rows of 1025..16384 floats (block_rows.cuh) and a streaming
+// fallback.  Column sums need no workspace: a cluster of 8 CTAs owns a
 // tile of 32 columns and splits the rows into 8 consecutive ranges; inside a
 // CTA warp w adds rows w, w+16, ... of its range in order, the 16 warps are
 // combined in warp order through shared memory and the 8 CTAs in rank order
 // through distributed shared memory.  The association is fixed, so results are
 // deterministic (a blocked order, not one sequential pass over the rows).
+#include "block_rows.cuh"
 #include "common.cuh"
 #include "launch.h"
 
@@ -185,6 +187,104 @@ rms_bwd_rowblock(const float* __restrict__ dy, const float* __restrict__ gamma, 
     }
 }
 
+// ------------------------------------------------------ block-row kernels
+// Rows of 1025..16384 floats, one CTA per row in registers (block_rows.cuh).
+
+template <int NT, int NV, int VEC>
+__global__ void __launch_bounds__(NT)
+rms_fwd_brow(const float* __restrict__ x, const float* __restrict__ gamma, float* __restrict__ out,
+             float* __restrict__ row_rms, int64_t rows, int cols, float eps) {
+    __shared__ float sc[4 * (NT / 32)];
+    BlockReduce<NT> red(sc);
+    const int nch = cols / VEC;
+    const float inv_cols = 1.0f / float(cols);
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const int64_t off = row * int64_t(cols);
+        float v[NV][VEC];
+        float ss = 0.f;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c = int(threadIdx.x) + k * NT;
+            if (c < nch) {
+                ld_chunk<VEC>(x + off + c * VEC, v[k]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) v[k][e] = 0.f;
+            }
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) ss = fmaf(v[k][e], v[k][e], ss);
+        }
+        const float rms = sqrtf(red.sum(ss) * inv_cols + eps);
+        const float inv = 1.0f / rms;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c = int(threadIdx.x) + k * NT;
+            if (c < nch) {
+                float gm[VEC], o[VEC];
+                ld_chunk<VEC>(gamma + c * VEC, gm);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) o[e] = gm[e] * (v[k][e] * inv);
+                st_chunk<VEC>(out + off + c * VEC, o);
+            }
+        }
+        if (threadIdx.x == 0) row_rms[row] = rms;
+    }
+}
+
+template <int NT, int NV, int VEC>
+__global__ void __launch_bounds__(NT)
+rms_bwd_brow(const float* __restrict__ dy, const float* __restrict__ gamma, const float* __restrict__ x,
+             const float* __restrict__ row_rms, float* __restrict__ dx, float* __restrict__ terms, int64_t rows,
+             int cols) {
+    __shared__ float sc[4 * (NT / 32)];
+    BlockReduce<NT> red(sc);
+    const int nch = cols / VEC;
+    const float inv_cols = 1.0f / float(cols);
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const int64_t off = row * int64_t(cols);
+        float a[NV][VEC], h[NV][VEC];
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c = int(threadIdx.x) + k * NT;
+            if (c < nch) {
+                ld_chunk<VEC>(dy + off + c * VEC, a[k]);
+                ld_chunk<VEC>(x + off + c * VEC, h[k]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) a[k][e] = h[k][e] = 0.f;
+            }
+        }
+        const float inv = 1.0f / __ldg(row_rms + row);
+        float s = 0.f;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c = int(threadIdx.x) + k * NT;
+            if (c < nch) {
+                float gm[VEC];
+                ld_chunk<VEC>(gamma + c * VEC, gm);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) s = fmaf(a[k][e] * gm[e], h[k][e], s);
+            }
+        }
+        const float c2 = red.sum(s) * inv_cols * inv * inv;  // mean(g' x) / r^2
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c = int(threadIdx.x) + k * NT;
+            if (c < nch) {
+                float gm[VEC], o[VEC], t[VEC];
+                ld_chunk<VEC>(gamma + c * VEC, gm);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    o[e] = (a[k][e] * gm[e] - h[k][e] * c2) * inv;
+                    t[e] = a[k][e] * h[k][e] * inv;
+                }
+                st_chunk<VEC>(dx + off + c * VEC, o);
+                st_chunk<VEC>(terms + off + c * VEC, t);
+            }
+        }
+    }
+}
+
 // ----------------------------------------------------------- column sums
 
 constexpr int kColTile = 32;
@@ -257,7 +357,12 @@ cudaError_t launch_rmsnorm_fwd(const float* x, const float* gamma, float* out, f
             x, gamma, out, row_rms, rows, int(cols), eps);
     });
     if (!done) {
-        if (vec4)
+        if (with_block_geometry(vec4, cols, kBlockRowMax, [&](auto geo) {
+                using G = decltype(geo);
+                rms_fwd_brow<G::NT, G::NV, G::VEC><<<block_row_grid(rows), G::NT, 0, stream>>>(
+                    x, gamma, out, row_rms, rows, int(cols), eps);
+            })) {
+        } else if (vec4)
             rms_fwd_rowblock<4><<<row_grid(rows), kBlockThreads, 0, stream>>>(x, gamma, out, row_rms, rows, cols, eps);
         else
             rms_fwd_rowblock<1><<<row_grid(rows), kBlockThreads, 0, stream>>>(x, gamma, out, row_rms, rows, cols, eps);
@@ -275,7 +380,12 @@ cudaError_t launch_rmsnorm_bwd(const float* dy, const float* gamma, const float*
             dy, gamma, x, row_rms, dx, terms, rows, int(cols));
     });
     if (!done) {
-        if (vec4)
+        if (with_block_geometry(vec4, cols, kBlockRowMax, [&](auto geo) {
+                using G = decltype(geo);
+                rms_bwd_brow<G::NT, G::NV, G::VEC><<<block_row_grid(rows), G::NT, 0, stream>>>(
+                    dy, gamma, x, row_rms, dx, terms, rows, int(cols));
+            })) {
+        } else if (vec4)
             rms_bwd_rowblock<4><<<row_grid(rows), kBlockThreads, 0, stream>>>(dy, gamma, x, row_rms, dx, terms,
                                                                               rows, cols);
         else

@@ -3,7 +3,7 @@
     python -m row_wise_softmax_warp_gb300.run_op --op softmax_ce --rows 1024 --cols 50304 --reps 3
 
 Ops: softmax_fwd, softmax_bwd, attn_fwd, attn_bwd (cols = seq_len), logsumexp,
-softmax_ce, layernorm_fwd, layernorm_bwd, masked_softmax, topk_kept,
+softmax_ce, layernorm_fwd, layernorm_bwd, rmsnorm_fwd, rmsnorm_bwd, masked_softmax, topk_kept,
 router_masked_topk, top_k_rows, argmax_onehot.  Inputs
 follow the workload distributions of ``inputs``; the L2 is flushed (512 MiB
 write) before every call.  Prints the median CUDA-event time per call.
@@ -60,6 +60,14 @@ def make(op: str, rows: int, cols: int, dev):
         ws = torch.empty(ro.rowops_layernorm_bwd_workspace(rows, cols), dtype=torch.uint8, device=dev)
         dx, dg, db = torch.empty_like(x), torch.empty_like(gm), torch.empty_like(gm)
         return lambda: ro.rowops_layernorm_bwd(dy, gm, xh, rs, dx, dg, db, workspace=ws)
+    if op in ("rmsnorm_fwd", "rmsnorm_bwd"):
+        n = inputs.layernorm(0, rows=rows, cols=cols)
+        x, gm, dy = t(n["x"]), t(n["gamma"]), t(n["dy"])
+        out, rr = ro.rowops_rmsnorm_fwd(x, gm, eps=n["eps"])
+        if op == "rmsnorm_fwd":
+            return lambda: ro.rowops_rmsnorm_fwd(x, gm, out, rr, eps=n["eps"])
+        dx, terms = torch.empty_like(x), torch.empty_like(x)
+        return lambda: ro.rowops_rmsnorm_bwd(dy, gm, x, rr, dx, terms)
     if op in ("masked_softmax", "topk_kept"):
         r = inputs.router(0, rows=rows, cols=cols)
         x, m = t(r["x"]), t(r["mask"])

@@ -36,7 +36,8 @@ def test_rmsnorm_4096x768(ro):
     _run(ro, inputs.layernorm(0))
 
 
-@pytest.mark.parametrize("cols", [1, 3, 4, 33, 128, 256, 257, 768, 1024, 1028, 3000])
+@pytest.mark.parametrize("cols", [1, 3, 4, 33, 128, 256, 257, 768, 1024, 1028, 2048, 3000, 4096, 8192, 16384,
+                                  16385])
 @pytest.mark.parametrize("misalign", [False, True])
 def test_rmsnorm_shapes(ro, cols, misalign):
     _run(ro, inputs.layernorm(cols, rows=41, cols=cols), misalign)
