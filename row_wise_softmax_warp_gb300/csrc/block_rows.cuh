@@ -106,6 +106,26 @@ struct BlockReduce {
         b = rb;
     }
 
+    // Two maxima in one round.
+    __device__ __forceinline__ void max2(float& a, float& b) {
+        a = group_max<32>(a);
+        b = group_max<32>(b);
+        float* p = next();
+        if ((threadIdx.x & 31) == 0) {
+            p[threadIdx.x >> 5] = a;
+            p[W + (threadIdx.x >> 5)] = b;
+        }
+        __syncthreads();
+        float ra = p[0], rb = p[W];
+#pragma unroll
+        for (int i = 1; i < W; ++i) {
+            ra = fmaxf(ra, p[i]);
+            rb = fmaxf(rb, p[W + i]);
+        }
+        a = ra;
+        b = rb;
+    }
+
     // Max of a float and sum of an int in one round (the int is carried as
     // its bit pattern; counts are far below 2^24, so float adds would do, but
     // the bits keep it exact whatever the count).

@@ -108,6 +108,12 @@ bool launch_ce_tma(const float* x, const int32_t* targets, float* grad, float* r
                    int64_t cols, float grad_scale, cudaStream_t stream, cudaError_t* err);
 bool launch_softmax_tma(const float* x, float* y, int64_t rows, int64_t cols, cudaStream_t stream,
                         cudaError_t* err);
+// Two-input long rows (weighted-logits and fixed-teacher CE): x and w must
+// share their alignment modulo 16 bytes; grad (which may be NULL) may differ.
+bool launch_soft_ce_tma(const float* x, const float* w, float* grad, float* row_loss, int64_t rows, int64_t cols,
+                        float grad_scale, cudaStream_t stream, cudaError_t* err);
+bool launch_teacher_ce_tma(const float* s, const float* t, float* grad, float* row_loss, int64_t rows,
+                           int64_t cols, float grad_scale, cudaStream_t stream, cudaError_t* err);
 cudaError_t launch_softmax_bwd(const float* y, const float* dy, float* dx, int64_t rows,
                                int64_t cols, bool vec4, cudaStream_t stream);
 cudaError_t launch_attn_fwd(const float* s, float* p, int64_t rows, int64_t cols, int64_t seq_len,

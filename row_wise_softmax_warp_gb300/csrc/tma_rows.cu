@@ -322,6 +322,228 @@ tma_rows(const float* x, float* out, const int32_t* __restrict__ targets, float*
     }
 }
 
+// Bounded wait for slot use q of the ring; false (after raising the abort) on
+// timeout or abort.
+__device__ __forceinline__ bool wait_use(uint64_t* full, int nslot, uint64_t q, volatile int* abort_flag) {
+    if (mbar_wait(&full[int(q % nslot)], uint32_t((q / nslot) & 1), abort_flag)) return true;
+    raise_abort(abort_flag);
+    return false;
+}
+
+// The consumer warps exchange 4 floats each through `red` (double-buffered by
+// the rendezvous count rv); every warp gets all of them in `all`.
+__device__ __forceinline__ bool rendezvous4(float (*red)[kConsumerWarps][4], uint64_t* red_bar, int cw, int lane,
+                                           uint32_t& rv, const float (&mine)[4], float (&all)[kConsumerWarps][4],
+                                           volatile int* abort_flag) {
+    const int par = int(rv & 1);
+    if (lane == 0) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) red[par][cw][i] = mine[i];
+        mbar_arrive(&red_bar[par]);
+    }
+    if (!mbar_wait(&red_bar[par], (rv >> 1) & 1, abort_flag)) {
+        raise_abort(abort_flag);
+        return false;
+    }
+    ++rv;
+    for (int q = 0; q < kConsumerWarps; ++q)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) all[q][i] = red[par][q][i];
+    return true;
+}
+
+// ----------------------------------------------- two-input rows, two passes
+// Weighted-logits and fixed-teacher cross-entropy on long rows: x (logits or
+// student) and w (weights or teacher logits) stream through the ring as
+// chunk pairs (x_k, w_k), twice per row: pass 0 folds the running (max, sum)
+// of x and of the teacher (or the weight sum), pass 1 forms the loss and the
+// gradient.  A CTA has one row pair in flight, so on 152 SMs the second pass
+// reads rows that the first pass brought into the L2 a moment earlier: HBM sees
+// one read of each input element and one write of each gradient element.
+// Rows are split at their first 16-byte boundary as above; x and w share
+// their alignment modulo 16 bytes (checked by the launcher); a gradient on
+// another 16-byte phase is written with scalar stores.  The kernel choice does
+// not depend on the gradient, so the row losses are the same bits with and
+// without it.
+template <bool TEACHER>
+__global__ void __launch_bounds__(kTmaThreads, 1)
+tma_rows2(const float* x, const float* w, float* grad, float* __restrict__ row_loss, int64_t rows, int cols,
+          int chunk, int nslot, float grad_scale, bool grad_vec) {
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    float* buf = reinterpret_cast<float*>(smem_raw);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + size_t(nslot) * chunk * sizeof(float));
+    uint64_t* empty = full + nslot;
+    __shared__ uint64_t red_bar[2];
+    __shared__ float red[2][kConsumerWarps][4];
+    __shared__ volatile int abort_flag;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    // The mean-loss kernel may be scheduled now; it waits for this grid.
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+
+    if (tid == 0) {
+        for (int s = 0; s < nslot; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumerWarps);
+        }
+        mbar_init(&red_bar[0], kConsumerWarps);
+        mbar_init(&red_bar[1], kConsumerWarps);
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        // ------------------------------------------------------- producer
+        if (lane != 0) return;
+        uint64_t n = 0;
+        bool ok = true;
+        for (int64_t row = blockIdx.x; ok && row < rows; row += gridDim.x) {
+            int head, body;
+            row_split(x + row * int64_t(cols), cols, head, body);
+            const float* src[2] = {x + row * int64_t(cols) + head, w + row * int64_t(cols) + head};
+            const int nch = (body + chunk - 1) / chunk;
+            for (int pass = 0; ok && pass < 2; ++pass)
+                for (int k = 0; ok && k < nch; ++k)
+                    for (int in = 0; in < 2; ++in, ++n) {
+                        const int s = int(n % nslot);
+                        const uint64_t use = n / nslot;
+                        if (use > 0 && !mbar_wait(&empty[s], uint32_t((use - 1) & 1), &abort_flag)) {
+                            raise_abort(&abort_flag);
+                            ok = false;
+                            break;
+                        }
+                        const int cnt = min(chunk, body - k * chunk);
+                        mbar_arrive_expect_tx(&full[s], uint32_t(cnt) * 4u);
+                        bulk_load(buf + size_t(s) * chunk, src[in] + size_t(k) * chunk, uint32_t(cnt) * 4u,
+                                  &full[s]);
+                    }
+        }
+        if (!ok) {
+            // Let the copies already issued land before the CTA's shared memory goes away.
+            const uint64_t first = n > uint64_t(nslot) ? n - nslot : 0;
+            for (uint64_t j = first; j < n; ++j) {
+                volatile int never = 0;
+                mbar_wait(&full[j % nslot], uint32_t((j / nslot) & 1), &never);
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------- consumers
+    const int ct = tid - 32;
+    const int cw = warp - 1;
+    uint64_t n = 0;    // slot uses consumed
+    uint32_t rv = 0;   // rendezvous so far
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const float* xr = x + row * int64_t(cols);
+        const float* wr = w + row * int64_t(cols);
+        int head, body;
+        row_split(xr, cols, head, body);
+        const int nch = (body + chunk - 1) / chunk;
+        int ej = -1;  // head (warp 0) and tail (warp 1) lanes, as in tma_rows
+        if (ct < head) ej = ct;
+        else if (ct >= 32 && ct - 32 < cols - head - body) ej = head + body + (ct - 32);
+        const float xe = ej >= 0 ? __ldg(xr + ej) : -INFINITY;
+        const float we = ej >= 0 ? __ldg(wr + ej) : (TEACHER ? -INFINITY : 0.f);
+        // pass 0: (max, sum) of x; teacher (max, sum) or the weight sum
+        float ma = -INFINITY, sa = 0.f, mb = -INFINITY, sb = 0.f;
+        if (ej >= 0) {
+            push1(ma, sa, xe);
+            if constexpr (TEACHER) push1(mb, sb, we); else sb += we;
+        }
+        for (int k = 0; k < nch; ++k, n += 2) {
+            if (!wait_use(full, nslot, n, &abort_flag) || !wait_use(full, nslot, n + 1, &abort_flag)) return;
+            const int cnt4 = min(chunk, body - k * chunk) >> 2;
+            const float4* ca = reinterpret_cast<const float4*>(buf + size_t(n % nslot) * chunk);
+            const float4* cb = reinterpret_cast<const float4*>(buf + size_t((n + 1) % nslot) * chunk);
+            for (int i = ct; i < cnt4; i += kConsumers) {
+                push4(ma, sa, ca[i]);
+                const float4 b = cb[i];
+                if constexpr (TEACHER) push4(mb, sb, b); else sb += (b.x + b.y) + (b.z + b.w);
+            }
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&empty[n % nslot]);
+                mbar_arrive(&empty[(n + 1) % nslot]);
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            merge2(ma, sa, __shfl_xor_sync(kFullMask, ma, o), __shfl_xor_sync(kFullMask, sa, o));
+            if constexpr (TEACHER)
+                merge2(mb, sb, __shfl_xor_sync(kFullMask, mb, o), __shfl_xor_sync(kFullMask, sb, o));
+            else
+                sb += __shfl_xor_sync(kFullMask, sb, o);
+        }
+        float all[kConsumerWarps][4];
+        const float mine[4] = {ma, sa, mb, sb};
+        if (!rendezvous4(red, red_bar, cw, lane, rv, mine, all, &abort_flag)) return;
+        float MA = all[0][0], SA = all[0][1], MB = all[0][2], SB = all[0][3];
+        for (int q = 1; q < kConsumerWarps; ++q) {
+            merge2(MA, SA, all[q][0], all[q][1]);
+            if constexpr (TEACHER) merge2(MB, SB, all[q][2], all[q][3]); else SB += all[q][3];
+        }
+        const float lse = MA + logf(SA);
+        const float inv_sa = 1.0f / SA;
+        const float qs = TEACHER ? 1.0f / SB : 1.f;
+        // pass 1: loss and gradient
+        float loss = 0.f;
+        float* dst = grad != nullptr ? grad + row * int64_t(cols) : nullptr;
+        auto element = [&](float a, float b, float& o) {
+            const float q = TEACHER ? ex2((b - MB) * kLog2e) * qs : b;
+            loss = fmaf(q, lse - a, loss);
+            const float p = ex2((a - MA) * kLog2e) * inv_sa;
+            o = TEACHER ? grad_scale * (p - q) : grad_scale * (p * SB - q);
+        };
+        if (ej >= 0) {
+            float o;
+            element(xe, we, o);
+            if (dst != nullptr) dst[ej] = o;
+        }
+        for (int k = 0; k < nch; ++k, n += 2) {
+            if (!wait_use(full, nslot, n, &abort_flag) || !wait_use(full, nslot, n + 1, &abort_flag)) return;
+            const int cnt4 = min(chunk, body - k * chunk) >> 2;
+            const float4* ca = reinterpret_cast<const float4*>(buf + size_t(n % nslot) * chunk);
+            const float4* cb = reinterpret_cast<const float4*>(buf + size_t((n + 1) % nslot) * chunk);
+            float* dk = dst != nullptr ? dst + head + size_t(k) * chunk : nullptr;
+            for (int i = ct; i < cnt4; i += kConsumers) {
+                const float4 a = ca[i], b = cb[i];
+                float4 o;
+                element(a.x, b.x, o.x);
+                element(a.y, b.y, o.y);
+                element(a.z, b.z, o.z);
+                element(a.w, b.w, o.w);
+                if (dk != nullptr) {
+                    if (grad_vec) {
+                        reinterpret_cast<float4*>(dk)[i] = o;
+                    } else {  // grad on another 16-byte phase than x: four stores
+                        dk[4 * i] = o.x;
+                        dk[4 * i + 1] = o.y;
+                        dk[4 * i + 2] = o.z;
+                        dk[4 * i + 3] = o.w;
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&empty[n % nslot]);
+                mbar_arrive(&empty[(n + 1) % nslot]);
+            }
+        }
+        loss = group_sum<32>(loss);
+        const float mine2[4] = {loss, 0.f, 0.f, 0.f};
+        if (!rendezvous4(red, red_bar, cw, lane, rv, mine2, all, &abort_flag)) return;
+        if (ct == 0) {
+            float l = all[0][0];
+            for (int q = 1; q < kConsumerWarps; ++q) l += all[q][0];
+            row_loss[row] = l;
+        }
+    }
+}
+
 constexpr int64_t kMaxChunk = 16384;       // floats per bulk copy, at most
 constexpr size_t kRingBytes = 200 * 1024;   // target ring size (whole rows resident)
 // Streaming ring (logsumexp).  On GB300, 8192 x 50304: 3 slots of 12576 floats
@@ -367,6 +589,38 @@ bool launch_tma(const float* x, float* out, const int32_t* targets, float* aux, 
     return true;
 }
 
+
+// Two-input rows (tma_rows2): chunks of at most 12288 floats, a ring of whole
+// chunk pairs in ~192 KB.
+constexpr int64_t kMaxChunk2 = 12288;
+constexpr size_t kRingBytes2 = 192 * 1024;
+
+template <bool TEACHER>
+bool launch_tma2(const float* x, const float* w, float* grad, float* row_loss, int64_t rows, int64_t cols,
+                 float grad_scale, cudaStream_t stream, cudaError_t* err) {
+    if (cols < 1024 || cols > INT32_MAX / 2) return false;
+    const uintptr_t xa = reinterpret_cast<uintptr_t>(x);
+    if ((xa & 3) != 0 || (reinterpret_cast<uintptr_t>(w) & 15) != (xa & 15)) return false;
+    const bool grad_vec = grad != nullptr && (reinterpret_cast<uintptr_t>(grad) & 15) == (xa & 15);
+    const int64_t per_row = (cols + kMaxChunk2 - 1) / kMaxChunk2;
+    const int chunk = int(((cols + per_row - 1) / per_row + 3) / 4 * 4);
+    int64_t fit = int64_t(kRingBytes2) / (int64_t(chunk) * 4);
+    if (fit > kMaxSlots) fit = kMaxSlots;
+    if (fit < 2) return false;
+    const int nslot = int(fit);
+    const size_t smem = size_t(nslot) * chunk * sizeof(float) + 2 * size_t(nslot) * sizeof(uint64_t);
+    if (smem > kMaxDynSmem) return false;
+    const int sms = sm_count();
+    if (sms <= 0) return false;
+    auto kern = tma_rows2<TEACHER>;
+    *err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (*err != cudaSuccess) return true;
+    const int64_t grid = rows < sms ? rows : sms;
+    kern<<<unsigned(grid), kTmaThreads, smem, stream>>>(x, w, grad, row_loss, rows, int(cols), chunk, nslot,
+                                                        grad_scale, grad_vec);
+    *err = cudaGetLastError();
+    return true;
+}
 }  // namespace
 
 
@@ -378,6 +632,16 @@ bool launch_lse_tma(const float* x, float* lse, int64_t rows, int64_t cols, cuda
 bool launch_ce_tma(const float* x, const int32_t* targets, float* grad, float* row_loss, int64_t rows,
                    int64_t cols, float grad_scale, cudaStream_t stream, cudaError_t* err) {
     return launch_tma<RowOp::kCe>(x, grad, targets, row_loss, rows, cols, grad_scale, stream, err);
+}
+
+bool launch_soft_ce_tma(const float* x, const float* w, float* grad, float* row_loss, int64_t rows, int64_t cols,
+                        float grad_scale, cudaStream_t stream, cudaError_t* err) {
+    return launch_tma2<false>(x, w, grad, row_loss, rows, cols, grad_scale, stream, err);
+}
+
+bool launch_teacher_ce_tma(const float* s, const float* t, float* grad, float* row_loss, int64_t rows,
+                           int64_t cols, float grad_scale, cudaStream_t stream, cudaError_t* err) {
+    return launch_tma2<true>(s, t, grad, row_loss, rows, cols, grad_scale, stream, err);
 }
 
 bool launch_softmax_tma(const float* x, float* y, int64_t rows, int64_t cols, cudaStream_t stream,

@@ -4,7 +4,9 @@
 
 Ops: softmax_fwd, softmax_bwd, attn_fwd, attn_bwd (cols = seq_len), logsumexp,
 softmax_ce, layernorm_fwd, layernorm_bwd, rmsnorm_fwd, rmsnorm_bwd, masked_softmax, topk_kept,
-router_masked_topk, top_k_rows, argmax_onehot.  Inputs
+router_masked_topk, top_k_rows, argmax_onehot, soft_ce, teacher_ce.  For rows of
+more than 1024 floats, top_k_rows and argmax_onehot take logits-like rows
+(top_k_rows with k from ROWOPS_TOPK, default 50).  Inputs
 follow the workload distributions of ``inputs``; the L2 is flushed (512 MiB
 write) before every call.  Prints the median CUDA-event time per call.
 """
@@ -76,6 +78,26 @@ def make(op: str, rows: int, cols: int, dev):
             return lambda: ro.rowops_masked_softmax(x, m, p)
         kept = torch.empty_like(p)
         return lambda: ro.rowops_topk_kept(p, r["k"], kept)
+    if op in ("soft_ce", "teacher_ce"):
+        c = inputs.cross_entropy(0, rows=rows, cols=cols)
+        c2 = inputs.cross_entropy(1, rows=rows, cols=cols)
+        x, w = t(c["logits"]), t(c2["logits"])
+        if op == "soft_ce":
+            w = torch.softmax(w, dim=1)
+        g = torch.empty_like(x)
+        rl = torch.empty(rows, device=dev)
+        ml = torch.empty(1, dtype=torch.float64, device=dev)
+        f = ro.rowops_soft_ce if op == "soft_ce" else ro.rowops_teacher_ce
+        return lambda: f(x, w, g, rl, ml, grad_scale=1.0 / rows)
+    if op in ("top_k_rows", "argmax_onehot") and cols > 1024:  # vocabulary-sized rows
+        x = t(inputs.cross_entropy(0, rows=rows, cols=cols)["logits"])
+        if op == "top_k_rows":
+            k = int(os.environ.get("ROWOPS_TOPK", "50"))
+            vals = torch.empty((rows, k), device=dev)
+            idx = torch.empty_like(vals)
+            return lambda: ro.rowops_top_k_rows(x, k, True, vals, idx)
+        oh = torch.empty_like(x)
+        return lambda: ro.rowops_argmax_onehot(x, oh)
     if op in ("router_masked_topk", "top_k_rows", "argmax_onehot"):
         r = inputs.router(0, rows=rows, cols=cols)
         x, m = t(r["x"]), t(r["mask"])

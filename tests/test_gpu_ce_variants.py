@@ -60,3 +60,22 @@ def test_soft_ce_one_hot_matches_integer_targets(ro):
     g2, l2, _ = ro.rowops_softmax_ce(gpu(x), gpu(t))
     check_abs(host(g1), host(g2), 2e-6 / 64, "one-hot grad")
     check_rel(host(l1), host(l2).astype(np.float64), "one-hot loss")
+
+
+@pytest.mark.parametrize("cols", [3001, 20000, 20001])
+@pytest.mark.parametrize("misalign", [False, True])
+def test_ce_variants_many_rows_per_cta(ro, cols, misalign):
+    # more rows than SMs: each CTA of the long-row kernel walks several rows
+    rows = 400
+    x, w, t = _inputs(rows, cols, 7 * cols)
+    g, rl, ml = ro.rowops_soft_ce(gpu(x, misalign), gpu(w, misalign), grad_scale=1.0 / rows)
+    gr, rlr, mlr = oracle.soft_ce(x, w, 1.0 / rows)
+    wsum = np.abs(w.astype(np.float64)).sum(axis=1, keepdims=True)
+    check_abs(host(g), gr, 2e-6 * (1.0 / rows) * np.maximum(1.0, wsum), f"soft ce grad cols={cols}")
+    scale = np.maximum(1.0, np.abs(w.astype(np.float64)).sum(axis=1) * (np.abs(x).max(axis=1) + 10))
+    check_abs(host(rl), rlr, 1e-5 * scale, f"soft ce loss cols={cols}")
+    g, rl, ml = ro.rowops_teacher_ce(gpu(x, misalign), gpu(t, misalign), grad_scale=1.0 / rows)
+    gr, rlr, mlr = oracle.teacher_ce(x, t, 1.0 / rows)
+    check_abs(host(g), gr, 4e-6 / rows, f"teacher grad cols={cols}")
+    check_rel(host(rl), rlr, f"teacher loss cols={cols}")
+    check_rel(host(ml), [mlr], "teacher mean")
