@@ -332,6 +332,272 @@ top_k_rows_rowblock(const float* __restrict__ x, float* __restrict__ values, flo
     }
 }
 
+// Rows of 1025..kSelectMaxCols floats with 2 <= k <= kSelectMaxK.  One CTA
+// per row (rows blockIdx.x, + gridDim.x, ...; 256 threads and 4 CTAs per SM
+// for rows of up to 8192 floats, 1024 threads and one CTA per SM beyond) reads the row
+// from global memory once and keeps its selection keys (rank key, complemented
+// for smallest-first) in shared memory.  An entry's order is that of the
+// 64-bit composite (key << 32) | (0xffffffff - column): larger key first, then
+// lower column.
+// Fast path (k <= NT): each thread's largest key is a row entry, so at least k
+// entries reach tau, the smallest over warps of each warp's ceil(k/W)-th
+// largest thread maximum (W warps), and the top k are among the entries at or
+// above tau (for
+// logits, a few times k of them).  Those candidates are sorted (bitonic, in
+// shared memory) and the first k written.
+// When more than kSelectMaxCand entries reach tau, a radix select finds the
+// k-th largest key instead:
+//   passes 1-4  histogram one byte of the keys whose higher bytes equal the
+//               prefix found so far and extend the prefix by the byte holding
+//               the k-th largest key; after the fourth pass the prefix is that
+//               key, T, and `need` says how many entries equal to T are taken;
+//   collect     every entry above T and the `need` lowest columns equal to T
+//               (each thread walks a contiguous segment of columns after one
+//               block scan of its count of entries equal to T), then sort them.
+// Values are re-read from the row for the output, keeping their bits.
+constexpr int kSelectWarps = 32;  // at most
+constexpr int kSelectMaxK = 1024;
+constexpr int kSelectMaxCols = 51200;  // keys in shared memory: 200 KB
+constexpr int kSelectUnroll = 4;
+constexpr int kSelectMaxCand = 2048;
+
+struct SelectSmem {
+    uint64_t cand[kSelectMaxCand];  // composites: fast-path candidates or the collected k
+    uint32_t hist[256];
+    uint32_t wtau[kSelectWarps];
+    int scan[kSelectWarps];
+    int count;
+    uint32_t prefix;
+    int need;
+    int pad;
+    uint32_t keys[4];  // cols entries follow (16-byte aligned)
+};
+
+inline size_t select_smem_bytes(int64_t cols) {
+    return sizeof(SelectSmem) + size_t(cols) * sizeof(uint32_t);
+}
+
+__device__ __forceinline__ uint32_t select_key(float v, uint32_t flip) { return rank_key(v) ^ flip; }
+
+__device__ __forceinline__ uint64_t composite(uint32_t key, int col) {
+    return (uint64_t(key) << 32) | uint32_t(0xffffffffu - uint32_t(col));
+}
+
+// Adds this warp's `in` lanes to hist[bin], one atomic per distinct bin.  Every
+// lane of the warp calls it.
+__device__ __forceinline__ void warp_hist_add(uint32_t* hist, bool in, uint32_t bin, int lane) {
+    unsigned todo = __ballot_sync(kFullMask, in);
+    while (todo) {
+        const int leader = __ffs(todo) - 1;
+        const uint32_t lb = __shfl_sync(kFullMask, bin, leader);
+        const unsigned same = __ballot_sync(kFullMask, in && bin == lb);
+        if (lane == leader) atomicAdd(&hist[lb], uint32_t(__popc(same)));
+        todo &= ~same;
+    }
+}
+
+// Sorts s[0, n) into descending order with the whole block (n a power of two;
+// s complete on entry, sorted and visible to every thread on return).
+__device__ void block_bitonic_desc(uint64_t* s, int n) {
+    for (int kk = 2; kk <= n; kk <<= 1)
+        for (int j = kk >> 1; j > 0; j >>= 1) {
+            for (int i = threadIdx.x; i < n; i += blockDim.x) {
+                const int l = i ^ j;
+                if (l > i) {
+                    const uint64_t a = s[i], b = s[l];
+                    const bool desc = (i & kk) == 0;
+                    if (desc ? (a < b) : (a > b)) {
+                        s[i] = b;
+                        s[l] = a;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+}
+
+// Pads s[n0, pow2) with 0 (below every entry), sorts, and writes the first k.
+__device__ void sort_and_write(uint64_t* s, int n0, int k, const float* __restrict__ xr, float* vr, float* ir) {
+    int n = 2;
+    while (n < n0) n <<= 1;
+    for (int i = n0 + int(threadIdx.x); i < n; i += blockDim.x) s[i] = 0;
+    __syncthreads();
+    block_bitonic_desc(s, n);
+    for (int i = threadIdx.x; i < k; i += blockDim.x) {
+        const int col = int(0xffffffffu - uint32_t(s[i]));
+        vr[i] = __ldg(xr + col);
+        ir[i] = float(col);
+    }
+    __syncthreads();  // shared memory is rebuilt for the next row
+}
+
+template <int NT, int VEC>
+__global__ void __launch_bounds__(NT, 1024 / NT)
+top_k_rows_select(const float* __restrict__ x, float* __restrict__ values, float* __restrict__ indices,
+                  int64_t rows, int cols, int k, int largest) {
+    constexpr int W = NT / 32;
+    extern __shared__ __align__(16) unsigned char select_raw[];
+    SelectSmem& sm = *reinterpret_cast<SelectSmem*>(select_raw);
+    uint32_t* keys = sm.keys;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const uint32_t flip = largest ? 0u : 0xffffffffu;
+    const int nch = cols / VEC;
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const float* xr = x + row * int64_t(cols);
+        float* vr = values + row * int64_t(k);
+        float* ir = indices + row * int64_t(k);
+        // keys to shared memory; each thread's largest key
+        uint32_t tmax = 0;
+        bool has = false;
+        for (int c0 = 0; c0 < nch; c0 += kSelectUnroll * NT) {  // block-uniform
+            float t[kSelectUnroll][VEC];
+#pragma unroll
+            for (int u = 0; u < kSelectUnroll; ++u) {
+                const int c = c0 + u * NT + tid;
+                if (c < nch) ld_chunk<VEC>(xr + c * VEC, t[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < kSelectUnroll; ++u) {
+                const int c = c0 + u * NT + tid;
+                if (c < nch) {
+                    has = true;
+                    uint32_t kx[VEC];
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) {
+                        kx[e] = select_key(t[u][e], flip);
+                        tmax = max(tmax, kx[e]);
+                    }
+                    if constexpr (VEC == 4)
+                        *reinterpret_cast<uint4*>(keys + c * 4) = make_uint4(kx[0], kx[1], kx[2], kx[3]);
+                    else
+                        keys[c] = kx[0];
+                }
+            }
+        }
+        // tau: each warp's m-th largest maximum (m = ceil(k/32); a thread
+        // without entries counts as key 0, which every key reaches), then the
+        // smallest over warps
+        {
+            uint32_t v = has ? tmax : 0u;
+#pragma unroll
+            for (int kk = 2; kk <= 32; kk <<= 1)  // warp bitonic sort, descending by lane
+#pragma unroll
+                for (int j = kk >> 1; j > 0; j >>= 1) {
+                    const uint32_t o = __shfl_xor_sync(kFullMask, v, j);
+                    const bool lower = (lane & j) == 0;
+                    const bool desc = (lane & kk) == 0;
+                    v = (lower == desc) ? max(v, o) : min(v, o);
+                }
+            const int m = (k + W - 1) / W;
+            const uint32_t wt = m <= 32 ? __shfl_sync(kFullMask, v, m - 1) : 0u;  // 0: no bound
+            if (lane == 0) sm.wtau[wid] = wt;
+            if (tid == 0) sm.count = 0;
+        }
+        __syncthreads();
+        uint32_t tau = sm.wtau[0];
+        for (int w = 1; w < W; ++w) tau = min(tau, sm.wtau[w]);
+        // candidates: entries at or above tau (warp-aggregated slots)
+        for (int j0 = 0; j0 < cols; j0 += NT) {  // block-uniform
+            const int j = j0 + tid;
+            const uint32_t kx = j < cols ? keys[j] : 0u;
+            const bool cand = j < cols && kx >= tau;
+            const unsigned bal = __ballot_sync(kFullMask, cand);
+            if (bal == 0) continue;  // warp-uniform
+            int base = 0;
+            if (lane == 0) base = atomicAdd(&sm.count, __popc(bal));
+            base = __shfl_sync(kFullMask, base, 0);
+            const int slot = base + __popc(bal & ((1u << lane) - 1u));
+            if (cand && slot < kSelectMaxCand) sm.cand[slot] = composite(kx, j);
+        }
+        __syncthreads();
+        const int ncand = sm.count;
+        if (ncand <= kSelectMaxCand) {  // block-uniform
+            sort_and_write(sm.cand, ncand, k, xr, vr, ir);
+            continue;
+        }
+        // radix select (many entries tie with or sit just above tau)
+        if (tid < 256) sm.hist[tid] = 0;
+        __syncthreads();
+        for (int j0 = 0; j0 < cols; j0 += NT) {  // block-uniform
+            const int j = j0 + tid;
+            const uint32_t kx = j < cols ? keys[j] : 0u;
+            warp_hist_add(sm.hist, j < cols, kx >> 24, lane);
+        }
+        uint32_t prefix = 0, pmask = 0;
+        int kr = k;  // entries still to find at or below the current prefix
+        for (int shift = 24; shift >= 0; shift -= 8) {
+            if (shift < 24) {
+                if (tid < 256) sm.hist[tid] = 0;
+                __syncthreads();
+                for (int j0 = 0; j0 < cols; j0 += NT) {  // block-uniform
+                    const int j = j0 + tid;
+                    const uint32_t kx = j < cols ? keys[j] : 0u;
+                    const bool in = j < cols && (kx & pmask) == prefix;
+                    warp_hist_add(sm.hist, in, (kx >> shift) & 255u, lane);
+                }
+            }
+            __syncthreads();
+            if (wid == 0) {
+                // bins from the top: lane l covers bins 255-8l .. 248-8l
+                uint32_t cnt[8], part = 0;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    cnt[q] = sm.hist[255 - 8 * lane - q];
+                    part += cnt[q];
+                }
+                uint32_t incl = part;  // inclusive scan over lanes (top bins first)
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint32_t y = __shfl_up_sync(kFullMask, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                const uint32_t excl = incl - part;
+                const unsigned hit = __ballot_sync(kFullMask, excl < uint32_t(kr) && uint32_t(kr) <= incl);
+                if (lane == __ffs(hit) - 1) {
+                    uint32_t above = excl;
+                    int b = 255 - 8 * lane;
+                    for (int q = 0; q < 8; ++q, --b) {
+                        if (above + cnt[q] >= uint32_t(kr)) break;
+                        above += cnt[q];
+                    }
+                    sm.prefix = prefix | (uint32_t(b) << shift);
+                    sm.need = kr - int(above);
+                }
+            }
+            __syncthreads();
+            prefix = sm.prefix;
+            kr = sm.need;
+            pmask |= 255u << shift;
+        }
+        // collect: entries above T, and the kr lowest columns equal to T
+        const uint32_t T = prefix;
+        const int seg = (cols + NT - 1) / NT;
+        const int j_begin = tid * seg;
+        const int j_end = min(cols, j_begin + seg);
+        int eq = 0;
+        for (int j = j_begin; j < j_end; ++j) eq += keys[j] == T ? 1 : 0;
+        int incl = eq;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(kFullMask, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (lane == 31) sm.scan[wid] = incl;
+        if (tid == 0) sm.count = 0;
+        __syncthreads();
+        int r = incl - eq;  // rank of this segment's first entry equal to T
+        for (int w = 0; w < wid; ++w) r += sm.scan[w];
+        for (int j = j_begin; j < j_end; ++j) {
+            const uint32_t kx = keys[j];
+            bool take = kx > T;
+            if (kx == T) take = r++ < kr;
+            if (take) sm.cand[atomicAdd(&sm.count, 1)] = composite(kx, j);
+        }
+        __syncthreads();
+        sort_and_write(sm.cand, k, k, xr, vr, ir);
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_router(const float* x, const uint8_t* mask, float* p, float* kept, int64_t rows,
@@ -358,7 +624,25 @@ cudaError_t launch_top_k_rows(const float* x, float* values, float* indices, int
         top_k_rows_group<G::LANES, G::NV, G::VEC><<<stream_grid(rows, G::LANES), kBlockThreads, 0, stream>>>(
             x, values, indices, rows, int(cols), int(k), largest ? 1 : 0);
     });
-    if (!done) {
+    cudaError_t err = cudaSuccess;
+    const int sms = sm_count();
+    if (!done && k >= 2 && k <= kSelectMaxK && cols <= kSelectMaxCols && sms > 0) {
+        const size_t smem = select_smem_bytes(cols);
+        auto launch = [&](auto kern, int nt, int per_sm) {
+            err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+            if (err != cudaSuccess) return;
+            const int64_t cap = int64_t(sms) * per_sm;
+            const unsigned grid = unsigned(rows < cap ? rows : cap);
+            kern<<<grid, nt, smem, stream>>>(x, values, indices, rows, int(cols), int(k), largest ? 1 : 0);
+        };
+        if (cols <= 8192) {  // 4 CTAs of 256 threads per SM (at most 50 KB of shared memory each)
+            if (vec4) launch(top_k_rows_select<256, 4>, 256, 4);
+            else launch(top_k_rows_select<256, 1>, 256, 4);
+        } else {
+            if (vec4) launch(top_k_rows_select<1024, 4>, 1024, 1);
+            else launch(top_k_rows_select<1024, 1>, 1024, 1);
+        }
+    } else if (!done) {
         if (vec4)
             top_k_rows_rowblock<4><<<row_grid(rows), kBlockThreads, 0, stream>>>(x, values, indices, rows,
                                                                                  int(cols), int(k), largest);
@@ -367,7 +651,7 @@ cudaError_t launch_top_k_rows(const float* x, float* values, float* indices, int
                                                                                  int(cols), int(k), largest);
     }
     note_launches(1);
-    return cudaGetLastError();
+    return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 }  // namespace rowops

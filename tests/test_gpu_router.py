@@ -162,3 +162,23 @@ def test_top_k_rows_router_logits(ro):
     v, i = ro.rowops_top_k_rows(gpu(r["x"]), 2, True)
     vr, ir = oracle.top_k_rows(r["x"], 2, True)
     assert np.array_equal(host(i), ir.astype(np.float32)) and np.array_equal(host(v), vr.astype(np.float32))
+
+
+@pytest.mark.parametrize("rows,cols", [(3, 50304), (300, 3001)])
+@pytest.mark.parametrize("misalign", [False, True])
+def test_top_k_rows_long_rows(ro, rows, cols, misalign):
+    # rows of more than 1024 floats: the radix select (2 <= k <= 1024) and the
+    # k-pass kernel beyond; values on a coarse grid force long runs of ties
+    rng = np.random.default_rng(rows + cols)
+    x = (rng.normal(0, 2, (rows, cols)) * 4).round().astype(np.float32) / 4
+    x[x == 0] = np.where(rng.random(int((x == 0).sum())) < 0.5, 0.0, -0.0).astype(np.float32)
+    x[rng.random(x.shape) < 1e-3] = np.nan
+    x[rng.random(x.shape) < 1e-3] = np.inf
+    x[rng.random(x.shape) < 1e-3] = -np.inf
+    xg = gpu(x, misalign)
+    for k in [k for k in (2, 50, 300, 1024, 1025) if k <= cols]:
+        for largest in (True, False):
+            v, i = ro.rowops_top_k_rows(xg, k, largest)
+            vr, ir = oracle.top_k_rows(x, k, largest)
+            assert np.array_equal(host(i), ir.astype(np.float32)), (cols, k, largest)
+            assert _same_bits(host(v), vr.astype(np.float32)), (cols, k, largest)
