@@ -106,6 +106,17 @@ struct BlockReduce {
         b = rb;
     }
 
+    __device__ __forceinline__ int min_int(int v) {
+        v = group_min_int<32>(v);
+        float* p = next();
+        if ((threadIdx.x & 31) == 0) p[threadIdx.x >> 5] = __int_as_float(v);
+        __syncthreads();
+        int r = __float_as_int(p[0]);
+#pragma unroll
+        for (int i = 1; i < W; ++i) r = min(r, __float_as_int(p[i]));
+        return r;
+    }
+
     // Two maxima in one round.
     __device__ __forceinline__ void max2(float& a, float& b) {
         a = group_max<32>(a);

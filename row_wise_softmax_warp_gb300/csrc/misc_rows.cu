@@ -4,9 +4,11 @@
 //   argmax_onehot     1 at the first maximal coordinate of the row, 0 elsewhere:
 //                     maximal = exceeded by no entry (x_i > x_j for no i), so
 //                     the first entry that is a NaN or equals the numeric max.
-// Group kernels (geometry of common.cuh) with streaming fallbacks.
+// Group kernels (geometry of common.cuh), block-row kernels for rows of
+// 1025..16384 floats (block_rows.cuh) and streaming fallbacks.
 #include <climits>
 
+#include "block_rows.cuh"
 #include "common.cuh"
 #include "launch.h"
 
@@ -168,6 +170,87 @@ argmax_rowblock(const float* __restrict__ x, float* __restrict__ out, int64_t ro
     }
 }
 
+// ------------------------------------------------------ block-row kernels
+
+template <int NT, int NV, int VEC>
+__global__ void __launch_bounds__(NT)
+lrp_brow(const float* __restrict__ x, const float* __restrict__ y, const float* __restrict__ r,
+         float* __restrict__ r_in, int64_t rows, int cols) {
+    __shared__ float sc[4 * (NT / 32)];
+    BlockReduce<NT> red(sc);
+    const int nch = cols / VEC;
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const int64_t off = row * int64_t(cols);
+        float rv[NV][VEC];
+        float s = 0.f;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c = int(threadIdx.x) + k * NT;
+            if (c < nch) {
+                ld_chunk<VEC>(r + off + c * VEC, rv[k]);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) s += rv[k][e];
+            }
+        }
+        s = red.sum(s);
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c = int(threadIdx.x) + k * NT;
+            if (c < nch) {
+                float xv[VEC], yv[VEC], o[VEC];
+                ld_chunk<VEC>(x + off + c * VEC, xv);
+                ld_chunk<VEC>(y + off + c * VEC, yv);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) o[e] = xv[e] * (rv[k][e] - yv[e] * s);
+                st_chunk<VEC>(r_in + off + c * VEC, o);
+            }
+        }
+    }
+}
+
+template <int NT, int NV, int VEC>
+__global__ void __launch_bounds__(NT)
+argmax_brow(const float* __restrict__ x, float* __restrict__ out, int64_t rows, int cols) {
+    __shared__ float sc[4 * (NT / 32)];
+    BlockReduce<NT> red(sc);
+    const int nch = cols / VEC;
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const int64_t off = row * int64_t(cols);
+        float v[NV][VEC];
+        float m = -INFINITY;  // numeric maximum (fmaxf skips NaN)
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c = int(threadIdx.x) + k * NT;
+            if (c < nch) {
+                ld_chunk<VEC>(x + off + c * VEC, v[k]);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) m = fmaxf(m, v[k][e]);
+            }
+        }
+        m = red.max(m);
+        int first = INT_MAX;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c = int(threadIdx.x) + k * NT;
+            if (c < nch)
+#pragma unroll
+                for (int e = 0; e < VEC; ++e)
+                    if (isnan(v[k][e]) || v[k][e] == m) first = min(first, c * VEC + e);
+        }
+        first = red.min_int(first);
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c = int(threadIdx.x) + k * NT;
+            if (c < nch) {
+                float o[VEC];
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) o[e] = (c * VEC + e == first) ? 1.f : 0.f;
+                st_chunk<VEC>(out + off + c * VEC, o);
+            }
+        }
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_lrp_softmax(const float* x, const float* y, const float* r, float* r_in, int64_t rows,
@@ -178,7 +261,12 @@ cudaError_t launch_lrp_softmax(const float* x, const float* y, const float* r, f
             x, y, r, r_in, rows, int(cols));
     });
     if (!done) {
-        if (vec4)
+        if (with_block_geometry(vec4, cols, kBlockRowMax, [&](auto geo) {
+                using G = decltype(geo);
+                lrp_brow<G::NT, G::NV, G::VEC><<<block_row_grid(rows), G::NT, 0, stream>>>(
+                    x, y, r, r_in, rows, int(cols));
+            })) {
+        } else if (vec4)
             lrp_rowblock<4><<<row_grid(rows), kBlockThreads, 0, stream>>>(x, y, r, r_in, rows, cols);
         else
             lrp_rowblock<1><<<row_grid(rows), kBlockThreads, 0, stream>>>(x, y, r, r_in, rows, cols);
@@ -195,7 +283,12 @@ cudaError_t launch_argmax_onehot(const float* x, float* out, int64_t rows, int64
             x, out, rows, int(cols));
     });
     if (!done) {
-        if (vec4)
+        if (with_block_geometry(vec4, cols, kBlockRowMax, [&](auto geo) {
+                using G = decltype(geo);
+                argmax_brow<G::NT, G::NV, G::VEC><<<block_row_grid(rows), G::NT, 0, stream>>>(
+                    x, out, rows, int(cols));
+            })) {
+        } else if (vec4)
             argmax_rowblock<4><<<row_grid(rows), kBlockThreads, 0, stream>>>(x, out, rows, cols);
         else
             argmax_rowblock<1><<<row_grid(rows), kBlockThreads, 0, stream>>>(x, out, rows, cols);

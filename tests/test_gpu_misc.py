@@ -9,7 +9,7 @@ from row_wise_softmax_warp_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
 
-COLS = [1, 3, 4, 16, 33, 64, 128, 256, 257, 1024, 1028, 3000]
+COLS = [1, 3, 4, 16, 33, 64, 128, 256, 257, 1024, 1028, 2048, 3000, 8192, 16384, 16385]
 
 
 @pytest.mark.parametrize("cols", COLS)
