@@ -455,8 +455,10 @@ def gpu_leg(args):
         next_ms[name] = sum(a.elapsed_time(b) for a, b in ts) / len(ts)
 
     # ------------------------------------------- the step ops back to back
-    b2b_ms_local, b2b_sets = back_to_back(ops, dev, stream, L2_BYTES)
-    b2b_ms = {n: max_over_ranks(b2b_ms_local[n], dist, dev) for n in b2b_ms_local}
+    b2b_ms, b2b_sets = {}, {}
+    if not args.no_back_to_back:
+        b2b_ms_local, b2b_sets = back_to_back(ops, dev, stream, L2_BYTES)
+        b2b_ms = {n: max_over_ranks(b2b_ms_local[n], dist, dev) for n in b2b_ms_local}
 
     # ------------------------------------------------ the step as a CUDA graph
     # The ten calls captured once and replayed: no host work per launch and no
@@ -608,16 +610,17 @@ def gpu_leg(args):
     elif graph_step is not None:
         line["graph_step"] = graph_step
     b2b_total = sum(b2b_ms.values())
-    line["back_to_back"] = {
-        "ms_per_step": round(b2b_total, 5),
-        "GB/s": round(world * total_bytes / (b2b_total * 1e-3) / 1e9, 1),
-        "ops": {n: {"ms": round(b2b_ms[n], 5),
-                    "GB/s": round(abytes[n][0] / (b2b_ms[n] * 1e-3) / 1e9, 1),
-                    "frac_of_measured": round(abytes[n][0] / (b2b_ms[n] * 1e-3) / 1e9 / peak, 4),
-                    "buffer_sets": b2b_sets[n]} for n in b2b_ms},
-        "note": "each op's calls replayed back to back as one CUDA graph (no flush, no events between "
-                "calls), cycling through copies of its buffers that total more than twice the L2",
-    }
+    if b2b_ms:
+        line["back_to_back"] = {
+            "ms_per_step": round(b2b_total, 5),
+            "GB/s": round(world * total_bytes / (b2b_total * 1e-3) / 1e9, 1),
+            "ops": {n: {"ms": round(b2b_ms[n], 5),
+                        "GB/s": round(abytes[n][0] / (b2b_ms[n] * 1e-3) / 1e9, 1),
+                        "frac_of_measured": round(abytes[n][0] / (b2b_ms[n] * 1e-3) / 1e9 / peak, 4),
+                        "buffer_sets": b2b_sets[n]} for n in b2b_ms},
+            "note": "each op's calls replayed back to back as one CUDA graph (no flush, no events between "
+                    "calls), cycling through copies of its buffers that total more than twice the L2",
+        }
     if not args.no_cpu_baseline and world == 1:  # the CPU baseline belongs to the N = 1 line
         line["cpu_baseline"] = cpu_leg(data, budget_s=args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -731,6 +734,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=30.0)
     ap.add_argument("--ref-step-seconds", type=float, default=4.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-back-to-back", action="store_true",
+                    help="skip the back-to-back figures (shorter launch lists under a profiler)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     if args.impl == "reference":

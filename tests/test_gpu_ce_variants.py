@@ -79,3 +79,34 @@ def test_ce_variants_many_rows_per_cta(ro, cols, misalign):
     check_abs(host(g), gr, 4e-6 / rows, f"teacher grad cols={cols}")
     check_rel(host(rl), rlr, f"teacher loss cols={cols}")
     check_rel(host(ml), [mlr], "teacher mean")
+
+
+def _at_offset(a: np.ndarray, off: int) -> torch.Tensor:
+    """Device copy of `a` whose data starts `off` floats past a 256-byte boundary."""
+    a = np.ascontiguousarray(a, np.float32)
+    flat = torch.zeros(a.size + 8, dtype=torch.float32, device="cuda")
+    view = flat[off:off + a.size].view(a.shape)
+    view.copy_(torch.from_numpy(a).cuda())
+    return view
+
+
+@pytest.mark.parametrize("cols", [20000, 20001])
+def test_ce_variants_inputs_on_different_16_byte_phases(ro, cols):
+    # long rows whose two inputs sit on different 16-byte phases: the
+    # plain-load two-pass kernel instead of the bulk copies
+    rows = 200
+    x, w, t = _inputs(rows, cols, 11 * cols)
+    xg, wg, tg = _at_offset(x, 0), _at_offset(w, 1), _at_offset(t, 2)
+    g, rl, ml = ro.rowops_soft_ce(xg, wg, grad_scale=1.0 / rows)
+    gr, rlr, mlr = oracle.soft_ce(x, w, 1.0 / rows)
+    wsum = np.abs(w.astype(np.float64)).sum(axis=1, keepdims=True)
+    check_abs(host(g), gr, 2e-6 * (1.0 / rows) * np.maximum(1.0, wsum), f"soft ce grad cols={cols}")
+    scale = np.maximum(1.0, np.abs(w.astype(np.float64)).sum(axis=1) * (np.abs(x).max(axis=1) + 10))
+    check_abs(host(rl), rlr, 1e-5 * scale, f"soft ce loss cols={cols}")
+    g, rl, ml = ro.rowops_teacher_ce(xg, tg, grad_scale=1.0 / rows)
+    gr, rlr, mlr = oracle.teacher_ce(x, t, 1.0 / rows)
+    check_abs(host(g), gr, 4e-6 / rows, f"teacher grad cols={cols}")
+    check_rel(host(rl), rlr, f"teacher loss cols={cols}")
+    check_rel(host(ml), [mlr], "teacher mean")
+    _, rl2, _ = ro.rowops_teacher_ce(xg, tg, with_grad=False)
+    assert torch.equal(rl2, rl)
