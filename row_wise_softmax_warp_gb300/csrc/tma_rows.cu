@@ -544,12 +544,162 @@ tma_rows2(const float* x, const float* w, float* grad, float* __restrict__ row_l
     }
 }
 
+// ------------------------------------------------- one input, two passes
+// Cross-entropy and softmax forward on rows longer than the ring can hold
+// whole: the row streams through the ring twice, pass 0 folding (max, sum)
+// and pass 1 writing the gradient or probabilities.  One row per SM is in
+// flight, so pass 1 reads from the L2 what pass 0 brought in.  Softmax may run
+// in place: every chunk of pass 1 is copied into shared memory before the
+// consumers overwrite it in global memory, and pass 0 of the row is over
+// before pass 1 writes anything.
+template <RowOp OP>
+__global__ void __launch_bounds__(kTmaThreads, 1)
+tma_rows_2pass(const float* x, float* out, const int32_t* __restrict__ targets, float* __restrict__ aux,
+               int64_t rows, int cols, int chunk, int nslot, float grad_scale) {
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    float* buf = reinterpret_cast<float*>(smem_raw);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + size_t(nslot) * chunk * sizeof(float));
+    uint64_t* empty = full + nslot;
+    __shared__ uint64_t red_bar[2];
+    __shared__ float red[2][kConsumerWarps][4];
+    __shared__ volatile int abort_flag;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    if constexpr (OP == RowOp::kCe) {
+        // The mean-loss kernel may be scheduled now; it waits for this grid.
+        asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    }
+    if (tid == 0) {
+        for (int s = 0; s < nslot; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumerWarps);
+        }
+        mbar_init(&red_bar[0], kConsumerWarps);
+        mbar_init(&red_bar[1], kConsumerWarps);
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        // ------------------------------------------------------- producer
+        if (lane != 0) return;
+        uint64_t n = 0;
+        bool ok = true;
+        for (int64_t row = blockIdx.x; ok && row < rows; row += gridDim.x) {
+            int head, body;
+            row_split(x + row * int64_t(cols), cols, head, body);
+            const float* src = x + row * int64_t(cols) + head;
+            const int nch = (body + chunk - 1) / chunk;
+            for (int pass = 0; ok && pass < 2; ++pass)
+                for (int k = 0; k < nch; ++k, ++n) {
+                    const int s = int(n % nslot);
+                    const uint64_t use = n / nslot;
+                    if (use > 0 && !mbar_wait(&empty[s], uint32_t((use - 1) & 1), &abort_flag)) {
+                        raise_abort(&abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    const int cnt = min(chunk, body - k * chunk);
+                    mbar_arrive_expect_tx(&full[s], uint32_t(cnt) * 4u);
+                    bulk_load(buf + size_t(s) * chunk, src + size_t(k) * chunk, uint32_t(cnt) * 4u, &full[s]);
+                }
+        }
+        if (!ok) {
+            // Let the copies already issued land before the CTA's shared memory goes away.
+            const uint64_t first = n > uint64_t(nslot) ? n - nslot : 0;
+            for (uint64_t j = first; j < n; ++j) {
+                volatile int never = 0;
+                mbar_wait(&full[j % nslot], uint32_t((j / nslot) & 1), &never);
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------- consumers
+    const int ct = tid - 32;
+    const int cw = warp - 1;
+    uint64_t n = 0;   // slot uses consumed
+    uint32_t rv = 0;  // rendezvous so far
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const float* xr = x + row * int64_t(cols);
+        int head, body;
+        row_split(xr, cols, head, body);
+        const int nch = (body + chunk - 1) / chunk;
+        int ej = -1;  // head (warp 0) and tail (warp 1) lanes, as in tma_rows
+        if (ct < head) ej = ct;
+        else if (ct >= 32 && ct - 32 < cols - head - body) ej = head + body + (ct - 32);
+        const float xe = ej >= 0 ? xr[ej] : -INFINITY;  // coherent: softmax may run in place
+        float m = -INFINITY, s = 0.f;
+        if (ej >= 0) push1(m, s, xe);
+        for (int k = 0; k < nch; ++k, ++n) {
+            if (!wait_use(full, nslot, n, &abort_flag)) return;
+            const int cnt4 = min(chunk, body - k * chunk) >> 2;
+            const float4* c4 = reinterpret_cast<const float4*>(buf + size_t(n % nslot) * chunk);
+            for (int i = ct; i < cnt4; i += kConsumers) push4(m, s, c4[i]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[n % nslot]);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            merge2(m, s, __shfl_xor_sync(kFullMask, m, o), __shfl_xor_sync(kFullMask, s, o));
+        float all[kConsumerWarps][4];
+        const float mine[4] = {m, s, 0.f, 0.f};
+        if (!rendezvous4(red, red_bar, cw, lane, rv, mine, all, &abort_flag)) return;
+        float M = all[0][0], S = all[0][1];
+        for (int q = 1; q < kConsumerWarps; ++q) merge2(M, S, all[q][0], all[q][1]);
+        const float inv = 1.0f / S;
+        int t = -1;
+        if constexpr (OP == RowOp::kCe) {
+            t = __ldg(targets + row);
+            if (ct == 0) {
+                const float lse = isinf(M) ? M : M + logf(S);
+                aux[row] = (t >= 0 && t < cols) ? lse - __ldg(xr + t) : __int_as_float(0x7fc00000);
+            }
+        }
+        float* dst = out + row * int64_t(cols);
+        if (ej >= 0) {
+            float p = ex2((xe - M) * kLog2e) * inv;
+            if constexpr (OP == RowOp::kCe) p = grad_scale * (p - (ej == t ? 1.f : 0.f));
+            dst[ej] = p;
+        }
+        for (int k = 0; k < nch; ++k, ++n) {
+            if (!wait_use(full, nslot, n, &abort_flag)) return;
+            const int cnt4 = min(chunk, body - k * chunk) >> 2;
+            const float4* c4 = reinterpret_cast<const float4*>(buf + size_t(n % nslot) * chunk);
+            float4* d4 = reinterpret_cast<float4*>(dst + head + size_t(k) * chunk);
+            for (int i = ct; i < cnt4; i += kConsumers) {
+                const float4 v = c4[i];
+                float4 p;
+                p.x = ex2((v.x - M) * kLog2e) * inv;
+                p.y = ex2((v.y - M) * kLog2e) * inv;
+                p.z = ex2((v.z - M) * kLog2e) * inv;
+                p.w = ex2((v.w - M) * kLog2e) * inv;
+                if constexpr (OP == RowOp::kCe) {
+                    const int j = head + k * chunk + 4 * i;
+                    p.x = grad_scale * (p.x - (j == t ? 1.f : 0.f));
+                    p.y = grad_scale * (p.y - (j + 1 == t ? 1.f : 0.f));
+                    p.z = grad_scale * (p.z - (j + 2 == t ? 1.f : 0.f));
+                    p.w = grad_scale * (p.w - (j + 3 == t ? 1.f : 0.f));
+                }
+                d4[i] = p;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[n % nslot]);
+        }
+    }
+}
+
 constexpr int64_t kMaxChunk = 16384;       // floats per bulk copy, at most
 constexpr size_t kRingBytes = 200 * 1024;   // target ring size (whole rows resident)
 // Streaming ring (logsumexp).  On GB300, 8192 x 50304: 3 slots of 12576 floats
 // (147 KB) ran at 0.98 of the HBM copy rate, 4 slots (one row, 196 KB) at 0.89.
 constexpr size_t kStreamRingBytes = 160 * 1024;
 constexpr size_t kMaxDynSmem = 226 * 1024;  // 227 KB per block, less room for static shared memory
+// Two-input kernel (tma_rows2): chunks of at most 12288 floats.
+constexpr int64_t kMaxChunk2 = 12288;
 
 template <RowOp OP>
 bool launch_tma(const float* x, float* out, const int32_t* targets, float* aux, int64_t rows,
@@ -564,7 +714,8 @@ bool launch_tma(const float* x, float* out, const int32_t* targets, float* aux, 
     // costs the pipeline a fixed ~0.5 us per SM, so chunks are kept large (on
     // GB300, 16 KB chunks left logsumexp at 0.70 of the HBM copy rate, 48-64 KB
     // chunks reach 0.95).  The ring holds as many chunks as fit in ~200 KB; for
-    // cross-entropy and softmax it must hold a whole row.
+    // cross-entropy and softmax it holds a whole row when one fits (about 56K
+// floats), and longer rows take the two-pass kernel.
     const int64_t per_row = (cols + kMaxChunk - 1) / kMaxChunk;
     const int chunk = int(((cols + per_row - 1) / per_row + 3) / 4 * 4);
     int64_t fit = int64_t(OP == RowOp::kLse ? kStreamRingBytes : kRingBytes) / (int64_t(chunk) * 4);
@@ -574,25 +725,45 @@ bool launch_tma(const float* x, float* out, const int32_t* targets, float* aux, 
     } else {
         if (fit < per_row) fit = per_row;  // whole row resident
     }
-    const int nslot = int(fit);
-    const size_t smem = size_t(nslot) * chunk * sizeof(float) + 2 * size_t(nslot) * sizeof(uint64_t);
-    if (smem > kMaxDynSmem || nslot > kMaxSlots) return false;
+    int nslot = int(fit);
+    size_t smem = size_t(nslot) * chunk * sizeof(float) + 2 * size_t(nslot) * sizeof(uint64_t);
     const int sms = sm_count();
     if (sms <= 0) return false;
-    auto kern = tma_rows<OP>;
-    *err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (*err != cudaSuccess) return true;
     const int64_t grid = rows < sms ? rows : sms;
-    kern<<<unsigned(grid), kTmaThreads, smem, stream>>>(x, out, targets, aux, rows, int(cols), chunk, nslot,
-                                                         grad_scale);
-    *err = cudaGetLastError();
-    return true;
+    if (smem <= kMaxDynSmem && nslot <= kMaxSlots) {
+        auto kern = tma_rows<OP>;
+        *err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (*err != cudaSuccess) return true;
+        kern<<<unsigned(grid), kTmaThreads, smem, stream>>>(x, out, targets, aux, rows, int(cols), chunk, nslot,
+                                                             grad_scale);
+        *err = cudaGetLastError();
+        return true;
+    }
+    if constexpr (OP == RowOp::kLse) {
+        return false;
+    } else {
+        // The row does not fit in shared memory: stream it twice through a
+        // ring of the logsumexp's size (the second pass reads the L2).  On
+        // GB300 (1024 rows of 152064 floats) 64 KB chunks in two slots ran
+        // at 277 us, 48 KB chunks in four slots at 297 us.
+        fit = int64_t(kStreamRingBytes) / (int64_t(chunk) * 4);
+        if (fit > 8) fit = 8;
+        if (fit < 2) fit = 2;
+        nslot = int(fit);
+        smem = size_t(nslot) * chunk * sizeof(float) + 2 * size_t(nslot) * sizeof(uint64_t);
+        if (smem > kMaxDynSmem) return false;
+        auto kern = tma_rows_2pass<OP>;
+        *err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (*err != cudaSuccess) return true;
+        kern<<<unsigned(grid), kTmaThreads, smem, stream>>>(x, out, targets, aux, rows, int(cols), chunk, nslot,
+                                                             grad_scale);
+        *err = cudaGetLastError();
+        return true;
+    }
 }
 
 
-// Two-input rows (tma_rows2): chunks of at most 12288 floats, a ring of whole
-// chunk pairs in ~192 KB.
-constexpr int64_t kMaxChunk2 = 12288;
+// Two-input rows (tma_rows2): a ring of whole chunk pairs in ~192 KB.
 constexpr size_t kRingBytes2 = 192 * 1024;
 
 template <bool TEACHER>
