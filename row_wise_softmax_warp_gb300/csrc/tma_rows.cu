@@ -1,5 +1,6 @@
-// tma_rows.cu - long rows (logsumexp, softmax cross-entropy, softmax forward)
-// streamed through shared memory by the Tensor Memory Accelerator.
+// tma_rows.cu - long rows (logsumexp, softmax cross-entropy, softmax forward,
+// weighted-logits and fixed-teacher cross-entropy) streamed through shared
+// memory by the Tensor Memory Accelerator's bulk copies.
 //
 // One persistent CTA per SM walks rows blockIdx.x, blockIdx.x + gridDim.x, ...
 // Warp 0 is the producer: one lane issues bulk copies (cp.async.bulk, global ->
@@ -16,6 +17,11 @@
 // (nslot * chunk >= cols), and the next row's chunks are loaded as soon as the
 // current row's gradient has been written from them.  HBM sees exactly one read
 // of every input element and one write of every output element.
+//
+// Two further kernels reuse the pipeline with two passes over each row, the
+// second reading the row again from the L2: tma_rows_2pass (cross-entropy and
+// softmax rows too long to stay resident) and tma_rows2 (weighted-logits and
+// fixed-teacher cross-entropy, whose two input rows stream as chunk pairs).
 //
 // Rows need not start on a 16-byte boundary (cols % 4 != 0, or an offset
 // base): the row's first boundary splits off a head of h < 4 floats, the body
