@@ -8,6 +8,13 @@
 // found exactly without counting:
 //   k <= 2      one pass keeping each lane's best two (value, column) pairs,
 //               then a butterfly merge of the pairs across the group;
+//   k <= LANES  (groups of 8 or more lanes, with per-warp shared scratch)
+//               candidates: each lane's largest value is an entry of the row,
+//               so at least k entries reach tau, the k-th largest of the
+//               group's lane maxima, and every entry ranked above an entry
+//               that reaches tau reaches it too.  When at most 32 entries of
+//               each row of the warp reach tau, they are ranked among
+//               themselves by counting; otherwise the rounds below run;
 //   k <= 8      k rounds of "best remaining entry": a group max of the
 //               remaining floats, then a group min of the columns holding that
 //               value (the index tie-break);
@@ -26,6 +33,15 @@
 #include "common.cuh"
 
 namespace rowops {
+// Per-warp shared-memory scratch of the candidate path: for each group of the
+// warp (at most 4: groups of 8 or more lanes) 32 candidate slots and the kept
+// bits of a row of up to 1024 columns.
+struct KeptScratch {
+    float v[4][32];
+    int c[4][32];
+    unsigned bits[4][32];
+};
+
 namespace kept_detail {
 
 constexpr int kMaxRounds = 8;
@@ -42,6 +58,79 @@ __device__ __forceinline__ uint64_t make_key(float x, int col, int cols) {
 
 // Number of low-word bits that can be nonzero: cols - 1 < 2^lb.
 __device__ __forceinline__ int low_bits(int cols) { return cols <= 1 ? 0 : 32 - __clz(cols - 1); }
+
+// The candidate path (see the file comment).  Returns false, touching nothing,
+// when a row of the warp has more than 32 candidates; warp-uniform.
+template <int LANES, int NV, int VEC>
+__device__ __forceinline__ bool kept_by_candidates(const float (&v)[NV][VEC], const bool (&valid)[NV][VEC],
+                                                   int k, bool (&keep)[NV][VEC], KeptScratch* ks) {
+    const int g = threadIdx.x % LANES;
+    const int leader = (threadIdx.x & 31) - g;
+    const int gi = (threadIdx.x & 31) / LANES;
+    float lm = -INFINITY;
+#pragma unroll
+    for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+        for (int e = 0; e < VEC; ++e)
+            if (valid[kk][e]) lm = fmaxf(lm, v[kk][e]);
+    // the group's lane maxima in descending order (bitonic network over g)
+    float s = lm;
+#pragma unroll
+    for (int kk = 2; kk <= LANES; kk <<= 1)
+#pragma unroll
+        for (int j = kk >> 1; j > 0; j >>= 1) {
+            const float o = __shfl_xor_sync(kFullMask, s, j);
+            const bool lower = (g & j) == 0;
+            const bool desc = (g & kk) == 0;
+            s = (lower == desc) ? fmaxf(s, o) : fminf(s, o);
+        }
+    const float tau = __shfl_sync(kFullMask, s, leader + k - 1);
+    int cnt = 0;
+#pragma unroll
+    for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) cnt += (valid[kk][e] && v[kk][e] >= tau) ? 1 : 0;
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < LANES; o <<= 1) {
+        const int y = __shfl_up_sync(kFullMask, incl, o, LANES);
+        if (g >= o) incl += y;
+    }
+    const int total = __shfl_sync(kFullMask, incl, leader + LANES - 1);
+    if (__any_sync(kFullMask, total > 32)) return false;
+    float* sv = ks->v[gi];
+    int* sc = ks->c[gi];
+    unsigned* sb = ks->bits[gi];
+    __syncwarp();  // the warp's previous use of the scratch is over
+    for (int w = g; w < 32; w += LANES) sb[w] = 0u;
+    int slot = incl - cnt;
+#pragma unroll
+    for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+        for (int e = 0; e < VEC; ++e)
+            if (valid[kk][e] && v[kk][e] >= tau) {
+                sv[slot] = v[kk][e];
+                sc[slot] = (g + kk * LANES) * VEC + e;
+                ++slot;
+            }
+    __syncwarp();
+    for (int i = g; i < total; i += LANES) {
+        const float vi = sv[i];
+        const int ci = sc[i];
+        int rank = 0;
+        for (int q = 0; q < total; ++q) rank += beats(sv[q], sc[q], vi, ci) ? 1 : 0;
+        if (rank < k) atomicOr(&sb[ci >> 5], 1u << (ci & 31));
+    }
+    __syncwarp();
+#pragma unroll
+    for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+            const int col = (g + kk * LANES) * VEC + e;
+            keep[kk][e] = valid[kk][e] && ((sb[col >> 5] >> (col & 31)) & 1u) != 0u;
+        }
+    return true;
+}
 
 }  // namespace kept_detail
 
@@ -71,7 +160,8 @@ __device__ __forceinline__ void kept_load_row(const float* __restrict__ x, int64
 // group of the warp has a NaN in its row).  Every lane of the warp must call it.
 template <int LANES, int NV, int VEC>
 __device__ __forceinline__ void kept_select(const float (&v)[NV][VEC], const bool (&valid)[NV][VEC],
-                                            bool any_nan, int cols, int k, bool (&keep)[NV][VEC]) {
+                                            bool any_nan, int cols, int k, bool (&keep)[NV][VEC],
+                                            KeptScratch* ks = nullptr) {
     using namespace kept_detail;
     const int g = threadIdx.x % LANES;
     const int leader = (threadIdx.x & 31) - g;
@@ -152,6 +242,9 @@ __device__ __forceinline__ void kept_select(const float (&v)[NV][VEC], const boo
                 const int c = (g + kk * LANES) * VEC + e;
                 keep[kk][e] = c == i1 || c == i2;
             }
+    } else if (LANES >= 8 && k <= LANES && ks != nullptr && cols <= 1024 &&
+               kept_by_candidates<LANES, NV, VEC>(v, valid, k, keep, ks)) {
+        // ranked among the candidates
     } else if (k <= kMaxRounds || cols - k <= kMaxRounds) {
         // Rounds of "best remaining entry".  Without NaN, float comparison is
         // the order of the rule (-0 == +0 ties, broken by column): from the

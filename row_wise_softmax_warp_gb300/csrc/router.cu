@@ -25,6 +25,7 @@ __global__ void __launch_bounds__(kBlockThreads)
 router_group(const float* x, const uint8_t* __restrict__ mask, float* p, float* __restrict__ kept,
              int64_t rows, int cols, int k) {
     constexpr int GPB = kBlockThreads / LANES;
+    __shared__ KeptScratch kscratch[kBlockThreads / 32];  // the candidate path's, one per warp
     const int g = threadIdx.x % LANES;
     const int grp = threadIdx.x / LANES;
     const int nch = cols / VEC;
@@ -84,7 +85,7 @@ router_group(const float* x, const uint8_t* __restrict__ mask, float* p, float* 
         // Top-k kept mask of those probabilities.
         bool keep[NV][VEC];
         kept_select<LANES, NV, VEC>(v, valid, __any_sync(kFullMask, !(fabsf(probe) <= 3.402823466e38f)), cols,
-                                    k, keep);
+                                    k, keep, &kscratch[threadIdx.x >> 5]);
 #pragma unroll
         for (int kk = 0; kk < NV; ++kk) {
             const int c = g + kk * LANES;

@@ -21,6 +21,7 @@ template <int LANES, int NV, int VEC>
 __global__ void __launch_bounds__(kBlockThreads)
 kept_group(const float* __restrict__ x, float* __restrict__ kept, int64_t rows, int cols, int k) {
     constexpr int GPB = kBlockThreads / LANES;
+    __shared__ KeptScratch kscratch[kBlockThreads / 32];  // the candidate path's, one per warp
     const int g = threadIdx.x % LANES;
     const int grp = threadIdx.x / LANES;
     const int nch = cols / VEC;
@@ -50,7 +51,7 @@ kept_group(const float* __restrict__ x, float* __restrict__ kept, int64_t rows, 
         // A non-finite sum (NaN, or infinities / overflow) sends the warp to the
         // literal count, which is exact for every input.
         kept_select<LANES, NV, VEC>(v, valid, __any_sync(kFullMask, !(fabsf(probe) <= 3.402823466e38f)), cols,
-                                    k, keep);
+                                    k, keep, &kscratch[threadIdx.x >> 5]);
 #pragma unroll
         for (int kk = 0; kk < NV; ++kk) {
             const int c = g + kk * LANES;

@@ -6,7 +6,8 @@ Ops: softmax_fwd, softmax_bwd, attn_fwd, attn_bwd (cols = seq_len), logsumexp,
 softmax_ce, layernorm_fwd, layernorm_bwd, rmsnorm_fwd, rmsnorm_bwd, masked_softmax, topk_kept,
 router_masked_topk, top_k_rows, argmax_onehot, soft_ce, teacher_ce.  For rows of
 more than 1024 floats, top_k_rows and argmax_onehot take logits-like rows
-(top_k_rows with k from ROWOPS_TOPK, default 50).  Inputs
+(top_k_rows with k from ROWOPS_TOPK, default 50); topk_kept and
+router_masked_topk take k from ROWOPS_K (default 2).  Inputs
 follow the workload distributions of ``inputs``; the L2 is flushed (512 MiB
 write) before every call.  Prints the median CUDA-event time per call.
 """
@@ -77,7 +78,7 @@ def make(op: str, rows: int, cols: int, dev):
         if op == "masked_softmax":
             return lambda: ro.rowops_masked_softmax(x, m, p)
         kept = torch.empty_like(p)
-        return lambda: ro.rowops_topk_kept(p, r["k"], kept)
+        return lambda: ro.rowops_topk_kept(p, int(os.environ.get("ROWOPS_K", r["k"])), kept)
     if op in ("soft_ce", "teacher_ce"):
         c = inputs.cross_entropy(0, rows=rows, cols=cols)
         c2 = inputs.cross_entropy(1, rows=rows, cols=cols)
@@ -103,7 +104,7 @@ def make(op: str, rows: int, cols: int, dev):
         x, m = t(r["x"]), t(r["mask"])
         if op == "router_masked_topk":
             p, kept = torch.empty_like(x), torch.empty_like(x)
-            return lambda: ro.rowops_router_masked_topk(x, m, r["k"], p, kept)
+            return lambda: ro.rowops_router_masked_topk(x, m, int(os.environ.get("ROWOPS_K", r["k"])), p, kept)
         if op == "top_k_rows":
             vals = torch.empty((rows, r["k"]), device=dev)
             idx = torch.empty_like(vals)

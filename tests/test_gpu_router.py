@@ -182,3 +182,24 @@ def test_top_k_rows_long_rows(ro, rows, cols, misalign):
             vr, ir = oracle.top_k_rows(x, k, largest)
             assert np.array_equal(host(i), ir.astype(np.float32)), (cols, k, largest)
             assert _same_bits(host(v), vr.astype(np.float32)), (cols, k, largest)
+
+
+@pytest.mark.parametrize("cols", [16, 64, 100, 128, 256, 512, 1000, 1024])
+@pytest.mark.parametrize("k", [3, 4, 8, 16, 32])
+def test_kept_candidates(ro, cols, k):
+    # 3 <= k <= group width: the candidate path (distinct values), and its
+    # fallback to rounds when many entries tie (values on a 1/8 grid)
+    if k >= cols:
+        pytest.skip("k < cols")
+    rng = np.random.default_rng(cols * 7 + k)
+    xs = [rng.normal(0, 2, (300, cols)).astype(np.float32),
+          (rng.integers(-32, 33, (300, cols)) / 8.0).astype(np.float32)]
+    for x in xs:
+        for misalign in (False, True):
+            kept = host(ro.rowops_topk_kept(gpu(x, misalign), k))
+            ref = oracle.topk_kept(x, k).astype(np.float32)
+            assert np.array_equal(kept, ref), (cols, k, misalign, np.argwhere(kept != ref)[:5])
+    r = inputs.router(cols + k, rows=300, cols=cols, p_allow=0.8, blocked_row_frac=0.02)
+    p, kept = ro.rowops_router_masked_topk(gpu(r["x"]), gpu(r["mask"]), k)
+    pr, kr = oracle.router_masked_topk(r["x"], r["mask"], k)
+    assert np.array_equal(host(kept), kr.astype(np.float32)), (cols, k)
