@@ -119,11 +119,86 @@ __device__ __forceinline__ uint32_t group_min_u32(uint32_t v) {
     return v;
 }
 
+// top_k_rows for 3 <= k <= LANES (groups of 8 or more lanes): the entries
+// whose selection key (rank key, complemented for smallest-first) reaches tau,
+// the k-th largest of the group's lane maxima, include the top k (each lane's
+// maximum is an entry of the row, so at least k reach it, and every entry
+// ranked above one that reaches it reaches it too).  When every row of the
+// warp has at most 32 such candidates they are ranked among themselves by
+// counting (larger key first, then lower column) and the first k written;
+// otherwise nothing is touched and false is returned (warp-uniform).
+template <int LANES, int NV, int VEC>
+__device__ __forceinline__ bool topk_by_candidates(const uint32_t (&sel)[NV][VEC], const bool (&avail)[NV][VEC],
+                                                   const float (&v)[NV][VEC], int k, bool live, float* vr,
+                                                   float* ir, KeptScratch* ks) {
+    const int g = threadIdx.x % LANES;
+    const int leader = (threadIdx.x & 31) - g;
+    const int gi = (threadIdx.x & 31) / LANES;
+    uint32_t lm = 0u;  // a lane without entries counts as key 0, which every key reaches
+#pragma unroll
+    for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+        for (int e = 0; e < VEC; ++e)
+            if (avail[kk][e]) lm = max(lm, sel[kk][e]);
+    uint32_t s = lm;  // the group's lane maxima in descending order
+#pragma unroll
+    for (int kk = 2; kk <= LANES; kk <<= 1)
+#pragma unroll
+        for (int j = kk >> 1; j > 0; j >>= 1) {
+            const uint32_t o = __shfl_xor_sync(kFullMask, s, j);
+            const bool lower = (g & j) == 0;
+            const bool desc = (g & kk) == 0;
+            s = (lower == desc) ? max(s, o) : min(s, o);
+        }
+    const uint32_t tau = __shfl_sync(kFullMask, s, leader + k - 1);
+    int cnt = 0;
+#pragma unroll
+    for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) cnt += (avail[kk][e] && sel[kk][e] >= tau) ? 1 : 0;
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < LANES; o <<= 1) {
+        const int y = __shfl_up_sync(kFullMask, incl, o, LANES);
+        if (g >= o) incl += y;
+    }
+    const int total = __shfl_sync(kFullMask, incl, leader + LANES - 1);
+    if (__any_sync(kFullMask, total > 32)) return false;
+    unsigned* sk = ks->bits[gi];
+    int* sc = ks->c[gi];
+    float* sv = ks->v[gi];
+    __syncwarp();  // the warp's previous use of the scratch is over
+    int slot = incl - cnt;
+#pragma unroll
+    for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+        for (int e = 0; e < VEC; ++e)
+            if (avail[kk][e] && sel[kk][e] >= tau) {
+                sk[slot] = sel[kk][e];
+                sc[slot] = (g + kk * LANES) * VEC + e;
+                sv[slot] = v[kk][e];
+                ++slot;
+            }
+    __syncwarp();
+    for (int i = g; i < total; i += LANES) {
+        const uint32_t ki = sk[i];
+        const int ci = sc[i];
+        int rank = 0;
+        for (int q = 0; q < total; ++q) rank += (sk[q] > ki || (sk[q] == ki && sc[q] < ci)) ? 1 : 0;
+        if (live && rank < k) {
+            vr[rank] = sv[i];
+            ir[rank] = float(ci);
+        }
+    }
+    return true;
+}
+
 template <int LANES, int NV, int VEC>
 __global__ void __launch_bounds__(kBlockThreads)
 top_k_rows_group(const float* __restrict__ x, float* __restrict__ values, float* __restrict__ indices,
                  int64_t rows, int cols, int k, int largest) {
     constexpr int GPB = kBlockThreads / LANES;
+    __shared__ KeptScratch kscratch[kBlockThreads / 32];  // the candidate path's, one per warp
     const int g = threadIdx.x % LANES;
     const int grp = threadIdx.x / LANES;
     const int leader = (threadIdx.x & 31) - g;
@@ -214,6 +289,19 @@ top_k_rows_group(const float* __restrict__ x, float* __restrict__ values, float*
                 }
             }
             continue;
+        }
+        if constexpr (LANES >= 8) {
+            if (k <= LANES) {  // block-uniform
+                uint32_t sel[NV][VEC];
+                const uint32_t flip = largest ? 0u : 0xffffffffu;
+#pragma unroll
+                for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) sel[kk][e] = key[kk][e] ^ flip;
+                if (topk_by_candidates<LANES, NV, VEC>(sel, avail, v, k, live, values + row * int64_t(k),
+                                                       indices + row * int64_t(k), &kscratch[threadIdx.x >> 5]))
+                    continue;
+            }
         }
         for (int r = 0; r < k; ++r) {
             uint32_t best = largest ? 0u : 0xffffffffu;

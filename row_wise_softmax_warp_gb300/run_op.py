@@ -6,8 +6,9 @@ Ops: softmax_fwd, softmax_bwd, attn_fwd, attn_bwd (cols = seq_len), logsumexp,
 softmax_ce, layernorm_fwd, layernorm_bwd, rmsnorm_fwd, rmsnorm_bwd, masked_softmax, topk_kept,
 router_masked_topk, top_k_rows, argmax_onehot, soft_ce, teacher_ce.  For rows of
 more than 1024 floats, top_k_rows and argmax_onehot take logits-like rows
-(top_k_rows with k from ROWOPS_TOPK, default 50); topk_kept and
-router_masked_topk take k from ROWOPS_K (default 2).  Inputs
+(top_k_rows with k from ROWOPS_TOPK, default 50); topk_kept,
+router_masked_topk and top_k_rows on shorter rows take k from ROWOPS_K
+(default 2).  Inputs
 follow the workload distributions of ``inputs``; the L2 is flushed (512 MiB
 write) before every call.  Prints the median CUDA-event time per call.
 """
@@ -106,9 +107,10 @@ def make(op: str, rows: int, cols: int, dev):
             p, kept = torch.empty_like(x), torch.empty_like(x)
             return lambda: ro.rowops_router_masked_topk(x, m, int(os.environ.get("ROWOPS_K", r["k"])), p, kept)
         if op == "top_k_rows":
-            vals = torch.empty((rows, r["k"]), device=dev)
+            k = int(os.environ.get("ROWOPS_K", r["k"]))
+            vals = torch.empty((rows, k), device=dev)
             idx = torch.empty_like(vals)
-            return lambda: ro.rowops_top_k_rows(x, r["k"], True, vals, idx)
+            return lambda: ro.rowops_top_k_rows(x, k, True, vals, idx)
         oh = torch.empty_like(x)
         return lambda: ro.rowops_argmax_onehot(x, oh)
     raise SystemExit(f"unknown op {op}")

@@ -203,3 +203,24 @@ def test_kept_candidates(ro, cols, k):
     p, kept = ro.rowops_router_masked_topk(gpu(r["x"]), gpu(r["mask"]), k)
     pr, kr = oracle.router_masked_topk(r["x"], r["mask"], k)
     assert np.array_equal(host(kept), kr.astype(np.float32)), (cols, k)
+
+
+@pytest.mark.parametrize("cols", [16, 64, 128, 256, 1000])
+@pytest.mark.parametrize("k", [3, 8, 16, 32])
+def test_top_k_rows_candidates(ro, cols, k):
+    # 3 <= k <= group width: the candidate path (distinct values, and values
+    # with NaN, infinities and many ties that send rows to the rounds)
+    if k >= cols:
+        pytest.skip("k < cols")
+    rng = np.random.default_rng(cols * 11 + k)
+    x1 = rng.normal(0, 2, (300, cols)).astype(np.float32)
+    x2 = (rng.integers(-16, 17, (300, cols)) / 4.0).astype(np.float32)
+    x2[rng.random(x2.shape) < 0.02] = np.nan
+    x2[rng.random(x2.shape) < 0.02] = -np.inf
+    for x in (x1, x2):
+        for largest in (True, False):
+            for misalign in (False, True):
+                v, i = ro.rowops_top_k_rows(gpu(x, misalign), k, largest)
+                vr, ir = oracle.top_k_rows(x, k, largest)
+                assert np.array_equal(host(i), ir.astype(np.float32)), (cols, k, largest, misalign)
+                assert _same_bits(host(v), vr.astype(np.float32)), (cols, k, largest, misalign)
