@@ -421,50 +421,41 @@ top_k_rows_rowblock(const float* __restrict__ x, float* __restrict__ values, flo
     }
 }
 
-// Rows of 1025..kSelectMaxCols floats with 2 <= k <= kSelectMaxK.  One CTA
-// per row (rows blockIdx.x, + gridDim.x, ...; 256 threads and 4 CTAs per SM
-// for rows of up to 8192 floats, 1024 threads and one CTA per SM beyond) reads the row
-// from global memory once and keeps its selection keys (rank key, complemented
-// for smallest-first) in shared memory.  An entry's order is that of the
-// 64-bit composite (key << 32) | (0xffffffff - column): larger key first, then
-// lower column.
-// Fast path (k <= NT): each thread's largest key is a row entry, so at least k
-// entries reach tau, the smallest over warps of each warp's ceil(k/W)-th
-// largest thread maximum (W warps), and the top k are among the entries at or
-// above tau (for
-// logits, a few times k of them).  Those candidates are sorted (bitonic, in
-// shared memory) and the first k written.
-// When more than kSelectMaxCand entries reach tau, a radix select finds the
-// k-th largest key instead:
-//   passes 1-4  histogram one byte of the keys whose higher bytes equal the
-//               prefix found so far and extend the prefix by the byte holding
-//               the k-th largest key; after the fourth pass the prefix is that
-//               key, T, and `need` says how many entries equal to T are taken;
-//   collect     every entry above T and the `need` lowest columns equal to T
-//               (each thread walks a contiguous segment of columns after one
-//               block scan of its count of entries equal to T), then sort them.
+// Rows of more than 1024 floats with 2 <= k <= kSelectMaxK.  One CTA per row
+// (rows blockIdx.x, + gridDim.x, ...; NT = 256 threads and 4 CTAs per SM for
+// rows of up to 8192 floats, 512 threads and 2 CTAs per SM beyond, so that
+// other CTAs' loads overlap a CTA's selection work).  An entry's order is that
+// of the 64-bit composite (key << 32) | (0xffffffff - column), key = rank key
+// complemented for smallest-first: larger key first, then lower column.
+//   pass 1   read the row from HBM and take each thread's largest key; each
+//            is an entry of the row, so at least k entries reach tau, the
+//            smallest over warps of each warp's ceil(k/W)-th largest thread
+//            maximum (W warps), and the top k are among the entries at or
+//            above tau;
+//   pass 2   read the row again (from the L2, where it still is) and collect
+//            those candidates in shared memory; when there are at most
+//            kSelectMaxCand of them (for logits, a few times k), sort them
+//            (bitonic) and write the first k.
+// Otherwise (large k, or many entries tied at tau) a radix select over the
+// row, again from the L2, finds the k-th largest key T: four passes each
+// histogram one byte of the keys whose higher bytes match the prefix found so
+// far; then the entries above T and the lowest columns equal to T (in column
+// order: a block scan per tile of the row) are collected and sorted.
 // Values are re-read from the row for the output, keeping their bits.
-constexpr int kSelectWarps = 32;  // at most
 constexpr int kSelectMaxK = 1024;
-constexpr int kSelectMaxCols = 51200;  // keys in shared memory: 200 KB
-constexpr int kSelectUnroll = 4;
 constexpr int kSelectMaxCand = 2048;
+constexpr int kSelectUnroll = 4;
 
+template <int NT>
 struct SelectSmem {
-    uint64_t cand[kSelectMaxCand];  // composites: fast-path candidates or the collected k
+    uint64_t cand[kSelectMaxCand];  // composites: candidates, or the collected k
     uint32_t hist[256];
-    uint32_t wtau[kSelectWarps];
-    int scan[kSelectWarps];
+    uint32_t wtau[NT / 32];
+    int scan[NT / 32];
     int count;
     uint32_t prefix;
     int need;
-    int pad;
-    uint32_t keys[4];  // cols entries follow (16-byte aligned)
 };
-
-inline size_t select_smem_bytes(int64_t cols) {
-    return sizeof(SelectSmem) + size_t(cols) * sizeof(uint32_t);
-}
 
 __device__ __forceinline__ uint32_t select_key(float v, uint32_t flip) { return rank_key(v) ^ flip; }
 
@@ -525,9 +516,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
 top_k_rows_select(const float* __restrict__ x, float* __restrict__ values, float* __restrict__ indices,
                   int64_t rows, int cols, int k, int largest) {
     constexpr int W = NT / 32;
-    extern __shared__ __align__(16) unsigned char select_raw[];
-    SelectSmem& sm = *reinterpret_cast<SelectSmem*>(select_raw);
-    uint32_t* keys = sm.keys;
+    __shared__ SelectSmem<NT> sm;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const uint32_t flip = largest ? 0u : 0xffffffffu;
     const int nch = cols / VEC;
@@ -535,7 +524,7 @@ top_k_rows_select(const float* __restrict__ x, float* __restrict__ values, float
         const float* xr = x + row * int64_t(cols);
         float* vr = values + row * int64_t(k);
         float* ir = indices + row * int64_t(k);
-        // keys to shared memory; each thread's largest key
+        // pass 1: each thread's largest key
         uint32_t tmax = 0;
         bool has = false;
         for (int c0 = 0; c0 < nch; c0 += kSelectUnroll * NT) {  // block-uniform
@@ -546,26 +535,16 @@ top_k_rows_select(const float* __restrict__ x, float* __restrict__ values, float
                 if (c < nch) ld_chunk<VEC>(xr + c * VEC, t[u]);
             }
 #pragma unroll
-            for (int u = 0; u < kSelectUnroll; ++u) {
-                const int c = c0 + u * NT + tid;
-                if (c < nch) {
+            for (int u = 0; u < kSelectUnroll; ++u)
+                if (c0 + u * NT + tid < nch) {
                     has = true;
-                    uint32_t kx[VEC];
 #pragma unroll
-                    for (int e = 0; e < VEC; ++e) {
-                        kx[e] = select_key(t[u][e], flip);
-                        tmax = max(tmax, kx[e]);
-                    }
-                    if constexpr (VEC == 4)
-                        *reinterpret_cast<uint4*>(keys + c * 4) = make_uint4(kx[0], kx[1], kx[2], kx[3]);
-                    else
-                        keys[c] = kx[0];
+                    for (int e = 0; e < VEC; ++e) tmax = max(tmax, select_key(t[u][e], flip));
                 }
-            }
         }
-        // tau: each warp's m-th largest maximum (m = ceil(k/32); a thread
-        // without entries counts as key 0, which every key reaches), then the
-        // smallest over warps
+        // tau: each warp's m-th largest maximum (m = ceil(k/W); a thread
+        // without entries counts as key 0, which every key reaches; m > 32
+        // gives no bound), then the smallest over warps
         {
             uint32_t v = has ? tmax : 0u;
 #pragma unroll
@@ -578,25 +557,37 @@ top_k_rows_select(const float* __restrict__ x, float* __restrict__ values, float
                     v = (lower == desc) ? max(v, o) : min(v, o);
                 }
             const int m = (k + W - 1) / W;
-            const uint32_t wt = m <= 32 ? __shfl_sync(kFullMask, v, m - 1) : 0u;  // 0: no bound
+            const uint32_t wt = m <= 32 ? __shfl_sync(kFullMask, v, m - 1) : 0u;
             if (lane == 0) sm.wtau[wid] = wt;
             if (tid == 0) sm.count = 0;
         }
         __syncthreads();
         uint32_t tau = sm.wtau[0];
         for (int w = 1; w < W; ++w) tau = min(tau, sm.wtau[w]);
-        // candidates: entries at or above tau (warp-aggregated slots)
-        for (int j0 = 0; j0 < cols; j0 += NT) {  // block-uniform
-            const int j = j0 + tid;
-            const uint32_t kx = j < cols ? keys[j] : 0u;
-            const bool cand = j < cols && kx >= tau;
-            const unsigned bal = __ballot_sync(kFullMask, cand);
-            if (bal == 0) continue;  // warp-uniform
-            int base = 0;
-            if (lane == 0) base = atomicAdd(&sm.count, __popc(bal));
-            base = __shfl_sync(kFullMask, base, 0);
-            const int slot = base + __popc(bal & ((1u << lane) - 1u));
-            if (cand && slot < kSelectMaxCand) sm.cand[slot] = composite(kx, j);
+        // pass 2: the candidates (warp-aggregated slots)
+        for (int c0 = 0; c0 < nch; c0 += kSelectUnroll * NT) {  // block-uniform
+            float t[kSelectUnroll][VEC];
+#pragma unroll
+            for (int u = 0; u < kSelectUnroll; ++u) {
+                const int c = c0 + u * NT + tid;
+                if (c < nch) ld_chunk<VEC>(xr + c * VEC, t[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < kSelectUnroll; ++u) {
+                const int c = c0 + u * NT + tid;
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    const uint32_t kx = c < nch ? select_key(t[u][e], flip) : 0u;
+                    const bool cand = c < nch && kx >= tau;
+                    const unsigned bal = __ballot_sync(kFullMask, cand);
+                    if (bal == 0) continue;  // warp-uniform
+                    int base = 0;
+                    if (lane == 0) base = atomicAdd(&sm.count, __popc(bal));
+                    base = __shfl_sync(kFullMask, base, 0);
+                    const int slot = base + __popc(bal & ((1u << lane) - 1u));
+                    if (cand && slot < kSelectMaxCand) sm.cand[slot] = composite(kx, c * VEC + e);
+                }
+            }
         }
         __syncthreads();
         const int ncand = sm.count;
@@ -604,24 +595,20 @@ top_k_rows_select(const float* __restrict__ x, float* __restrict__ values, float
             sort_and_write(sm.cand, ncand, k, xr, vr, ir);
             continue;
         }
-        // radix select (many entries tie with or sit just above tau)
-        if (tid < 256) sm.hist[tid] = 0;
-        __syncthreads();
-        for (int j0 = 0; j0 < cols; j0 += NT) {  // block-uniform
-            const int j = j0 + tid;
-            const uint32_t kx = j < cols ? keys[j] : 0u;
-            warp_hist_add(sm.hist, j < cols, kx >> 24, lane);
-        }
+        // radix select of the k-th largest key, over the row in the L2
         uint32_t prefix = 0, pmask = 0;
         int kr = k;  // entries still to find at or below the current prefix
         for (int shift = 24; shift >= 0; shift -= 8) {
-            if (shift < 24) {
-                if (tid < 256) sm.hist[tid] = 0;
-                __syncthreads();
-                for (int j0 = 0; j0 < cols; j0 += NT) {  // block-uniform
-                    const int j = j0 + tid;
-                    const uint32_t kx = j < cols ? keys[j] : 0u;
-                    const bool in = j < cols && (kx & pmask) == prefix;
+            if (tid < 256) sm.hist[tid] = 0;
+            __syncthreads();
+            for (int c0 = 0; c0 < nch; c0 += NT) {  // block-uniform
+                const int c = c0 + tid;
+                float t[VEC];
+                if (c < nch) ld_chunk<VEC>(xr + c * VEC, t);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    const uint32_t kx = c < nch ? select_key(t[e], flip) : 0u;
+                    const bool in = c < nch && (kx & pmask) == prefix;
                     warp_hist_add(sm.hist, in, (kx >> shift) & 255u, lane);
                 }
             }
@@ -658,31 +645,52 @@ top_k_rows_select(const float* __restrict__ x, float* __restrict__ values, float
             kr = sm.need;
             pmask |= 255u << shift;
         }
-        // collect: entries above T, and the kr lowest columns equal to T
+        // collect: entries above T, and the kr lowest columns equal to T; a
+        // tile of the row is NT consecutive chunks, one per thread, so thread
+        // order is column order within a tile
         const uint32_t T = prefix;
-        const int seg = (cols + NT - 1) / NT;
-        const int j_begin = tid * seg;
-        const int j_end = min(cols, j_begin + seg);
-        int eq = 0;
-        for (int j = j_begin; j < j_end; ++j) eq += keys[j] == T ? 1 : 0;
-        int incl = eq;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(kFullMask, incl, o);
-            if (lane >= o) incl += y;
-        }
-        if (lane == 31) sm.scan[wid] = incl;
         if (tid == 0) sm.count = 0;
+        int taken_eq = 0;  // entries equal to T taken in earlier tiles
         __syncthreads();
-        int r = incl - eq;  // rank of this segment's first entry equal to T
-        for (int w = 0; w < wid; ++w) r += sm.scan[w];
-        for (int j = j_begin; j < j_end; ++j) {
-            const uint32_t kx = keys[j];
-            bool take = kx > T;
-            if (kx == T) take = r++ < kr;
-            if (take) sm.cand[atomicAdd(&sm.count, 1)] = composite(kx, j);
+        for (int c0 = 0; c0 < nch; c0 += NT) {  // block-uniform
+            const int c = c0 + tid;
+            float t[VEC];
+            uint32_t kx[VEC];
+            int eq = 0;
+            if (c < nch) {
+                ld_chunk<VEC>(xr + c * VEC, t);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    kx[e] = select_key(t[e], flip);
+                    eq += kx[e] == T ? 1 : 0;
+                }
+            }
+            int incl = eq;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(kFullMask, incl, o);
+                if (lane >= o) incl += y;
+            }
+            if (lane == 31) sm.scan[wid] = incl;
+            __syncthreads();
+            int wbase = 0, tile_eq = 0;
+            for (int w = 0; w < W; ++w) {
+                const int v = sm.scan[w];
+                if (w < wid) wbase += v;
+                tile_eq += v;
+            }
+            int r = taken_eq + wbase + incl - eq;  // rank among equal entries of this thread's first
+            if (c < nch) {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    bool take = kx[e] > T;
+                    if (kx[e] == T) take = r++ < kr;
+                    if (take) sm.cand[atomicAdd(&sm.count, 1)] = composite(kx[e], c * VEC + e);
+                }
+            }
+            taken_eq += tile_eq;
+            __syncthreads();  // sm.scan is rewritten by the next tile
         }
-        __syncthreads();
         sort_and_write(sm.cand, k, k, xr, vr, ir);
     }
 }
@@ -715,21 +723,18 @@ cudaError_t launch_top_k_rows(const float* x, float* values, float* indices, int
     });
     cudaError_t err = cudaSuccess;
     const int sms = sm_count();
-    if (!done && k >= 2 && k <= kSelectMaxK && cols <= kSelectMaxCols && sms > 0) {
-        const size_t smem = select_smem_bytes(cols);
+    if (!done && k >= 2 && k <= kSelectMaxK && sms > 0) {
         auto launch = [&](auto kern, int nt, int per_sm) {
-            err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-            if (err != cudaSuccess) return;
             const int64_t cap = int64_t(sms) * per_sm;
             const unsigned grid = unsigned(rows < cap ? rows : cap);
-            kern<<<grid, nt, smem, stream>>>(x, values, indices, rows, int(cols), int(k), largest ? 1 : 0);
+            kern<<<grid, nt, 0, stream>>>(x, values, indices, rows, int(cols), int(k), largest ? 1 : 0);
         };
-        if (cols <= 8192) {  // 4 CTAs of 256 threads per SM (at most 50 KB of shared memory each)
+        if (cols <= 8192) {  // 4 CTAs of 256 threads per SM
             if (vec4) launch(top_k_rows_select<256, 4>, 256, 4);
             else launch(top_k_rows_select<256, 1>, 256, 4);
-        } else {
-            if (vec4) launch(top_k_rows_select<1024, 4>, 1024, 1);
-            else launch(top_k_rows_select<1024, 1>, 1024, 1);
+        } else {  // 2 CTAs of 512 threads per SM: 61 MB of 50304-float rows stay in the L2
+            if (vec4) launch(top_k_rows_select<512, 4>, 512, 2);
+            else launch(top_k_rows_select<512, 1>, 512, 2);
         }
     } else if (!done) {
         if (vec4)
