@@ -11,9 +11,11 @@ One step = one call of every row op, each on its workload at full size:
 The L2 cache is flushed (a 512 MiB write) before every op, outside its CUDA
 events, so every op starts cold.  value = algorithmic bytes of all ops (the
 minimum each must read and write) / summed device time, in GB/s, over all
-ranks.  e2e repeats the steps through the same public calls with the inputs
-copied from pinned host memory and the outputs copied back inside the timed
-region.  back_to_back times each op launched back to back (no flush, no
+ranks.  e2e repeats the steps through the same public calls as a training
+step runs them: each step uploads its inputs from pinned host memory (each
+once), keeps the intermediates on the device and reads back the mean loss,
+all inside the timed region; e2e_every_buffer instead uploads every op's
+inputs and reads back every output.  back_to_back times each op launched back to back (no flush, no
 events between calls) while cycling through copies of its buffers that total
 more than twice the L2: the per-call cost inside a training step, without the
 few microseconds that an event pair around a single launch adds.
@@ -379,6 +381,132 @@ def barrier(dist, device):
 
 # ----------------------------------------------------------------- GPU arm
 
+def e2e_every_buffer(ops, dev, stream, ke, dist):
+    """End-to-end steps in which every op's inputs come from pinned host memory
+    and every output goes back, per op.  Transfers run on two copy streams (one
+    per direction) and compute on the launching stream, ordered by events, so
+    op i's inputs travel while op i-1 computes and op i-2's outputs return.
+    Returns (ms per step, H2D bytes, D2H bytes)."""
+    import torch
+    table = ops.table()
+    io = ops.e2e_io()
+    names = [n for n, _ in table]
+    pinned_in = {n: [torch.empty(x.shape, dtype=x.dtype, pin_memory=True).copy_(x) for x in io[n][0]]
+                 for n in names}
+    pinned_out = {n: [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in io[n][1]] for n in names}
+    h2d = sum(x.numel() * x.element_size() for n in names for x in io[n][0])
+    d2h = sum(x.numel() * x.element_size() for n in names for x in io[n][1])
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    in_ready = {n: ev() for n in names}
+    computed = {n: ev() for n in names}
+    out_done = {n: ev() for n in names}
+    for n in names:  # mark all as complete once, so the first step's waits pass
+        computed[n].record(stream)
+        out_done[n].record(stream)
+
+    def step():
+        for name, fn in table:
+            with torch.cuda.stream(s_in):
+                s_in.wait_event(computed[name])  # last step's op finished reading its inputs
+                for dst, src in zip(io[name][0], pinned_in[name]):
+                    dst.copy_(src, non_blocking=True)
+                in_ready[name].record(s_in)
+            stream.wait_event(in_ready[name])
+            stream.wait_event(out_done[name])  # last step's outputs are home
+            fn()
+            computed[name].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(computed[name])
+                for dst, src in zip(pinned_out[name], io[name][1]):
+                    dst.copy_(src, non_blocking=True)
+                out_done[name].record(s_out)
+
+    step()
+    torch.cuda.synchronize()
+    barrier(dist, dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    s_in.wait_event(e0)
+    s_out.wait_event(e0)
+    for _ in range(ke):
+        step()
+    for n in names:
+        stream.wait_event(out_done[n])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / ke, h2d, d2h
+
+
+def e2e_step_inputs(ops, dev, stream, ke, dist):
+    """End-to-end steps as a training step runs them: the step's inputs come
+    from pinned host memory, each uploaded once per step just before its first
+    use; intermediates stay on the device (softmax y, LayerNorm xhat and
+    inv_std, attention P, router P); the step's result, the mean
+    cross-entropy loss, is read back.  The upload of an input for the next
+    step waits until this step's last op reading it has run.  Returns
+    (ms per step, H2D bytes, D2H bytes)."""
+    import torch
+    table = ops.table()
+    names = [n for n, _ in table]
+    # external inputs, by the op that first reads them, and their last reader
+    first = {"softmax_fwd": [ops.sx], "softmax_bwd": [ops.sdy], "layernorm_fwd": [ops.lx, ops.lg, ops.lb],
+             "layernorm_bwd": [ops.ldy], "attn_softmax_fwd": [ops.as_], "attn_softmax_bwd": [ops.adp],
+             "logsumexp": [ops.cx], "softmax_ce": [ops.ct], "masked_softmax": [ops.rx, ops.rm], "topk_kept": []}
+    last = {id(ops.sx): "softmax_fwd", id(ops.sdy): "softmax_bwd", id(ops.lx): "layernorm_fwd",
+            id(ops.lg): "layernorm_bwd", id(ops.lb): "layernorm_fwd", id(ops.ldy): "layernorm_bwd",
+            id(ops.as_): "attn_softmax_fwd", id(ops.adp): "attn_softmax_bwd", id(ops.cx): "softmax_ce",
+            id(ops.ct): "softmax_ce", id(ops.rx): "masked_softmax", id(ops.rm): "masked_softmax"}
+    results = {"softmax_ce": [ops.cml]}
+    pinned_in = {n: [torch.empty(x.shape, dtype=x.dtype, pin_memory=True).copy_(x) for x in first[n]]
+                 for n in names}
+    pinned_out = {n: [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in results.get(n, [])]
+                  for n in names}
+    h2d = sum(x.numel() * x.element_size() for n in names for x in first[n])
+    d2h = sum(x.numel() * x.element_size() for n in names for x in results.get(n, []))
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    in_ready = {n: ev() for n in names}
+    computed = {n: ev() for n in names}
+    out_done = {n: ev() for n in names}
+    for n in names:  # mark all as complete once, so the first step's waits pass
+        computed[n].record(stream)
+        out_done[n].record(stream)
+
+    def step():
+        for name, fn in table:
+            with torch.cuda.stream(s_in):
+                for dst, src in zip(first[name], pinned_in[name]):
+                    s_in.wait_event(computed[last[id(dst)]])  # last step's readers are done with it
+                    dst.copy_(src, non_blocking=True)
+                in_ready[name].record(s_in)
+            stream.wait_event(in_ready[name])
+            stream.wait_event(out_done[name])  # last step's result is home
+            fn()
+            computed[name].record(stream)
+            if pinned_out[name]:
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(computed[name])
+                    for dst, src in zip(pinned_out[name], results[name]):
+                        dst.copy_(src, non_blocking=True)
+                    out_done[name].record(s_out)
+
+    step()
+    torch.cuda.synchronize()
+    barrier(dist, dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    s_in.wait_event(e0)
+    s_out.wait_event(e0)
+    for _ in range(ke):
+        step()
+    for n in names:
+        stream.wait_event(out_done[n])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / ke, h2d, d2h
+
+
 def gpu_leg(args):
     import torch
     rank, world, dist = dist_setup()
@@ -493,66 +621,16 @@ def gpu_leg(args):
         graph_step = {"unavailable": str(e).splitlines()[0][:200]}
 
     # ------------------------------------------------------------ e2e
-    # Same calls, inputs from pinned host memory and outputs back to pinned host
-    # memory inside the timed region.  Transfers run on two copy streams (one
-    # per direction) and compute on the launching stream, ordered by events, so
-    # op i's inputs travel while op i-1 computes and op i-2's outputs return.
-    # Every op has its own device buffers here, so the overlap has no hazards.
-    ops2 = Ops(data, dev)
-    table2 = ops2.table()
-    io = ops2.e2e_io()
-    names = [n for n, _ in table2]
-    pinned_in = {n: [torch.empty(x.shape, dtype=x.dtype, pin_memory=True).copy_(x) for x in io[n][0]]
-                 for n in names}
-    pinned_out = {n: [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in io[n][1]] for n in names}
-    h2d = sum(x.numel() * x.element_size() for n in names for x in io[n][0])
-    d2h = sum(x.numel() * x.element_size() for n in names for x in io[n][1])
     ke = max(1, args.e2e_steps if args.e2e_steps else K)
-    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    ev = lambda: torch.cuda.Event()  # noqa: E731
-    in_ready = {n: ev() for n in names}
-    computed = {n: ev() for n in names}
-    out_done = {n: ev() for n in names}
-    for n in names:  # mark all as complete once, so the first step's waits pass
-        computed[n].record(stream)
-        out_done[n].record(stream)
-
-    def e2e_step():
-        for name, fn in table2:
-            with torch.cuda.stream(s_in):
-                s_in.wait_event(computed[name])  # last step's op finished reading its inputs
-                for dst, src in zip(io[name][0], pinned_in[name]):
-                    dst.copy_(src, non_blocking=True)
-                in_ready[name].record(s_in)
-            stream.wait_event(in_ready[name])
-            stream.wait_event(out_done[name])  # last step's outputs are home
-            fn()
-            computed[name].record(stream)
-            with torch.cuda.stream(s_out):
-                s_out.wait_event(computed[name])
-                for dst, src in zip(pinned_out[name], io[name][1]):
-                    dst.copy_(src, non_blocking=True)
-                out_done[name].record(s_out)
-
-    e2e_step()
-    torch.cuda.synchronize()
-    barrier(dist, dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    s_in.wait_event(e0)
-    s_out.wait_event(e0)
-    for _ in range(ke):
-        e2e_step()
-    for n in names:
-        stream.wait_event(out_done[n])
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms_local = e0.elapsed_time(e1) / ke
+    ops2 = Ops(data, dev)
+    e2e_ms_local, h2d, d2h = e2e_step_inputs(ops2, dev, stream, ke, dist)
+    all_ms_local, all_h2d, all_d2h = e2e_every_buffer(ops2, dev, stream, ke, dist)
     clocks.mark = False
     clocks.stop()
 
     step_ms = max_over_ranks(step_ms_local, dist, dev)
     e2e_ms = max_over_ranks(e2e_ms_local, dist, dev)
+    all_ms = max_over_ranks(all_ms_local, dist, dev)
     wall_ms = max_over_ranks(wall_ms_local, dist, dev)
     per_op = {n: max_over_ranks(per_op_ms[n], dist, dev) for n, _ in table}
     if rank != 0:
@@ -598,7 +676,14 @@ def gpu_leg(args):
                      for n in next_ms},
         "e2e": {"value": round(world * total_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                "ms_per_step": round(e2e_ms, 3), "steps": ke},
+                "ms_per_step": round(e2e_ms, 3), "steps": ke,
+                "note": "each step uploads the step's inputs (each once), keeps the intermediates on the "
+                        "device (softmax y, LayerNorm xhat/inv_std, attention P, router P) and reads back "
+                        "the mean cross-entropy loss"},
+        "e2e_every_buffer": {"value": round(world * total_bytes / (all_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                             "h2d_bytes_per_step": int(all_h2d), "d2h_bytes_per_step": int(all_d2h),
+                             "ms_per_step": round(all_ms, 3), "steps": ke,
+                             "note": "every op's inputs uploaded and every output read back, per op"},
         "clocks": clocks.summary(),
     }
     if graph_step is not None and "ms" in graph_step:
