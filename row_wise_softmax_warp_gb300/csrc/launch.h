@@ -92,11 +92,6 @@ inline unsigned row_grid(int64_t rows, int per_row = 1) {
 
 cudaError_t launch_softmax_fwd(const float* x, float* y, int64_t rows, int64_t cols, bool vec4,
                                cudaStream_t stream);
-// Rows too long for one warp: the TMA kernel (any 4-byte aligned rows), else
-// for vectorised rows the cluster kernel of lse_ce.cu.  Returns false
-// (nothing launched) when neither applies.
-bool launch_softmax_fwd_long(const float* x, float* y, int64_t rows, int64_t cols, bool vec4,
-                             cudaStream_t stream, cudaError_t* err);
 // TMA-streamed long rows (tma_rows.cu): rows of more than 1024 floats from
 // 4-byte aligned buffers (an output row must share its input row's alignment
 // modulo 16 bytes); each returns false, launching nothing, when the shape does

@@ -1,18 +1,13 @@
-// lse_ce.cu - per-row logsumexp, fused softmax cross-entropy (loss + logits
-// gradient) and the long-row softmax forward.
+// lse_ce.cu - per-row logsumexp and fused softmax cross-entropy (loss + logits
+// gradient), and the fixed-order mean of the row losses.
 //
 // Kernel shapes:
-//   *_group           : rows of up to 1024 floats in registers (common.cuh).
-//   *_brow            : rows of 1025..16384 floats in registers, one CTA per
-//                       row (block_rows.cuh).
-//   long_row_cluster  : rows of 1K..128K floats (vectorised).  A thread-block
-//                       cluster of CL CTAs owns one row; each CTA holds a slice
-//                       in registers (NV float4 per thread), reduces its slice
-//                       to (max, sum exp) and the CTAs exchange those pairs
-//                       through distributed shared memory.  The row is read from
-//                       HBM exactly once, and the gradient or probabilities are
-//                       written from registers.
-//   *_rowblock        : any length and alignment, streaming two passes.
+//   *_group    : rows of up to 1024 floats in registers (common.cuh).
+//   *_brow     : rows of 1025..8192 floats in registers, one CTA per row
+//                (block_rows.cuh).
+//   longer rows: the bulk-copy pipeline of tma_rows.cu.
+//   *_rowblock : any length and alignment, streaming two passes (rows whose
+//                output sits on another 16-byte phase than the input).
 #include "block_rows.cuh"
 #include "common.cuh"
 #include "launch.h"
@@ -205,166 +200,6 @@ ce_brow(const float* __restrict__ x, const int32_t* __restrict__ targets, float*
     }
 }
 
-// ---------------------------------------------------------- long rows
-
-enum class LongOp { kLse, kCe, kSoftmax };
-
-__device__ __forceinline__ void cluster_arrive() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() {
-    asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
-}
-
-template <LongOp OP, int NV>
-__global__ void __launch_bounds__(kBlockThreads)
-long_row_cluster(const float* x, float* out,  // out may be x (in-place softmax)
-                 const int32_t* __restrict__ targets, float* __restrict__ aux, int64_t rows,
-                 int cols, float grad_scale) {
-    namespace cg = cooperative_groups;
-    cg::cluster_group cluster = cg::this_cluster();
-    const int CL = int(cluster.num_blocks());
-    const int rank = int(cluster.block_rank());
-    const int tid = threadIdx.x;
-    const int lane = tid & 31;
-    __shared__ float scratch[kBlockThreads / 32];
-    __shared__ float part[2];   // this CTA's (max, sum) published to the cluster
-    __shared__ float total[2];  // the row's (max, sum)
-    const int nch = cols / 4;
-    const int cpc = (nch + CL - 1) / CL;
-    const int c_begin = rank * cpc;
-    const int c_end = min(nch, c_begin + cpc);
-    const int64_t nclusters = gridDim.x / CL;
-    bool pending_wait = false;
-    for (int64_t row = blockIdx.x / CL; row < rows; row += nclusters) {
-        const int64_t off = row * int64_t(cols);
-        float v[NV][4];
-#pragma unroll
-        for (int k = 0; k < NV; ++k) {
-            const int c = c_begin + tid + k * kBlockThreads;
-            if (c < c_end) {
-                ld_chunk<4>(x + off + c * 4, v[k]);
-            } else {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) v[k][e] = -INFINITY;
-            }
-        }
-        float m = -INFINITY;
-#pragma unroll
-        for (int k = 0; k < NV; ++k)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) m = fmaxf(m, v[k][e]);
-        const float mc = block_max<kBlockThreads>(m, scratch);
-        float s = 0.f;
-#pragma unroll
-        for (int k = 0; k < NV; ++k)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                v[k][e] = (mc == -INFINITY) ? 0.f : expf(v[k][e] - mc);
-                s += v[k][e];
-            }
-        const float sc = block_sum<kBlockThreads>(s, scratch);
-        // Publish (mc, sc); peers must have finished reading the previous row's.
-        if (pending_wait) cluster_wait();
-        if (tid == 0) {
-            part[0] = mc;
-            part[1] = sc;
-        }
-        cluster_arrive();
-        cluster_wait();
-        if (tid < 32) {
-            float pm = -INFINITY, ps = 0.f;
-            if (lane < CL) {
-                const float* pq = cluster.map_shared_rank(part, lane);
-                pm = pq[0];
-                ps = pq[1];
-            }
-            MaxSum t{-INFINITY, 0.f};
-            for (int q = 0; q < CL; ++q)
-                t = ms_merge(t, MaxSum{__shfl_sync(kFullMask, pm, q), __shfl_sync(kFullMask, ps, q)});
-            if (lane == 0) {
-                total[0] = t.m;
-                total[1] = t.s;
-            }
-        }
-        cluster_arrive();  // done reading the peers' partials
-        pending_wait = true;
-        __syncthreads();
-        const float tm = total[0], ts = total[1];
-        if constexpr (OP == LongOp::kLse) {
-            if (rank == 0 && tid == 0) out[row] = isinf(tm) ? tm : tm + logf(ts);
-        } else {
-            const float alpha = (mc == -INFINITY) ? 0.f : expf(mc - tm) / ts;
-            int t = -1;
-            if constexpr (OP == LongOp::kCe) t = __ldg(targets + row);
-            const bool tvalid = t >= 0 && t < cols;
-#pragma unroll
-            for (int k = 0; k < NV; ++k) {
-                const int c = c_begin + tid + k * kBlockThreads;
-                if (c < c_end) {
-                    float o[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        if constexpr (OP == LongOp::kCe)
-                            o[e] = grad_scale * (v[k][e] * alpha - ((tvalid && c * 4 + e == t) ? 1.f : 0.f));
-                        else
-                            o[e] = v[k][e] * alpha;
-                    }
-                    st_chunk<4>(out + off + c * 4, o);
-                }
-            }
-            if constexpr (OP == LongOp::kCe) {
-                if (rank == 0 && tid == 0)
-                    aux[row] = tvalid ? (tm + logf(ts)) - __ldg(x + off + t) : __int_as_float(0x7fc00000);
-            }
-        }
-    }
-    // Keep this CTA's shared memory alive until every peer has read it.
-    if (pending_wait) cluster_wait();
-}
-
-// Picks (NV, CL) for a vectorised row of nch float4 chunks; false if too long.
-bool long_row_config(int64_t nch, int* nv, int* cl) {
-    const int nvs[3] = {4, 8, 16};
-    for (int i = 0; i < 3; ++i)
-        for (int c = 1; c <= 8; c *= 2)
-            if (int64_t(c) * kBlockThreads * nvs[i] >= nch) {
-                *nv = nvs[i];
-                *cl = c;
-                return true;
-            }
-    return false;
-}
-
-template <LongOp OP, int NV>
-cudaError_t launch_long_nv(int cl, const float* x, float* out, const int32_t* targets, float* aux,
-                           int64_t rows, int cols, float grad_scale, cudaStream_t stream) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(row_grid(rows, cl));
-    cfg.blockDim = dim3(kBlockThreads);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = cl;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, long_row_cluster<OP, NV>, x, out, targets, aux, rows, cols,
-                              grad_scale);
-}
-
-template <LongOp OP>
-cudaError_t launch_long(int nv, int cl, const float* x, float* out, const int32_t* targets,
-                        float* aux, int64_t rows, int cols, float grad_scale, cudaStream_t stream) {
-    switch (nv) {
-        case 4: return launch_long_nv<OP, 4>(cl, x, out, targets, aux, rows, cols, grad_scale, stream);
-        case 8: return launch_long_nv<OP, 8>(cl, x, out, targets, aux, rows, cols, grad_scale, stream);
-        default: return launch_long_nv<OP, 16>(cl, x, out, targets, aux, rows, cols, grad_scale, stream);
-    }
-}
-
 // ------------------------------------------------------------ streaming
 
 template <int VEC>
@@ -548,7 +383,6 @@ cudaError_t launch_logsumexp(const float* x, float* lse, int64_t rows, int64_t c
         lse_group<G::LANES, G::NV, G::VEC>
             <<<group_grid(rows, G::LANES), kBlockThreads, 0, stream>>>(x, lse, rows, int(cols));
     });
-    int nv = 0, cl = 0;
     cudaError_t err = cudaSuccess;
     if (!done) {
         if (with_block_geometry(vec4, cols, kLseBrowMax, [&](auto geo) {
@@ -557,10 +391,7 @@ cudaError_t launch_logsumexp(const float* x, float* lse, int64_t rows, int64_t c
                     <<<block_row_grid(rows), G::NT, 0, stream>>>(x, lse, rows, int(cols));
             })) {
         } else if (launch_lse_tma(x, lse, rows, cols, stream, &err)) {
-        } else if (vec4 && long_row_config(cols / 4, &nv, &cl))
-            err = launch_long<LongOp::kLse>(nv, cl, x, lse, nullptr, nullptr, rows, int(cols), 1.f,
-                                            stream);
-        else if (vec4)
+        } else if (vec4)
             lse_rowblock<4><<<row_grid(rows), kBlockThreads, 0, stream>>>(x, lse, rows, cols);
         else
             lse_rowblock<1><<<row_grid(rows), kBlockThreads, 0, stream>>>(x, lse, rows, cols);
@@ -578,7 +409,6 @@ cudaError_t launch_softmax_ce(const float* logits, const int32_t* targets, float
         ce_group<G::LANES, G::NV, G::VEC><<<group_grid(rows, G::LANES), kBlockThreads, 0, stream>>>(
             logits, targets, grad, row_loss, rows, int(cols), grad_scale);
     });
-    int nv = 0, cl = 0;
     cudaError_t err = cudaSuccess;
     if (!done) {
         if (with_block_geometry(vec4, cols, kCeBrowMax, [&](auto geo) {
@@ -587,10 +417,7 @@ cudaError_t launch_softmax_ce(const float* logits, const int32_t* targets, float
                     logits, targets, grad, row_loss, rows, int(cols), grad_scale);
             })) {
         } else if (launch_ce_tma(logits, targets, grad, row_loss, rows, cols, grad_scale, stream, &err)) {
-        } else if (vec4 && long_row_config(cols / 4, &nv, &cl))
-            err = launch_long<LongOp::kCe>(nv, cl, logits, grad, targets, row_loss, rows, int(cols),
-                                           grad_scale, stream);
-        else if (vec4)
+        } else if (vec4)
             ce_rowblock<4><<<row_grid(rows), kBlockThreads, 0, stream>>>(logits, targets, grad,
                                                                          row_loss, rows, cols,
                                                                          grad_scale);
@@ -618,18 +445,6 @@ cudaError_t launch_row_mean(const float* row_loss, int64_t rows, double* mean_lo
     const cudaError_t err = cudaLaunchKernelEx(&cfg, ce_mean, row_loss, rows, mean_loss);
     note_launches(1);
     return err != cudaSuccess ? err : cudaGetLastError();
-}
-
-// Long vectorised rows of softmax_fwd use the cluster kernel; called from
-// softmax.cu's dispatcher through this hook.
-bool launch_softmax_fwd_long(const float* x, float* y, int64_t rows, int64_t cols, bool vec4,
-                             cudaStream_t stream, cudaError_t* err) {
-    if (launch_softmax_tma(x, y, rows, cols, stream, err)) return true;
-    if (!vec4) return false;
-    int nv = 0, cl = 0;
-    if (!long_row_config(cols / 4, &nv, &cl)) return false;
-    *err = launch_long<LongOp::kSoftmax>(nv, cl, x, y, nullptr, nullptr, rows, int(cols), 1.f, stream);
-    return true;
 }
 
 }  // namespace rowops

@@ -824,7 +824,7 @@ cudaError_t launch_softmax_fwd(const float* x, float* y, int64_t rows, int64_t c
                 softmax_fwd_brow<G::NT, G::NV, G::VEC>
                     <<<block_row_grid(rows), G::NT, 0, stream>>>(x, y, rows, int(cols));
             })) {
-        } else if (launch_softmax_fwd_long(x, y, rows, cols, vec4, stream, &err)) {
+        } else if (launch_softmax_tma(x, y, rows, cols, stream, &err)) {
         } else if (vec4) {
             softmax_fwd_rowblock<4><<<row_grid(rows), kBlockThreads, 0, stream>>>(x, y, rows, cols);
         } else {
