@@ -278,61 +278,108 @@ ln_bwd_group(const float* __restrict__ dy, const float* __restrict__ gamma,
     cl_wait();  // peers are done with this CTA's bpart
 }
 
-// Any length and alignment: one block per fixed row range accumulates its
-// columns straight into its workspace slot (each column owned by one thread).
-template <int VEC>
-__global__ void __launch_bounds__(kBlockThreads)
-ln_bwd_rowblock(const float* __restrict__ dy, const float* __restrict__ gamma,
-                const float* __restrict__ xhat, const float* __restrict__ inv_std,
-                float* __restrict__ dx, float* __restrict__ ws, int64_t rows, int64_t cols,
-                int64_t rows_per_cta) {
-    __shared__ float scratch[kBlockThreads / 32];
-    const int64_t nch = cols / VEC;
+// Rows of more than 8192 floats: one 1024-thread CTA per SM walks a fixed
+// block of rows in two passes per row (the second reads the row again from
+// the L2, where one row per SM stays); each thread owns the same chunks of
+// every row, so it adds its columns' partials of dgamma and dbeta without
+// atomics, in shared memory when 2 x cols floats fit (SMEM) or else in the
+// CTA's workspace slot, which ends up holding the CTA's partials either way.
+constexpr int kLnLongThreads = 1024;
+constexpr int64_t kLnLongSmemCols = 25600;  // 2 x cols floats in 200 KB
+
+template <int VEC, bool SMEM>
+__global__ void __launch_bounds__(kLnLongThreads, 1)
+ln_bwd_long(const float* __restrict__ dy, const float* __restrict__ gamma, const float* __restrict__ xhat,
+            const float* __restrict__ inv_std, float* __restrict__ dx, float* __restrict__ ws, int64_t rows,
+            int cols, int64_t rows_per_cta) {
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    extern __shared__ __align__(16) float sp[];
+    __shared__ float sc[4 * (kLnLongThreads / 32)];
+    BlockReduce<kLnLongThreads> red(sc);
+    constexpr int NT = kLnLongThreads;
+    constexpr int U = VEC == 4 ? 2 : 8;  // 64 bytes of dy and xhat in flight per thread
+    const int nch = cols / VEC;
     const float inv_cols = 1.0f / float(cols);
     float* wg = ws + int64_t(blockIdx.x) * 2 * cols;
-    float* wb = wg + cols;
-    for (int64_t c = threadIdx.x; c < nch; c += kBlockThreads) {
-        const float z[VEC] = {};
-        st_chunk<VEC>(wg + c * VEC, z);
-        st_chunk<VEC>(wb + c * VEC, z);
+    float* pg = SMEM ? sp : wg;
+    float* pb = pg + cols;
+    for (int c = threadIdx.x; c < nch; c += NT) {
+        st_zero_chunk<VEC>(pg + c * VEC);
+        st_zero_chunk<VEC>(pb + c * VEC);
     }
     const int64_t r_begin = int64_t(blockIdx.x) * rows_per_cta;
     int64_t r_end = r_begin + rows_per_cta;
     if (r_end > rows) r_end = rows;
-    for (int64_t row = r_begin; row < r_end; ++row) {
-        const int64_t off = row * cols;
+    for (int64_t row = r_begin; row < r_end; ++row) {  // block-uniform
+        const int64_t off = row * int64_t(cols);
         float s1 = 0.f, s2 = 0.f;
-        for (int64_t c = threadIdx.x; c < nch; c += kBlockThreads) {
-            float a[VEC], h[VEC], gm[VEC];
-            ld_chunk<VEC>(dy + off + c * VEC, a);
-            ld_chunk<VEC>(xhat + off + c * VEC, h);
-            ld_chunk<VEC>(gamma + c * VEC, gm);
+        for (int c0 = threadIdx.x; c0 < nch; c0 += U * NT) {
+            float a[U][VEC], h[U][VEC];
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                const float gp = a[e] * gm[e];
-                s1 += gp;
-                s2 = fmaf(gp, h[e], s2);
+            for (int u = 0; u < U; ++u) {
+                const int c = c0 + u * NT;
+                if (c < nch) {
+                    ld_chunk<VEC>(dy + off + c * VEC, a[u]);
+                    ld_chunk<VEC>(xhat + off + c * VEC, h[u]);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int c = c0 + u * NT;
+                if (c < nch) {
+                    float gm[VEC];
+                    ld_chunk<VEC>(gamma + c * VEC, gm);
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) {
+                        const float gp = a[u][e] * gm[e];  // g' = dy * gamma
+                        s1 += gp;
+                        s2 = fmaf(gp, h[u][e], s2);
+                    }
+                }
             }
         }
-        s1 = block_sum<kBlockThreads>(s1, scratch) * inv_cols;
-        s2 = block_sum<kBlockThreads>(s2, scratch) * inv_cols;
+        red.sum2(s1, s2);
+        s1 *= inv_cols;
+        s2 *= inv_cols;
         const float r = __ldg(inv_std + row);
-        for (int64_t c = threadIdx.x; c < nch; c += kBlockThreads) {
-            float a[VEC], h[VEC], gm[VEC], o[VEC], pg[VEC], pb[VEC];
-            ld_chunk<VEC>(dy + off + c * VEC, a);
-            ld_chunk<VEC>(xhat + off + c * VEC, h);
-            ld_chunk<VEC>(gamma + c * VEC, gm);
-            ld_chunk_coherent<VEC>(wg + c * VEC, pg);
-            ld_chunk_coherent<VEC>(wb + c * VEC, pb);
+        for (int c0 = threadIdx.x; c0 < nch; c0 += U * NT) {
+            float a[U][VEC], h[U][VEC];
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                o[e] = r * (a[e] * gm[e] - s1 - h[e] * s2);
-                pg[e] = fmaf(a[e], h[e], pg[e]);
-                pb[e] += a[e];
+            for (int u = 0; u < U; ++u) {
+                const int c = c0 + u * NT;
+                if (c < nch) {
+                    ld_chunk<VEC>(dy + off + c * VEC, a[u]);
+                    ld_chunk<VEC>(xhat + off + c * VEC, h[u]);
+                }
             }
-            st_chunk<VEC>(dx + off + c * VEC, o);
-            st_chunk<VEC>(wg + c * VEC, pg);
-            st_chunk<VEC>(wb + c * VEC, pb);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int c = c0 + u * NT;
+                if (c < nch) {
+                    float gm[VEC], o[VEC], tg[VEC], tb[VEC];
+                    ld_chunk<VEC>(gamma + c * VEC, gm);
+                    ld_chunk_coherent<VEC>(pg + c * VEC, tg);
+                    ld_chunk_coherent<VEC>(pb + c * VEC, tb);
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) {
+                        o[e] = r * (a[u][e] * gm[e] - s1 - h[u][e] * s2);
+                        tg[e] = fmaf(a[u][e], h[u][e], tg[e]);
+                        tb[e] += a[u][e];
+                    }
+                    st_chunk<VEC>(dx + off + c * VEC, o);
+                    st_chunk<VEC>(pg + c * VEC, tg);
+                    st_chunk<VEC>(pb + c * VEC, tb);
+                }
+            }
+        }
+    }
+    if constexpr (SMEM) {
+        for (int c = threadIdx.x; c < nch; c += NT) {
+            float tg[VEC], tb[VEC];
+            ld_chunk_coherent<VEC>(pg + c * VEC, tg);
+            ld_chunk_coherent<VEC>(pb + c * VEC, tb);
+            st_chunk<VEC>(wg + c * VEC, tg);
+            st_chunk<VEC>(wg + cols + c * VEC, tb);
         }
     }
 }
@@ -572,9 +619,10 @@ cudaError_t launch_layernorm_fwd(const float* x, const float* gamma, const float
 // per resident CTA of the block-row kernel (1024 threads per SM), one
 // per block of the streaming kernel.
 int64_t ln_bwd_slots(int64_t rows, int64_t cols) {
-    if (cols > 1024 && cols <= kLnBwdBrowMax) {
+    if (cols > 1024) {
         const int sms = sm_count();
-        const int64_t p = int64_t(sms > 0 ? sms : 1) * (1024 / ln_bwd_brow_threads(cols));
+        const int64_t per_sm = cols <= kLnBwdBrowMax ? 1024 / ln_bwd_brow_threads(cols) : 1;
+        const int64_t p = int64_t(sms > 0 ? sms : 1) * per_sm;
         return rows < p ? rows : p;
     }
     return ln_bwd_partials(rows);
@@ -624,12 +672,23 @@ cudaError_t launch_layernorm_bwd(const float* dy, const float* gamma, const floa
     });
     if (!done) {
         const int64_t per_cta = (rows + partials - 1) / partials;
-        if (vec4)
-            ln_bwd_rowblock<4><<<unsigned(partials), kBlockThreads, 0, stream>>>(
-                dy, gamma, xhat, inv_std, dx, ws, rows, cols, per_cta);
-        else
-            ln_bwd_rowblock<1><<<unsigned(partials), kBlockThreads, 0, stream>>>(
-                dy, gamma, xhat, inv_std, dx, ws, rows, cols, per_cta);
+        const bool in_smem = cols <= kLnLongSmemCols;
+        const size_t smem = in_smem ? size_t(2) * size_t(cols) * sizeof(float) : 0;
+        auto launch = [&](auto kern) {
+            if (smem > 0) {
+                err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+                if (err != cudaSuccess) return;
+            }
+            kern<<<unsigned(partials), kLnLongThreads, smem, stream>>>(dy, gamma, xhat, inv_std, dx, ws, rows,
+                                                                       int(cols), per_cta);
+        };
+        if (vec4) {
+            if (in_smem) launch(ln_bwd_long<4, true>);
+            else launch(ln_bwd_long<4, false>);
+        } else {
+            if (in_smem) launch(ln_bwd_long<1, true>);
+            else launch(ln_bwd_long<1, false>);
+        }
     }
     if (err == cudaSuccess) err = cudaGetLastError();
     if (err != cudaSuccess) return err;

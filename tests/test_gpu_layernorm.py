@@ -45,7 +45,7 @@ def test_layernorm_row_counts(ro, rows):
     _run(ro, inputs.layernorm(rows, rows=rows, cols=256))
 
 
-@pytest.mark.parametrize("rows,cols", [(2000, 2048), (700, 4100), (333, 8192)])
+@pytest.mark.parametrize("rows,cols", [(2000, 2048), (700, 4100), (333, 8192), (400, 16384), (300, 30001)])
 @pytest.mark.parametrize("misalign", [False, True])
 def test_layernorm_block_rows_many_rows_per_cta(ro, rows, cols, misalign):
     # rows of 1025..8192 floats: each CTA of the block-row backward walks
