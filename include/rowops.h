@@ -188,7 +188,7 @@ size_t rowops_layernorm_bwd_workspace(int64_t rows, int64_t cols);
  * `workspace` (at least rowops_layernorm_bwd_workspace(rows, cols) bytes of
  * 16-byte aligned device memory; its contents need not be initialised and are
  * garbage afterwards), then a second kernel adds the partials in a fixed order.
- * The workspace size depends on rows and cols and, for rows of 1025..8192
+ * The workspace size depends on rows and cols and, for rows of more than 1024
  * floats (one partial per resident CTA), on the current device's SM count;
  * query it with the device current that will run the call.
  * Concurrent calls need separate workspaces.  cols == 0 is ROWOPS_ERR_SHAPE; a

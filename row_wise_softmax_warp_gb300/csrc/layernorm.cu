@@ -17,6 +17,9 @@
 // Rows of 1025..8192 floats take a block-row stage 1 instead (ln_bwd_brow):
 // one CTA per row at a time, each thread keeping its columns' partials in
 // registers across the CTA's block of rows, one workspace slot per CTA.
+// Longer rows take ln_bwd_long: one 1024-thread CTA per SM, two passes over
+// each row, each thread's column partials in shared memory (or, past 25600
+// floats, in the CTA's workspace slot), one slot per CTA.
 #include "block_rows.cuh"
 #include "common.cuh"
 #include "launch.h"
