@@ -708,6 +708,8 @@ def gpu_leg(args):
         }
     if not args.no_cpu_baseline and world == 1:  # the CPU baseline belongs to the N = 1 line
         line["cpu_baseline"] = cpu_leg(data, budget_s=args.cpu_seconds)
+        one = cpu_leg(data, budget_s=args.cpu_seconds / 6, n_threads=1)
+        line["cpu_baseline"]["single_thread"] = {k: one[k] for k in ("value", "unit", "seconds", "sample")}
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
@@ -715,12 +717,13 @@ def gpu_leg(args):
 
 # ----------------------------------------------------------------- CPU leg
 
-def cpu_leg(data, budget_s=12.0):
-    """Times the double-precision oracle (as it stands) on all host cores, on a
-    bounded, deterministic sample of each workload's rows; returns GB/s of the
-    same algorithmic bytes per processed row."""
+def cpu_leg(data, budget_s=12.0, n_threads=None):
+    """Times the double-precision oracle (as it stands) on all host cores (or
+    `n_threads` of them), on a bounded, deterministic sample of each workload's
+    rows; returns GB/s of the same algorithmic bytes per processed row."""
     import oracle
-    threads = oracle.threads()
+    threads = n_threads or oracle.threads()
+    nt = threads
     share = budget_s / 10.0  # seconds of work per op, roughly
     results = []
 
@@ -737,15 +740,18 @@ def cpu_leg(data, budget_s=12.0):
 
     d = data["softmax"]
     y32 = oracle.softmax_rows(d["x"]).astype(np.float32)
-    run("softmax_fwd", lambda a, b: oracle.softmax_rows(d["x"][a:b]), lambda a, b: (b - a) * 128 * 8, 256, 256)
-    run("softmax_bwd", lambda a, b: oracle.softmax_rows_backward(y32[a:b], d["dy"][a:b]),
+    run("softmax_fwd", lambda a, b: oracle.softmax_rows(d["x"][a:b], n_threads=nt),
+        lambda a, b: (b - a) * 128 * 8, 256, 256)
+    run("softmax_bwd", lambda a, b: oracle.softmax_rows_backward(y32[a:b], d["dy"][a:b], n_threads=nt),
         lambda a, b: (b - a) * 128 * 12, 256, 256)
     n = data["layernorm"]
-    run("layernorm_fwd", lambda a, b: oracle.layernorm_forward(n["x"][a:b], n["gamma"], n["beta"], n["eps"]),
+    run("layernorm_fwd",
+        lambda a, b: oracle.layernorm_forward(n["x"][a:b], n["gamma"], n["beta"], n["eps"], n_threads=nt),
         lambda a, b: (b - a) * (768 * 12 + 4), 4096, 256)
     _, xh, rs = oracle.layernorm_forward(n["x"], n["gamma"], n["beta"], n["eps"])
     xh32, rs32 = xh.astype(np.float32), rs.astype(np.float32)
-    run("layernorm_bwd", lambda a, b: oracle.layernorm_backward(n["dy"][a:b], n["gamma"], xh32[a:b], rs32[a:b]),
+    run("layernorm_bwd",
+        lambda a, b: oracle.layernorm_backward(n["dy"][a:b], n["gamma"], xh32[a:b], rs32[a:b], n_threads=nt),
         lambda a, b: (b - a) * (768 * 12 + 4), 4096, 256)
     at = data["attention"]
     S, sc = at["seq_len"], at["scale"]
@@ -753,29 +759,34 @@ def cpu_leg(data, budget_s=12.0):
     def attn_bytes(a, b, reads):
         q = np.arange(a, b) % S
         return int(4 * (reads * (q + 1).sum() + (b - a) * S))
-    run("attn_softmax_fwd", lambda a, b: oracle.attn_softmax_forward(at["scores"][a:b], S, sc),
+    run("attn_softmax_fwd",
+        lambda a, b: oracle.attn_softmax_forward(at["scores"][a:b], S, sc, row0=a, n_threads=nt),
         lambda a, b: attn_bytes(a, b, 1), at["scores"].shape[0], 1024)
-    run("attn_softmax_bwd", lambda a, b: oracle.attn_softmax_backward(at["scores"][a:b], at["dp"][a:b], S, sc),
+    run("attn_softmax_bwd",
+        lambda a, b: oracle.attn_softmax_backward(at["scores"][a:b], at["dp"][a:b], S, sc, row0=a, n_threads=nt),
         lambda a, b: attn_bytes(a, b, 2), at["scores"].shape[0], 1024)
     c = data["ce"]
-    run("logsumexp", lambda a, b: oracle.logsumexp_rows(c["logits"][a:b]), lambda a, b: (b - a) * (50304 * 4 + 4),
-        8192, 16)
-    run("softmax_ce", lambda a, b: oracle.softmax_cross_entropy(c["logits"][a:b], c["targets"][a:b], 1 / 8192),
+    run("logsumexp", lambda a, b: oracle.logsumexp_rows(c["logits"][a:b], n_threads=nt),
+        lambda a, b: (b - a) * (50304 * 4 + 4), 8192, 16)
+    run("softmax_ce",
+        lambda a, b: oracle.softmax_cross_entropy(c["logits"][a:b], c["targets"][a:b], 1 / 8192, n_threads=nt),
         lambda a, b: (b - a) * (50304 * 8 + 4), 8192, 16)
     r = data["router"]
-    run("masked_softmax", lambda a, b: oracle.masked_softmax(r["x"][a:b], r["mask"][a:b]),
+    run("masked_softmax", lambda a, b: oracle.masked_softmax(r["x"][a:b], r["mask"][a:b], n_threads=nt),
         lambda a, b: (b - a) * 64 * 9, 262144, 8192)
-    run("topk_kept", lambda a, b: oracle.topk_kept(r["x"][a:b], 2), lambda a, b: (b - a) * 64 * 8, 262144, 8192)
+    run("topk_kept", lambda a, b: oracle.topk_kept(r["x"][a:b], 2, n_threads=nt),
+        lambda a, b: (b - a) * 64 * 8, 262144, 8192)
     tot_b = sum(x[2] for x in results)
     tot_t = sum(x[3] for x in results)
     full = {"softmax_fwd": 256, "softmax_bwd": 256, "layernorm_fwd": 4096, "layernorm_bwd": 4096,
             "attn_softmax_fwd": at["scores"].shape[0], "attn_softmax_bwd": at["scores"].shape[0],
             "logsumexp": 8192, "softmax_ce": 8192, "masked_softmax": 262144, "topk_kept": 262144}
+    cores = "one host core" if threads == 1 else "all host cores" if n_threads is None else f"{threads} host cores"
     if all(k == full[n] for n, k, _, _ in results):
-        sample = "the whole workload of every op (double-precision C oracle, all host cores)"
+        sample = "the whole workload of every op (double-precision C oracle, " + cores + ")"
     else:
         sample = "; ".join(f"{n}: {k} of {full[n]} rows" for n, k, _, _ in results) + \
-                 " (first rows of each workload, double-precision C oracle, all host cores)"
+                 " (first rows of each workload, double-precision C oracle, " + cores + ")"
     return {"value": round(tot_b / tot_t / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
             "seconds": round(tot_t, 2), "sample": sample}
 
