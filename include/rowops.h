@@ -188,8 +188,8 @@ size_t rowops_layernorm_bwd_workspace(int64_t rows, int64_t cols);
  * `workspace` (at least rowops_layernorm_bwd_workspace(rows, cols) bytes of
  * 16-byte aligned device memory; its contents need not be initialised and are
  * garbage afterwards), then a second kernel adds the partials in a fixed order.
- * The workspace size depends on rows and cols and, for rows of more than 1024
- * floats (one partial per resident CTA), on the current device's SM count;
+ * The workspace size depends on rows, cols and the current device's SM count
+ * (the partials are per cluster or per CTA of a grid sized to one wave);
  * query it with the device current that will run the call.
  * Concurrent calls need separate workspaces.  cols == 0 is ROWOPS_ERR_SHAPE; a
  * short, NULL or misaligned workspace is ROWOPS_ERR_WORKSPACE.  No output may

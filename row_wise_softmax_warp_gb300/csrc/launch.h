@@ -109,6 +109,13 @@ bool launch_soft_ce_tma(const float* x, const float* w, float* grad, float* row_
                         float grad_scale, cudaStream_t stream, cudaError_t* err);
 bool launch_teacher_ce_tma(const float* s, const float* t, float* grad, float* row_loss, int64_t rows,
                            int64_t cols, float grad_scale, cudaStream_t stream, cudaError_t* err);
+// LayerNorm backward stage 1 on rows of 384..1024 floats on 16-byte
+// boundaries (one CTA per SM, row blocks through the bulk-copy ring); writes
+// ln_bwd_tma_ctas(rows, cols) partials to ws.  ln_bwd_tma_ctas is 0 for
+// shapes it does not take.
+int64_t ln_bwd_tma_ctas(int64_t rows, int64_t cols);
+bool launch_ln_bwd_tma(const float* dy, const float* gamma, const float* xhat, const float* inv_std, float* dx,
+                       float* ws, int64_t rows, int64_t cols, cudaStream_t stream, cudaError_t* err);
 cudaError_t launch_softmax_bwd(const float* y, const float* dy, float* dx, int64_t rows,
                                int64_t cols, bool vec4, cudaStream_t stream);
 cudaError_t launch_attn_fwd(const float* s, float* p, int64_t rows, int64_t cols, int64_t seq_len,

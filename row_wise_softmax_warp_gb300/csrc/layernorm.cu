@@ -151,14 +151,27 @@ ln_fwd_rowblock(const float* __restrict__ x, const float* __restrict__ gamma,
 //   g' = dy*gamma, dx = r*(g' - mean(g') - xhat*mean(g'*xhat)),
 //   dgamma_j = sum_i dy*xhat, dbeta_j = sum_i dy.
 
-// Geometry of the stage-1 grid: a pure function of rows.
-inline int64_t ln_bwd_ctas(int64_t rows) {
+// Resident stage-1 CTAs per SM: shared memory holds (GPB + 1) x 2 x MAXC
+// floats per CTA, so three CTAs of the 1024-float geometries fit and four of
+// the others; the launch bounds give each geometry the registers of that
+// residency.
+constexpr int ln_bwd_blocks_per_sm(int maxc) { return maxc > 768 ? 3 : 4; }
+
+// Geometry of the stage-1 grid, a pure function of rows, cols and the SM
+// count: 8 rows per CTA, at most one wave of resident CTAs (and 1024), in
+// whole clusters; CTAs walk more rows beyond that.
+inline int64_t ln_bwd_ctas(int64_t rows, int64_t cols) {
+    const int sms = sm_count();
+    int64_t cap = int64_t(sms > 0 ? sms : 1) * ln_bwd_blocks_per_sm(cols > 768 ? 1024 : 768);
+    cap = cap / kLnClusterCtas * kLnClusterCtas;
+    if (cap > 1024) cap = 1024;
+    if (cap < kLnClusterCtas) cap = kLnClusterCtas;
     int64_t b = (rows + 7) / 8;
-    if (b > 1024) b = 1024;
+    if (b > cap) b = cap;
     if (b < 1) b = 1;
     return (b + kLnClusterCtas - 1) / kLnClusterCtas * kLnClusterCtas;
 }
-inline int64_t ln_bwd_partials(int64_t rows) { return ln_bwd_ctas(rows) / kLnClusterCtas; }
+inline int64_t ln_bwd_partials(int64_t rows, int64_t cols) { return ln_bwd_ctas(rows, cols) / kLnClusterCtas; }
 
 __device__ __forceinline__ void cl_arrive() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
@@ -169,10 +182,10 @@ __device__ __forceinline__ void cl_wait() {
 
 // Dynamic shared memory: red[GPB groups][2][MAXC] (each group's column
 // partials, dgamma then dbeta) then bpart[2][MAXC] (the CTA's), MAXC = the
-// geometry's largest row.  Four blocks per SM (at most 64 registers) keep the
-// grid (<= 512 CTAs on 4096 rows) in a single wave on 152 SMs.
+// geometry's largest row.  With ln_bwd_blocks_per_sm(MAXC) blocks per SM the
+// grid is a single wave.
 template <int LANES, int NV, int VEC>
-__global__ void __launch_bounds__(kBlockThreads, 4)
+__global__ void __launch_bounds__(kBlockThreads, ln_bwd_blocks_per_sm(LANES * NV * VEC))
 ln_bwd_group(const float* __restrict__ dy, const float* __restrict__ gamma,
              const float* __restrict__ xhat, const float* __restrict__ inv_std,
              float* __restrict__ dx, float* __restrict__ ws, int64_t rows, int cols,
@@ -565,16 +578,19 @@ ln_params_reduce(const float* ws, int64_t partials, int64_t cols,
     const int64_t stride = 2 * cols;
     float t = 0.f;
     if (i < stride) {
-        int64_t p = w;
-        for (; p + 3 * 8 < partials; p += 4 * 8) {
-            const float a = ws[p * stride + i], b = ws[(p + 8) * stride + i];
-            const float c = ws[(p + 16) * stride + i], d = ws[(p + 24) * stride + i];
-            t += a;
-            t += b;
-            t += c;
-            t += d;
+        // Batches of B loads in flight (one L2 round trip per batch for up to
+        // 8 * B partials), added in partial order; a missing partial adds +0.
+        constexpr int B = 24;
+        for (int64_t p0 = w; p0 < partials; p0 += 8 * B) {
+            float v[B];
+#pragma unroll
+            for (int b = 0; b < B; ++b) {
+                const int64_t p = p0 + 8 * b;
+                v[b] = p < partials ? ws[p * stride + i] : 0.f;
+            }
+#pragma unroll
+            for (int b = 0; b < B; ++b) t += v[b];
         }
-        for (; p < partials; p += 8) t += ws[p * stride + i];
     }
     part[w][lane] = t;
     __syncthreads();
@@ -618,9 +634,11 @@ cudaError_t launch_layernorm_fwd(const float* x, const float* gamma, const float
     return cudaGetLastError();
 }
 
-// Column partials of the backward: one per cluster of the group kernel, one
-// per resident CTA of the block-row kernel (1024 threads per SM), one
-// per block of the streaming kernel.
+// Column partials of the backward: one per CTA of the row-block kernel or
+// one per cluster of the group kernel (rows of up to 1024 floats; the
+// workspace takes the larger count, so that it does not depend on alignment),
+// one per resident CTA of the block-row kernel (1024 threads per SM), one per
+// CTA of the long-row kernel.
 int64_t ln_bwd_slots(int64_t rows, int64_t cols) {
     if (cols > 1024) {
         const int sms = sm_count();
@@ -628,7 +646,8 @@ int64_t ln_bwd_slots(int64_t rows, int64_t cols) {
         const int64_t p = int64_t(sms > 0 ? sms : 1) * per_sm;
         return rows < p ? rows : p;
     }
-    return ln_bwd_partials(rows);
+    const int64_t g = ln_bwd_partials(rows, cols), t = ln_bwd_tma_ctas(rows, cols);
+    return g > t ? g : t;
 }
 
 size_t layernorm_bwd_workspace(int64_t rows, int64_t cols) {
@@ -640,9 +659,14 @@ cudaError_t launch_layernorm_bwd(const float* dy, const float* gamma, const floa
                                  const float* inv_std, float* dx, float* dgamma, float* dbeta,
                                  int64_t rows, int64_t cols, float* ws, bool vec4,
                                  cudaStream_t stream) {
-    const int64_t partials = ln_bwd_slots(rows, cols);
+    int64_t partials = ln_bwd_slots(rows, cols);
     cudaError_t err = cudaSuccess;
-    bool done = with_ln_bwd_brow_geometry(vec4, cols, [&](auto geo) {
+    bool done = false;
+    if (vec4 && launch_ln_bwd_tma(dy, gamma, xhat, inv_std, dx, ws, rows, cols, stream, &err)) {
+        done = true;
+        partials = ln_bwd_tma_ctas(rows, cols);
+    }
+    if (!done) done = with_ln_bwd_brow_geometry(vec4, cols, [&](auto geo) {
         using G = decltype(geo);
         const int64_t per_cta = (rows + partials - 1) / partials;
         ln_bwd_brow<G::NT, G::NV, G::VEC><<<unsigned(partials), G::NT, 0, stream>>>(
@@ -656,6 +680,7 @@ cudaError_t launch_layernorm_bwd(const float* dy, const float* gamma, const floa
         auto kern = ln_bwd_group<G::LANES, G::NV, G::VEC>;
         err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
         if (err != cudaSuccess) return;
+        partials = ln_bwd_partials(rows, cols);
         const int64_t ctas = partials * kLnClusterCtas;
         const int64_t per_cta = (rows + ctas - 1) / ctas;
         cudaLaunchConfig_t cfg = {};

@@ -45,6 +45,15 @@ def test_layernorm_row_counts(ro, rows):
     _run(ro, inputs.layernorm(rows, rows=rows, cols=256))
 
 
+@pytest.mark.parametrize("rows", [1, 15, 16, 17, 151, 153, 4097, 20000])
+@pytest.mark.parametrize("cols", [384, 388, 764, 1020, 1024])
+def test_layernorm_bwd_row_blocks(ro, rows, cols):
+    # rows of 384..1024 floats on 16-byte boundaries: blocks of rows through
+    # the bulk-copy ring, with partial last slots and blocks, CTAs with fewer
+    # rows than warps, and the CTA cap of the 1020- and 1024-float rows
+    _run(ro, inputs.layernorm(rows * 7 + cols, rows=rows, cols=cols))
+
+
 @pytest.mark.parametrize("rows,cols", [(2000, 2048), (700, 4100), (333, 8192), (400, 16384), (300, 30001)])
 @pytest.mark.parametrize("misalign", [False, True])
 def test_layernorm_block_rows_many_rows_per_cta(ro, rows, cols, misalign):
