@@ -116,6 +116,10 @@ bool launch_teacher_ce_tma(const float* s, const float* t, float* grad, float* r
 int64_t ln_bwd_tma_ctas(int64_t rows, int64_t cols);
 bool launch_ln_bwd_tma(const float* dy, const float* gamma, const float* xhat, const float* inv_std, float* dx,
                        float* ws, int64_t rows, int64_t cols, cudaStream_t stream, cudaError_t* err);
+// Softmax backward on long rows (two passes through the ring); y and dy must
+// share their alignment modulo 16 bytes.
+bool launch_softmax_bwd_tma(const float* y, const float* dy, float* dx, int64_t rows, int64_t cols,
+                            cudaStream_t stream, cudaError_t* err);
 cudaError_t launch_softmax_bwd(const float* y, const float* dy, float* dx, int64_t rows,
                                int64_t cols, bool vec4, cudaStream_t stream);
 cudaError_t launch_attn_fwd(const float* s, float* p, int64_t rows, int64_t cols, int64_t seq_len,

@@ -843,19 +843,23 @@ cudaError_t launch_softmax_bwd(const float* y, const float* dy, float* dx, int64
         softmax_bwd_group<G::LANES, G::NV, G::VEC>
             <<<group_grid(rows, G::LANES), kBlockThreads, 0, stream>>>(y, dy, dx, rows, int(cols));
     });
+    cudaError_t err = cudaSuccess;
     if (!done) {
         if (with_block_geometry(vec4, cols, kBlockRowMax, [&](auto geo) {
                 using G = decltype(geo);
                 softmax_bwd_brow<G::NT, G::NV, G::VEC>
                     <<<block_row_grid(rows), G::NT, 0, stream>>>(y, dy, dx, rows, int(cols));
             })) {
+        } else if (launch_softmax_bwd_tma(y, dy, dx, rows, cols, stream, &err)) {
+            // longer rows: (y, dy) chunk pairs through the bulk-copy ring, two passes
         } else if (vec4)
             softmax_bwd_rowblock<4><<<row_grid(rows), kBlockThreads, 0, stream>>>(y, dy, dx, rows, cols);
         else
             softmax_bwd_rowblock<1><<<row_grid(rows), kBlockThreads, 0, stream>>>(y, dy, dx, rows, cols);
     }
     note_launches(1);
-    return cudaGetLastError();
+    const cudaError_t last = cudaGetLastError();
+    return err != cudaSuccess ? err : last;
 }
 
 // Split rows for vectorised rows of 513..1024 floats (two warps per row): the

@@ -384,6 +384,45 @@ __device__ __forceinline__ bool rendezvous4(float (*red)[kConsumerWarps][4], uin
 }
 
 // ----------------------------------------------- two-input rows, two passes
+// Producer of the two-input kernels (one lane): the chunk pairs (x_k, w_k) of
+// each of the CTA's rows, twice (pass 0 with the evict-normal L2 policy, pass 1
+// evict-first), into consecutive ring slots.
+__device__ void produce_pairs(const float* x, const float* w, int64_t rows, int cols, int chunk, int nslot,
+                              float* buf, uint64_t* full, uint64_t* empty, volatile int* abort_flag) {
+    const uint64_t keep = policy_evict_normal(), drop = policy_evict_first();
+    uint64_t n = 0;
+    bool ok = true;
+    for (int64_t row = blockIdx.x; ok && row < rows; row += gridDim.x) {
+        int head, body;
+        row_split(x + row * int64_t(cols), cols, head, body);
+        const float* src[2] = {x + row * int64_t(cols) + head, w + row * int64_t(cols) + head};
+        const int nch = (body + chunk - 1) / chunk;
+        for (int pass = 0; ok && pass < 2; ++pass)
+            for (int k = 0; ok && k < nch; ++k)
+                for (int in = 0; in < 2; ++in, ++n) {
+                    const int s = int(n % nslot);
+                    const uint64_t use = n / nslot;
+                    if (use > 0 && !mbar_wait(&empty[s], uint32_t((use - 1) & 1), abort_flag)) {
+                        raise_abort(abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    const int cnt = min(chunk, body - k * chunk);
+                    mbar_arrive_expect_tx(&full[s], uint32_t(cnt) * 4u);
+                    bulk_load_hint(buf + size_t(s) * chunk, src[in] + size_t(k) * chunk, uint32_t(cnt) * 4u,
+                                   &full[s], pass == 0 ? keep : drop);
+                }
+    }
+    if (!ok) {
+        // Let the copies already issued land before the CTA's shared memory goes away.
+        const uint64_t first = n > uint64_t(nslot) ? n - nslot : 0;
+        for (uint64_t j = first; j < n; ++j) {
+            volatile int never = 0;
+            mbar_wait(&full[j % nslot], uint32_t((j / nslot) & 1), &never);
+        }
+    }
+}
+
 // Weighted-logits and fixed-teacher cross-entropy on long rows: x (logits or
 // student) and w (weights or teacher logits) stream through the ring as
 // chunk pairs (x_k, w_k), twice per row: pass 0 folds the running (max, sum)
@@ -427,40 +466,7 @@ tma_rows2(const float* x, const float* w, float* grad, float* __restrict__ row_l
     __syncthreads();
 
     if (warp == 0) {
-        // ------------------------------------------------------- producer
-        if (lane != 0) return;
-        const uint64_t keep = policy_evict_normal(), drop = policy_evict_first();
-        uint64_t n = 0;
-        bool ok = true;
-        for (int64_t row = blockIdx.x; ok && row < rows; row += gridDim.x) {
-            int head, body;
-            row_split(x + row * int64_t(cols), cols, head, body);
-            const float* src[2] = {x + row * int64_t(cols) + head, w + row * int64_t(cols) + head};
-            const int nch = (body + chunk - 1) / chunk;
-            for (int pass = 0; ok && pass < 2; ++pass)
-                for (int k = 0; ok && k < nch; ++k)
-                    for (int in = 0; in < 2; ++in, ++n) {
-                        const int s = int(n % nslot);
-                        const uint64_t use = n / nslot;
-                        if (use > 0 && !mbar_wait(&empty[s], uint32_t((use - 1) & 1), &abort_flag)) {
-                            raise_abort(&abort_flag);
-                            ok = false;
-                            break;
-                        }
-                        const int cnt = min(chunk, body - k * chunk);
-                        mbar_arrive_expect_tx(&full[s], uint32_t(cnt) * 4u);
-                        bulk_load_hint(buf + size_t(s) * chunk, src[in] + size_t(k) * chunk, uint32_t(cnt) * 4u,
-                                       &full[s], pass == 0 ? keep : drop);
-                    }
-        }
-        if (!ok) {
-            // Let the copies already issued land before the CTA's shared memory goes away.
-            const uint64_t first = n > uint64_t(nslot) ? n - nslot : 0;
-            for (uint64_t j = first; j < n; ++j) {
-                volatile int never = 0;
-                mbar_wait(&full[j % nslot], uint32_t((j / nslot) & 1), &never);
-            }
-        }
+        if (lane == 0) produce_pairs(x, w, rows, cols, chunk, nslot, buf, full, empty, &abort_flag);
         return;
     }
 
@@ -572,6 +578,116 @@ tma_rows2(const float* x, const float* w, float* grad, float* __restrict__ row_l
             float l = all[0][0];
             for (int q = 1; q < kConsumerWarps; ++q) l += all[q][0];
             row_loss[row] = l;
+        }
+    }
+}
+
+// Softmax backward on rows longer than the block-row kernels hold (MicroGPT
+// softmax_backward: dx = y * (dy - sum_k y_k dy_k)): the (y, dy) chunk pairs
+// stream through the ring twice, as in tma_rows2; pass 0 folds the row's dot
+// product, the 16 warps add theirs in warp order, and pass 1 writes dx
+// (evict-first, so the L2 keeps the rows waiting for their second pass).
+// y and dy share their alignment modulo 16 bytes; dx on another phase is
+// written with scalar stores.
+__global__ void __launch_bounds__(kTmaThreads, 1)
+tma_softmax_bwd(const float* y, const float* dy, float* dx, int64_t rows, int cols, int chunk, int nslot,
+                bool dx_vec) {
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    float* buf = reinterpret_cast<float*>(smem_raw);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + size_t(nslot) * chunk * sizeof(float));
+    uint64_t* empty = full + nslot;
+    __shared__ uint64_t red_bar[2];
+    __shared__ float red[2][kConsumerWarps][4];
+    __shared__ volatile int abort_flag;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    if (tid == 0) {
+        for (int s = 0; s < nslot; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumerWarps);
+        }
+        mbar_init(&red_bar[0], kConsumerWarps);
+        mbar_init(&red_bar[1], kConsumerWarps);
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    __syncthreads();
+    if (warp == 0) {
+        if (lane == 0) produce_pairs(y, dy, rows, cols, chunk, nslot, buf, full, empty, &abort_flag);
+        return;
+    }
+
+    const int ct = tid - 32;
+    const int cw = warp - 1;
+    uint64_t n = 0;   // slot uses consumed
+    uint32_t rv = 0;  // rendezvous so far
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const float* yr = y + row * int64_t(cols);
+        const float* dr = dy + row * int64_t(cols);
+        int head, body;
+        row_split(yr, cols, head, body);
+        const int nch = (body + chunk - 1) / chunk;
+        int ej = -1;  // head (warp 0) and tail (warp 1) lanes, as in tma_rows
+        if (ct < head) ej = ct;
+        else if (ct >= 32 && ct - 32 < cols - head - body) ej = head + body + (ct - 32);
+        const float ye = ej >= 0 ? __ldg(yr + ej) : 0.f;
+        const float de = ej >= 0 ? __ldg(dr + ej) : 0.f;
+        float dot = ye * de;
+        for (int k = 0; k < nch; ++k, n += 2) {
+            if (!wait_use(full, nslot, n, &abort_flag) || !wait_use(full, nslot, n + 1, &abort_flag)) return;
+            const int cnt4 = min(chunk, body - k * chunk) >> 2;
+            const float4* ca = reinterpret_cast<const float4*>(buf + size_t(n % nslot) * chunk);
+            const float4* cb = reinterpret_cast<const float4*>(buf + size_t((n + 1) % nslot) * chunk);
+            for (int i = ct; i < cnt4; i += kConsumers) {
+                const float4 a = ca[i], b = cb[i];
+                dot = fmaf(a.x, b.x, dot);
+                dot = fmaf(a.y, b.y, dot);
+                dot = fmaf(a.z, b.z, dot);
+                dot = fmaf(a.w, b.w, dot);
+            }
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&empty[n % nslot]);
+                mbar_arrive(&empty[(n + 1) % nslot]);
+            }
+        }
+        dot = group_sum<32>(dot);
+        float all[kConsumerWarps][4];
+        const float mine[4] = {dot, 0.f, 0.f, 0.f};
+        if (!rendezvous4(red, red_bar, cw, lane, rv, mine, all, &abort_flag)) return;
+        float c = all[0][0];
+        for (int q = 1; q < kConsumerWarps; ++q) c += all[q][0];
+        float* dst = dx + row * int64_t(cols);
+        if (ej >= 0) dst[ej] = ye * (de - c);
+        for (int k = 0; k < nch; ++k, n += 2) {
+            if (!wait_use(full, nslot, n, &abort_flag) || !wait_use(full, nslot, n + 1, &abort_flag)) return;
+            const int cnt4 = min(chunk, body - k * chunk) >> 2;
+            const float4* ca = reinterpret_cast<const float4*>(buf + size_t(n % nslot) * chunk);
+            const float4* cb = reinterpret_cast<const float4*>(buf + size_t((n + 1) % nslot) * chunk);
+            float* dk = dst + head + size_t(k) * chunk;
+            for (int i = ct; i < cnt4; i += kConsumers) {
+                const float4 a = ca[i], b = cb[i];
+                float4 o;
+                o.x = a.x * (b.x - c);
+                o.y = a.y * (b.y - c);
+                o.z = a.z * (b.z - c);
+                o.w = a.w * (b.w - c);
+                if (dx_vec) {
+                    __stcs(reinterpret_cast<float4*>(dk) + i, o);
+                } else {
+                    __stcs(dk + 4 * i, o.x);
+                    __stcs(dk + 4 * i + 1, o.y);
+                    __stcs(dk + 4 * i + 2, o.z);
+                    __stcs(dk + 4 * i + 3, o.w);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&empty[n % nslot]);
+                mbar_arrive(&empty[(n + 1) % nslot]);
+            }
         }
     }
 }
@@ -801,21 +917,29 @@ bool launch_tma(const float* x, float* out, const int32_t* targets, float* aux, 
 // Two-input rows (tma_rows2): a ring of whole chunk pairs in ~192 KB.
 constexpr size_t kRingBytes2 = 192 * 1024;
 
+// Ring of the two-input kernels for rows of `cols` floats: chunk (floats),
+// slots and dynamic shared memory; false when the rows do not suit them.
+bool pair_ring(int64_t cols, int* chunk, int* nslot, size_t* smem) {
+    if (cols < 1024 || cols > INT32_MAX / 2) return false;
+    const int64_t per_row = (cols + kMaxChunk2 - 1) / kMaxChunk2;
+    *chunk = int(((cols + per_row - 1) / per_row + 3) / 4 * 4);
+    int64_t fit = int64_t(kRingBytes2) / (int64_t(*chunk) * 4);
+    if (fit > kMaxSlots) fit = kMaxSlots;
+    if (fit < 2) return false;
+    *nslot = int(fit);
+    *smem = size_t(*nslot) * *chunk * sizeof(float) + 2 * size_t(*nslot) * sizeof(uint64_t);
+    return *smem <= kMaxDynSmem;
+}
+
 template <bool TEACHER>
 bool launch_tma2(const float* x, const float* w, float* grad, float* row_loss, int64_t rows, int64_t cols,
                  float grad_scale, cudaStream_t stream, cudaError_t* err) {
-    if (cols < 1024 || cols > INT32_MAX / 2) return false;
     const uintptr_t xa = reinterpret_cast<uintptr_t>(x);
     if ((xa & 3) != 0 || (reinterpret_cast<uintptr_t>(w) & 15) != (xa & 15)) return false;
     const bool grad_vec = grad != nullptr && (reinterpret_cast<uintptr_t>(grad) & 15) == (xa & 15);
-    const int64_t per_row = (cols + kMaxChunk2 - 1) / kMaxChunk2;
-    const int chunk = int(((cols + per_row - 1) / per_row + 3) / 4 * 4);
-    int64_t fit = int64_t(kRingBytes2) / (int64_t(chunk) * 4);
-    if (fit > kMaxSlots) fit = kMaxSlots;
-    if (fit < 2) return false;
-    const int nslot = int(fit);
-    const size_t smem = size_t(nslot) * chunk * sizeof(float) + 2 * size_t(nslot) * sizeof(uint64_t);
-    if (smem > kMaxDynSmem) return false;
+    int chunk = 0, nslot = 0;
+    size_t smem = 0;
+    if (!pair_ring(cols, &chunk, &nslot, &smem)) return false;
     const int sms = sm_count();
     if (sms <= 0) return false;
     auto kern = tma_rows2<TEACHER>;
@@ -1043,6 +1167,25 @@ bool launch_teacher_ce_tma(const float* s, const float* t, float* grad, float* r
 bool launch_softmax_tma(const float* x, float* y, int64_t rows, int64_t cols, cudaStream_t stream,
                         cudaError_t* err) {
     return launch_tma<RowOp::kSoftmax>(x, y, nullptr, nullptr, rows, cols, 1.f, stream, err);
+}
+
+bool launch_softmax_bwd_tma(const float* y, const float* dy, float* dx, int64_t rows, int64_t cols,
+                            cudaStream_t stream, cudaError_t* err) {
+    const uintptr_t ya = reinterpret_cast<uintptr_t>(y);
+    if ((ya & 3) != 0 || (reinterpret_cast<uintptr_t>(dy) & 15) != (ya & 15)) return false;
+    const bool dx_vec = (reinterpret_cast<uintptr_t>(dx) & 15) == (ya & 15);
+    int chunk = 0, nslot = 0;
+    size_t smem = 0;
+    if (!pair_ring(cols, &chunk, &nslot, &smem)) return false;
+    const int sms = sm_count();
+    if (sms <= 0) return false;
+    *err = cudaFuncSetAttribute(tma_softmax_bwd, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (*err != cudaSuccess) return true;
+    const int64_t grid = rows < sms ? rows : sms;
+    tma_softmax_bwd<<<unsigned(grid), kTmaThreads, smem, stream>>>(y, dy, dx, rows, int(cols), chunk, nslot,
+                                                                   dx_vec);
+    *err = cudaGetLastError();
+    return true;
 }
 
 int64_t ln_bwd_tma_ctas(int64_t rows, int64_t cols) {

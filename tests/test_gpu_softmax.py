@@ -1,10 +1,11 @@
 """GPU parity: softmax_rows forward and backward against the oracle.
 
 Covers the 256 x 128 workload in full, every row-length regime (sub-warp
-groups, whole-warp registers, the cluster long-row kernel, the streaming
+groups, whole-warp registers, CTA rows, the bulk-copy pipelines, the streaming
 fallback), ragged tails, misaligned (scalar-path) buffers and in-place use."""
 import numpy as np
 import pytest
+import torch
 
 import oracle
 from parity_util import check_bound, check_probs, gpu, host, softmax_bwd_bound
@@ -79,3 +80,28 @@ def test_softmax_deterministic(ro):
     a = host(ro.rowops_softmax_fwd(x))
     b = host(ro.rowops_softmax_fwd(x))
     assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def _at_offset(a: np.ndarray, off: int) -> torch.Tensor:
+    """Device copy of `a` whose data starts `off` floats past a 256-byte boundary."""
+    a = np.ascontiguousarray(a, np.float32)
+    flat = torch.zeros(a.size + 8, dtype=torch.float32, device="cuda")
+    view = flat[off:off + a.size].view(a.shape)
+    view.copy_(torch.from_numpy(a).cuda())
+    return view
+
+
+@pytest.mark.parametrize("rows,cols", [(400, 16388), (160, 32768), (3, 100003)])
+@pytest.mark.parametrize("offs", [(0, 0, 0), (1, 1, 0), (2, 2, 3), (0, 1, 0)])
+def test_softmax_bwd_long_rows(ro, rows, cols, offs):
+    # rows past the block-row kernels: (y, dy) chunk pairs through the
+    # bulk-copy ring, with more rows than SMs, heads and tails off 16-byte
+    # boundaries, dx on another phase (scalar stores), and y and dy on
+    # different phases (the streaming fallback)
+    d = _x(rows, cols, rows + cols)
+    y32 = oracle.softmax_rows(d["x"]).astype(np.float32)
+    dx = _at_offset(np.zeros_like(y32), offs[2])
+    ro.rowops_softmax_bwd(_at_offset(y32, offs[0]), _at_offset(d["dy"], offs[1]), dx)
+    check_bound(host(dx), oracle.softmax_rows_backward(y32, d["dy"]), softmax_bwd_bound(y32, d["dy"]),
+                f"softmax bwd {rows}x{cols} offsets {offs}")
+    assert ro.library().rowops_pipeline_timeouts() == 0
