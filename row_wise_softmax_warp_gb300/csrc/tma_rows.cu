@@ -693,14 +693,56 @@ tma_softmax_bwd(const float* y, const float* dy, float* dx, int64_t rows, int co
 }
 
 // ------------------------------------------------- one input, two passes
+// Cluster helpers for the split two-pass kernel.
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+    return r;
+}
+// Every thread of every CTA of the cluster (not warp-aligned).
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release;\n" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire;\n" ::: "memory");
+}
+__device__ __forceinline__ uint32_t map_to_rank(const void* p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
+    return r;
+}
+// Bounded wait on a barrier that another CTA of the cluster arrives on; the
+// acquire makes that CTA's writes before its arrival visible.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+    for (uint32_t i = 0; i < kWaitPolls; ++i) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(smem_addr(bar)), "r"(parity), "r"(kSuspendNs)
+            : "memory");
+        if (ok) return true;
+        if (*abort_flag) return false;
+    }
+    return false;
+}
+
 // Cross-entropy and softmax forward on rows longer than the ring can hold
 // whole: the row streams through the ring twice, pass 0 folding (max, sum)
-// and pass 1 writing the gradient or probabilities.  One row per SM is in
-// flight, so pass 1 reads from the L2 what pass 0 brought in.  Softmax may run
-// in place: every chunk of pass 1 is copied into shared memory before the
-// consumers overwrite it in global memory, and pass 0 of the row is over
-// before pass 1 writes anything.
-template <RowOp OP>
+// and pass 1 writing the gradient or probabilities; pass 1 reads from the L2
+// what pass 0 brought in.  With SPLIT = 2 a cluster of two CTAs (on two SMs)
+// shares each row: rank 0 takes the head and the first half of the body,
+// rank 1 the rest and the tail; after pass 0 each CTA stores its (max, sum)
+// into the other's shared memory and arrives on the other's barrier, and both
+// merge the two pairs in rank order (the same bits in both).  A row then holds
+// half as much of the L2 between its passes, so with one row per SM in flight
+// the second pass finds more of it there.  Every wait is bounded; every thread
+// of the cluster meets at a final cluster barrier, so neither CTA leaves while
+// the other may still write into its shared memory.  Softmax may run in
+// place: every chunk of pass 1 is copied into shared memory before the
+// consumers overwrite it in global memory, and pass 0 of the row is over (in
+// both CTAs) before pass 1 writes anything.
+template <RowOp OP, int SPLIT>
 __global__ void __launch_bounds__(kTmaThreads, 1)
 tma_rows_2pass(const float* x, float* out, const int32_t* __restrict__ targets, float* __restrict__ aux,
                int64_t rows, int cols, int chunk, int nslot, float grad_scale) {
@@ -711,6 +753,8 @@ tma_rows_2pass(const float* x, float* out, const int32_t* __restrict__ targets, 
     __shared__ uint64_t red_bar[2];
     __shared__ float red[2][kConsumerWarps][4];
     __shared__ volatile int abort_flag;
+    __shared__ uint64_t xbar[2];                // SPLIT: the other CTA's (max, sum) has arrived
+    __shared__ __align__(8) float xch[2][2];    // and is here (double-buffered by row parity)
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -719,6 +763,9 @@ tma_rows_2pass(const float* x, float* out, const int32_t* __restrict__ targets, 
         // The mean-loss kernel may be scheduled now; it waits for this grid.
         asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     }
+    const int rank = SPLIT > 1 ? int(cluster_rank()) : 0;
+    const int64_t unit = blockIdx.x / SPLIT;     // rows unit, unit + units, ...
+    const int64_t units = gridDim.x / SPLIT;
     if (tid == 0) {
         for (int s = 0; s < nslot; ++s) {
             mbar_init(&full[s], 1);
@@ -726,121 +773,172 @@ tma_rows_2pass(const float* x, float* out, const int32_t* __restrict__ targets, 
         }
         mbar_init(&red_bar[0], kConsumerWarps);
         mbar_init(&red_bar[1], kConsumerWarps);
+        mbar_init(&xbar[0], 1);
+        mbar_init(&xbar[1], 1);
         abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
     __syncthreads();
+    if constexpr (SPLIT > 1) cluster_sync_all();  // the other CTA's barriers are ready
+
+    // This CTA's part of a row: body floats [lo, hi) (multiples of 4), the
+    // head (rank 0) and the tail (last rank).
+    auto part = [&](int body, int& lo, int& hi) {
+        const int half = ((body / SPLIT) + 3) & ~3;
+        lo = rank == 0 ? 0 : (half < body ? half : body);
+        hi = rank == SPLIT - 1 ? body : (half < body ? half : body);
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------- producer
-        if (lane != 0) return;
-        const uint64_t keep = policy_evict_normal(), drop = policy_evict_first();
-        uint64_t n = 0;
-        bool ok = true;
-        for (int64_t row = blockIdx.x; ok && row < rows; row += gridDim.x) {
-            int head, body;
-            row_split(x + row * int64_t(cols), cols, head, body);
-            const float* src = x + row * int64_t(cols) + head;
-            const int nch = (body + chunk - 1) / chunk;
-            for (int pass = 0; ok && pass < 2; ++pass)
-                for (int k = 0; k < nch; ++k, ++n) {
-                    const uint64_t policy = pass == 0 ? keep : drop;
-                    const int s = int(n % nslot);
-                    const uint64_t use = n / nslot;
-                    if (use > 0 && !mbar_wait(&empty[s], uint32_t((use - 1) & 1), &abort_flag)) {
-                        raise_abort(&abort_flag);
-                        ok = false;
-                        break;
+        if (lane == 0) {
+            const uint64_t keep = policy_evict_normal(), drop = policy_evict_first();
+            uint64_t n = 0;
+            bool ok = true;
+            for (int64_t row = unit; ok && row < rows; row += units) {
+                int head, body, lo, hi;
+                row_split(x + row * int64_t(cols), cols, head, body);
+                part(body, lo, hi);
+                const float* src = x + row * int64_t(cols) + head + lo;
+                const int len = hi - lo;
+                const int nch = (len + chunk - 1) / chunk;
+                for (int pass = 0; ok && pass < 2; ++pass)
+                    for (int k = 0; k < nch; ++k, ++n) {
+                        const uint64_t policy = pass == 0 ? keep : drop;
+                        const int s = int(n % nslot);
+                        const uint64_t use = n / nslot;
+                        if (use > 0 && !mbar_wait(&empty[s], uint32_t((use - 1) & 1), &abort_flag)) {
+                            raise_abort(&abort_flag);
+                            ok = false;
+                            break;
+                        }
+                        const int cnt = min(chunk, len - k * chunk);
+                        mbar_arrive_expect_tx(&full[s], uint32_t(cnt) * 4u);
+                        bulk_load_hint(buf + size_t(s) * chunk, src + size_t(k) * chunk, uint32_t(cnt) * 4u,
+                                       &full[s], policy);
                     }
-                    const int cnt = min(chunk, body - k * chunk);
-                    mbar_arrive_expect_tx(&full[s], uint32_t(cnt) * 4u);
-                    bulk_load_hint(buf + size_t(s) * chunk, src + size_t(k) * chunk, uint32_t(cnt) * 4u, &full[s],
-                                   policy);
+            }
+            if (!ok) {
+                // Let the copies already issued land before the CTA's shared memory goes away.
+                const uint64_t first = n > uint64_t(nslot) ? n - nslot : 0;
+                for (uint64_t j = first; j < n; ++j) {
+                    volatile int never = 0;
+                    mbar_wait(&full[j % nslot], uint32_t((j / nslot) & 1), &never);
                 }
-        }
-        if (!ok) {
-            // Let the copies already issued land before the CTA's shared memory goes away.
-            const uint64_t first = n > uint64_t(nslot) ? n - nslot : 0;
-            for (uint64_t j = first; j < n; ++j) {
-                volatile int never = 0;
-                mbar_wait(&full[j % nslot], uint32_t((j / nslot) & 1), &never);
             }
         }
-        return;
-    }
-
-    // ---------------------------------------------------------- consumers
-    const int ct = tid - 32;
-    const int cw = warp - 1;
-    uint64_t n = 0;   // slot uses consumed
-    uint32_t rv = 0;  // rendezvous so far
-    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
-        const float* xr = x + row * int64_t(cols);
-        int head, body;
-        row_split(xr, cols, head, body);
-        const int nch = (body + chunk - 1) / chunk;
-        int ej = -1;  // head (warp 0) and tail (warp 1) lanes, as in tma_rows
-        if (ct < head) ej = ct;
-        else if (ct >= 32 && ct - 32 < cols - head - body) ej = head + body + (ct - 32);
-        const float xe = ej >= 0 ? xr[ej] : -INFINITY;  // coherent: softmax may run in place
-        float m = -INFINITY, s = 0.f;
-        if (ej >= 0) push1(m, s, xe);
-        for (int k = 0; k < nch; ++k, ++n) {
-            if (!wait_use(full, nslot, n, &abort_flag)) return;
-            const int cnt4 = min(chunk, body - k * chunk) >> 2;
-            const float4* c4 = reinterpret_cast<const float4*>(buf + size_t(n % nslot) * chunk);
-            for (int i = ct; i < cnt4; i += kConsumers) push4(m, s, c4[i]);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[n % nslot]);
-        }
+    } else {
+        // ------------------------------------------------------ consumers
+        const int ct = tid - 32;
+        const int cw = warp - 1;
+        uint64_t n = 0;   // slot uses consumed
+        uint32_t rv = 0;  // rendezvous so far
+        uint32_t it = 0;  // rows of this CTA so far (exchange parity)
+        for (int64_t row = unit; row < rows; row += units, ++it) {
+            const float* xr = x + row * int64_t(cols);
+            int head, body, lo, hi;
+            row_split(xr, cols, head, body);
+            part(body, lo, hi);
+            const int len = hi - lo;
+            const int nch = (len + chunk - 1) / chunk;
+            int ej = -1;  // head (warp 0 of rank 0) and tail (warp 1 of the last rank) lanes
+            if (rank == 0 && ct < head) ej = ct;
+            else if (rank == SPLIT - 1 && ct >= 32 && ct - 32 < cols - head - body) ej = head + body + (ct - 32);
+            const float xe = ej >= 0 ? xr[ej] : -INFINITY;  // coherent: softmax may run in place
+            float m = -INFINITY, s = 0.f;
+            if (ej >= 0) push1(m, s, xe);
+            bool ok = true;
+            for (int k = 0; k < nch; ++k, ++n) {
+                if (!wait_use(full, nslot, n, &abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const int cnt4 = min(chunk, len - k * chunk) >> 2;
+                const float4* c4 = reinterpret_cast<const float4*>(buf + size_t(n % nslot) * chunk);
+                for (int i = ct; i < cnt4; i += kConsumers) push4(m, s, c4[i]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[n % nslot]);
+            }
+            if (!ok) break;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            merge2(m, s, __shfl_xor_sync(kFullMask, m, o), __shfl_xor_sync(kFullMask, s, o));
-        float all[kConsumerWarps][4];
-        const float mine[4] = {m, s, 0.f, 0.f};
-        if (!rendezvous4(red, red_bar, cw, lane, rv, mine, all, &abort_flag)) return;
-        float M = all[0][0], S = all[0][1];
-        for (int q = 1; q < kConsumerWarps; ++q) merge2(M, S, all[q][0], all[q][1]);
-        const float inv = 1.0f / S;
-        int t = -1;
-        if constexpr (OP == RowOp::kCe) {
-            t = __ldg(targets + row);
-            if (ct == 0) {
-                const float lse = isinf(M) ? M : M + logf(S);
-                aux[row] = (t >= 0 && t < cols) ? lse - __ldg(xr + t) : __int_as_float(0x7fc00000);
-            }
-        }
-        float* dst = out + row * int64_t(cols);
-        if (ej >= 0) {
-            float p = ex2((xe - M) * kLog2e) * inv;
-            if constexpr (OP == RowOp::kCe) p = grad_scale * (p - (ej == t ? 1.f : 0.f));
-            dst[ej] = p;
-        }
-        for (int k = 0; k < nch; ++k, ++n) {
-            if (!wait_use(full, nslot, n, &abort_flag)) return;
-            const int cnt4 = min(chunk, body - k * chunk) >> 2;
-            const float4* c4 = reinterpret_cast<const float4*>(buf + size_t(n % nslot) * chunk);
-            float4* d4 = reinterpret_cast<float4*>(dst + head + size_t(k) * chunk);
-            for (int i = ct; i < cnt4; i += kConsumers) {
-                const float4 v = c4[i];
-                float4 p;
-                p.x = ex2((v.x - M) * kLog2e) * inv;
-                p.y = ex2((v.y - M) * kLog2e) * inv;
-                p.z = ex2((v.z - M) * kLog2e) * inv;
-                p.w = ex2((v.w - M) * kLog2e) * inv;
-                if constexpr (OP == RowOp::kCe) {
-                    const int j = head + k * chunk + 4 * i;
-                    p.x = grad_scale * (p.x - (j == t ? 1.f : 0.f));
-                    p.y = grad_scale * (p.y - (j + 1 == t ? 1.f : 0.f));
-                    p.z = grad_scale * (p.z - (j + 2 == t ? 1.f : 0.f));
-                    p.w = grad_scale * (p.w - (j + 3 == t ? 1.f : 0.f));
+            for (int o = 16; o > 0; o >>= 1)
+                merge2(m, s, __shfl_xor_sync(kFullMask, m, o), __shfl_xor_sync(kFullMask, s, o));
+            float all[kConsumerWarps][4];
+            const float mine[4] = {m, s, 0.f, 0.f};
+            if (!rendezvous4(red, red_bar, cw, lane, rv, mine, all, &abort_flag)) break;
+            float M = all[0][0], S = all[0][1];
+            for (int q = 1; q < kConsumerWarps; ++q) merge2(M, S, all[q][0], all[q][1]);
+            if constexpr (SPLIT > 1) {
+                const int par = int(it & 1);
+                if (ct == 0) {
+                    const uint32_t other = uint32_t(rank ^ 1);
+                    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};\n" ::"r"(map_to_rank(&xch[par][0], other)),
+                                 "f"(M), "f"(S)
+                                 : "memory");
+                    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(
+                                     map_to_rank(&xbar[par], other))
+                                 : "memory");
                 }
-                __stcs(&d4[i], p);  // written once, not read again: evict first
+                if (!mbar_wait_cluster(&xbar[par], (it >> 1) & 1, &abort_flag)) {
+                    raise_abort(&abort_flag);
+                    break;
+                }
+                const float Mo = xch[par][0], So = xch[par][1];
+                if (rank == 0) {
+                    merge2(M, S, Mo, So);
+                } else {
+                    float M0 = Mo, S0 = So;
+                    merge2(M0, S0, M, S);
+                    M = M0;
+                    S = S0;
+                }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[n % nslot]);
+            const float inv = 1.0f / S;
+            int t = -1;
+            if constexpr (OP == RowOp::kCe) {
+                t = __ldg(targets + row);
+                if (rank == 0 && ct == 0) {
+                    const float lse = isinf(M) ? M : M + logf(S);
+                    aux[row] = (t >= 0 && t < cols) ? lse - __ldg(xr + t) : __int_as_float(0x7fc00000);
+                }
+            }
+            float* dst = out + row * int64_t(cols);
+            if (ej >= 0) {
+                float p = ex2((xe - M) * kLog2e) * inv;
+                if constexpr (OP == RowOp::kCe) p = grad_scale * (p - (ej == t ? 1.f : 0.f));
+                dst[ej] = p;
+            }
+            for (int k = 0; k < nch; ++k, ++n) {
+                if (!wait_use(full, nslot, n, &abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const int cnt4 = min(chunk, len - k * chunk) >> 2;
+                const float4* c4 = reinterpret_cast<const float4*>(buf + size_t(n % nslot) * chunk);
+                float4* d4 = reinterpret_cast<float4*>(dst + head + lo + size_t(k) * chunk);
+                for (int i = ct; i < cnt4; i += kConsumers) {
+                    const float4 v = c4[i];
+                    float4 p;
+                    p.x = ex2((v.x - M) * kLog2e) * inv;
+                    p.y = ex2((v.y - M) * kLog2e) * inv;
+                    p.z = ex2((v.z - M) * kLog2e) * inv;
+                    p.w = ex2((v.w - M) * kLog2e) * inv;
+                    if constexpr (OP == RowOp::kCe) {
+                        const int j = head + lo + k * chunk + 4 * i;
+                        p.x = grad_scale * (p.x - (j == t ? 1.f : 0.f));
+                        p.y = grad_scale * (p.y - (j + 1 == t ? 1.f : 0.f));
+                        p.z = grad_scale * (p.z - (j + 2 == t ? 1.f : 0.f));
+                        p.w = grad_scale * (p.w - (j + 3 == t ? 1.f : 0.f));
+                    }
+                    __stcs(&d4[i], p);  // written once, not read again: evict first
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[n % nslot]);
+            }
+            if (!ok) break;
         }
     }
+    if constexpr (SPLIT > 1) cluster_sync_all();  // no CTA leaves while the other may still write to it
 }
 
 constexpr int64_t kMaxChunk = 16384;       // floats per bulk copy, at most
@@ -849,6 +947,11 @@ constexpr size_t kRingBytes = 200 * 1024;   // target ring size (whole rows resi
 // (147 KB) ran at 0.98 of the HBM copy rate, 4 slots (one row, 196 KB) at 0.89.
 constexpr size_t kStreamRingBytes = 160 * 1024;
 constexpr size_t kMaxDynSmem = 226 * 1024;  // 227 KB per block, less room for static shared memory
+// Two-pass rows (see launch_tma).  On GB300, CE on 1024 x 152064 with the
+// row split over two CTAs: 48 KB chunks in four slots 239 us, 64 KB in three
+// 242 us, 64 KB in two (a 160 KB ring) 251 us, 32 KB in six 267 us.
+constexpr int64_t kMaxChunk2p = 12288;
+constexpr size_t kRing2p = 200 * 1024;
 // Two-input kernel (tma_rows2): chunks of at most 12288 floats.
 constexpr int64_t kMaxChunk2 = 12288;
 
@@ -893,17 +996,51 @@ bool launch_tma(const float* x, float* out, const int32_t* targets, float* aux, 
     if constexpr (OP == RowOp::kLse) {
         return false;
     } else {
-        // The row does not fit in shared memory: stream it twice through a
-        // ring of the logsumexp's size (the second pass reads the L2).  On
-        // GB300 (1024 rows of 152064 floats) 64 KB chunks in two slots ran
-        // at 277 us, 48 KB chunks in four slots at 297 us.
-        fit = int64_t(kStreamRingBytes) / (int64_t(chunk) * 4);
+        // The row does not fit in shared memory: stream it twice (the second
+        // pass reads the L2), each CTA of a cluster taking half of it, in
+        // chunks of at most kMaxChunk2p floats through a ring of about kRing2p.
+        const int64_t half = (cols + 1) / 2;
+        const int64_t per_half = (half + kMaxChunk2p - 1) / kMaxChunk2p;
+        const int chunk2 = int(((half + per_half - 1) / per_half + 3) / 4 * 4);
+        fit = int64_t(kRing2p) / (int64_t(chunk2) * 4);
         if (fit > 8) fit = 8;
         if (fit < 2) fit = 2;
         nslot = int(fit);
+        const int chunk = chunk2;
         smem = size_t(nslot) * chunk * sizeof(float) + 2 * size_t(nslot) * sizeof(uint64_t);
         if (smem > kMaxDynSmem) return false;
-        auto kern = tma_rows_2pass<OP>;
+        // Two CTAs per row in clusters of two, as many clusters as can be
+        // resident at once (one CTA per SM); one CTA per row if the device
+        // cannot place them.
+        auto kern2 = tma_rows_2pass<OP, 2>;
+        *err = cudaFuncSetAttribute(kern2, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (*err != cudaSuccess) return true;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2);
+        cfg.blockDim = dim3(kTmaThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, kern2, &cfg) != cudaSuccess) {
+            (void)cudaGetLastError();  // not fatal: fall back to one CTA per row
+            clusters = 0;
+        }
+        if (clusters > 0) {
+            const int64_t nclu = rows < clusters ? rows : clusters;
+            cfg.gridDim = dim3(unsigned(2 * nclu));
+            *err = cudaLaunchKernelEx(&cfg, kern2, x, out, targets, aux, rows, int(cols), chunk, nslot,
+                                      grad_scale);
+            if (*err == cudaSuccess) *err = cudaGetLastError();
+            return true;
+        }
+        auto kern = tma_rows_2pass<OP, 1>;
         *err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
         if (*err != cudaSuccess) return true;
         kern<<<unsigned(grid), kTmaThreads, smem, stream>>>(x, out, targets, aux, rows, int(cols), chunk, nslot,

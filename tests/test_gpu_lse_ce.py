@@ -133,7 +133,7 @@ def _at_offset(a: np.ndarray, off: int) -> torch.Tensor:
     return view
 
 
-@pytest.mark.parametrize("cols", [1025, 3001, 50257, 50258, 50259, 60001, 131072])
+@pytest.mark.parametrize("cols", [1025, 3001, 50257, 50258, 50259, 60001, 100003, 131072, 152064])
 @pytest.mark.parametrize("off", [0, 1, 3])
 def test_long_rows_not_on_16_byte_boundaries(ro, cols, off):
     # rows of cols % 4 != 0 (and buffers offset by `off` floats) start at every
