@@ -18,10 +18,13 @@
 // current row's gradient has been written from them.  HBM sees exactly one read
 // of every input element and one write of every output element.
 //
-// Two further kernels reuse the pipeline with two passes over each row, the
+// Further kernels reuse the pipeline with two passes over each row, the
 // second reading the row again from the L2: tma_rows_2pass (cross-entropy and
-// softmax rows too long to stay resident) and tma_rows2 (weighted-logits and
-// fixed-teacher cross-entropy, whose two input rows stream as chunk pairs).
+// softmax rows too long to stay resident, each row split over a cluster of two
+// CTAs), tma_rows2 (weighted-logits and fixed-teacher cross-entropy, whose two
+// input rows stream as chunk pairs) and tma_softmax_bwd (softmax backward on
+// long rows, (y, dy) chunk pairs).  ln_bwd_tma streams blocks of whole rows for
+// the LayerNorm backward.
 //
 // Rows need not start on a 16-byte boundary (cols % 4 != 0, or an offset
 // base): the row's first boundary splits off a head of h < 4 floats, the body
