@@ -41,6 +41,8 @@
 // raises an abort flag that all waits of the CTA watch, counts one timeout in
 // g_pipeline_timeouts and makes every thread leave; the producer first waits,
 // again bounded, for the copies it has in flight.
+#include <mutex>
+
 #include "common.cuh"
 #include "launch.h"
 #include "rowops.h"
@@ -1030,10 +1032,34 @@ bool launch_tma(const float* x, float* out, const int32_t* targets, float* aux, 
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
+        // Resident clusters for this shared-memory size, asked once per device
+        // and size (which also keeps the query out of stream captures after
+        // the first call, so captured and eager calls pick the same kernel).
         int clusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&clusters, kern2, &cfg) != cudaSuccess) {
-            (void)cudaGetLastError();  // not fatal: fall back to one CTA per row
-            clusters = 0;
+        {
+            static std::mutex mu;
+            static int64_t keys[16][2];
+            static int counts[16];
+            static int used = 0;
+            int dev = -1;
+            (void)cudaGetDevice(&dev);
+            std::lock_guard<std::mutex> lock(mu);
+            int i = 0;
+            while (i < used && !(keys[i][0] == dev && keys[i][1] == int64_t(smem))) ++i;
+            if (i < used) {
+                clusters = counts[i];
+            } else {
+                if (cudaOccupancyMaxActiveClusters(&clusters, kern2, &cfg) != cudaSuccess) {
+                    (void)cudaGetLastError();  // not fatal: fall back to one CTA per row
+                    clusters = 0;
+                }
+                if (used < 16) {
+                    keys[used][0] = dev;
+                    keys[used][1] = int64_t(smem);
+                    counts[used] = clusters;
+                    ++used;
+                }
+            }
         }
         if (clusters > 0) {
             const int64_t nclu = rows < clusters ? rows : clusters;

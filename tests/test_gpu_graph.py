@@ -3,8 +3,9 @@ bits as the same calls made eagerly.
 
 Every entry point only enqueues kernels on the stream it is given (no
 allocation, no synchronisation), so a whole step of calls can be captured
-once and replayed; this covers the group, cluster, bulk-copy pipeline and
-programmatic-dependent (two-kernel) paths."""
+once and replayed; this covers the group, cluster, bulk-copy pipeline
+(including rows split over a cluster of CTAs) and programmatic-dependent
+(two-kernel) paths."""
 import numpy as np
 import pytest
 import torch
@@ -34,6 +35,12 @@ class Step:
         self.cx, self.ct, self.cgs = gpu(c["logits"]), gpu(c["targets"]), c["grad_scale"]
         r = inputs.router(seed, rows=5000, cols=64)
         self.rx, self.rm, self.k = gpu(r["x"]), gpu(r["mask"]), r["k"]
+        # rows for the cluster kernels: a vocabulary row split over a cluster,
+        # and the long-row softmax backward
+        v = inputs.cross_entropy(seed + 7, rows=6, cols=152064)
+        self.vx, self.vt, self.vgs = gpu(v["logits"]), gpu(v["targets"]), v["grad_scale"]
+        w = inputs.softmax_pair(seed + 9, rows=5, cols=40000)
+        self.wy, self.wdy = gpu(w["x"]).softmax(dim=1), gpu(w["dy"])
         e = torch.empty_like
         self.out = {
             "sy": e(self.sx), "sdx": e(self.sx),
@@ -46,6 +53,8 @@ class Step:
             "tv": torch.empty((5000, self.k), device="cuda"), "ti": torch.empty((5000, self.k), device="cuda"),
             "rms": e(self.lx), "rmsr": torch.empty(300, device="cuda"), "rmsdx": e(self.lx), "rmst": e(self.lx),
             "rmsdg": e(self.lg),
+            "vg": e(self.vx), "vrl": torch.empty(6, device="cuda"),
+            "vml": torch.empty(1, dtype=torch.float64, device="cuda"), "vy": e(self.vx), "wdx": e(self.wy),
         }
 
     def run(self):
@@ -66,6 +75,9 @@ class Step:
         ro.rowops_rmsnorm_fwd(self.lx, self.lg, o["rms"], o["rmsr"], eps=self.eps)
         ro.rowops_rmsnorm_bwd(self.ldy, self.lg, self.lx, o["rmsr"], o["rmsdx"], o["rmst"])
         ro.rowops_column_sums(o["rmst"], o["rmsdg"])
+        ro.rowops_softmax_ce(self.vx, self.vt, o["vg"], o["vrl"], o["vml"], grad_scale=self.vgs)
+        ro.rowops_softmax_fwd(self.vx, o["vy"])
+        ro.rowops_softmax_bwd(self.wy, self.wdy, o["wdx"])
 
     def snapshot(self):
         torch.cuda.synchronize()
@@ -99,7 +111,7 @@ def test_step_graph_replay_matches_eager(ro):
     _same(eager, step.snapshot())
     # New input values in the same buffers: the replay follows them.
     other = Step(ro, 1)
-    for name in ("sx", "sdy", "lx", "lg", "lb", "ldy", "as_", "adp", "cx", "ct", "rx", "rm"):
+    for name in ("sx", "sdy", "lx", "lg", "lb", "ldy", "as_", "adp", "cx", "ct", "rx", "rm", "vx", "vt", "wy", "wdy"):
         getattr(step, name).copy_(getattr(other, name))
     other.run()
     g.replay()
