@@ -324,7 +324,7 @@ def peaks():
 # Sources each recorded kernel is compiled from (its kernels, their launchers
 # and the shared device helpers); a change to any of them voids the record.
 KERNEL_SOURCES = {
-    "softmax_ce": ("common.cuh", "tma_rows.cu"),  # the kernel's device code
+    "softmax_ce": ("common.cuh", "pipeline.cuh", "tma_rows.cu"),  # the kernel's device code
 }
 
 

@@ -109,6 +109,11 @@ bool launch_soft_ce_tma(const float* x, const float* w, float* grad, float* row_
                         float grad_scale, cudaStream_t stream, cudaError_t* err);
 bool launch_teacher_ce_tma(const float* s, const float* t, float* grad, float* row_loss, int64_t rows,
                            int64_t cols, float grad_scale, cudaStream_t stream, cudaError_t* err);
+// Timeouts counted by the bounded waits of each bulk-copy translation unit
+// (rowops_pipeline_timeouts adds them up).
+uint32_t pipeline_timeouts_rows();
+uint32_t pipeline_timeouts_pairs();
+uint32_t pipeline_timeouts_ln();
 // LayerNorm backward stage 1 on rows of 384..1024 floats on 16-byte
 // boundaries (one CTA per SM, row blocks through the bulk-copy ring); writes
 // ln_bwd_tma_ctas(rows, cols) partials to ws.  ln_bwd_tma_ctas is 0 for
