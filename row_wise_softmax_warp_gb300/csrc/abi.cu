@@ -228,7 +228,8 @@ int rowops_layernorm_bwd(const float* dy, const float* gamma, const float* xhat,
     if (cols == 0) return ROWOPS_ERR_SHAPE;
     if (rows == 0) return ROWOPS_OK;
     if (!dy || !gamma || !xhat || !inv_std || !dx || !dgamma || !dbeta) return ROWOPS_ERR_NULL;
-    if (!elems_aligned({{dy, 4}, {gamma, 4}, {xhat, 4}, {inv_std, 4}, {dx, 4}, {dgamma, 4}, {dbeta, 4}})) return ROWOPS_ERR_ALIGN;
+    if (!elems_aligned({{dy, 4}, {gamma, 4}, {xhat, 4}, {inv_std, 4}, {dx, 4}, {dgamma, 4}, {dbeta, 4}}))
+        return ROWOPS_ERR_ALIGN;
     const size_t need = rowops::layernorm_bwd_workspace(rows, cols);
     if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return ROWOPS_ERR_WORKSPACE;
     const int64_t n = rows * cols * 4;

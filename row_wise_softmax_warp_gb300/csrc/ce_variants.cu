@@ -240,7 +240,8 @@ ce2_stream(const float* __restrict__ x, const float* __restrict__ w, float* __re
         // (max, sum) pairs of the block: warp butterfly, then warps in order.
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
-            const MaxSum ta = ms_merge({ma, sa}, {__shfl_xor_sync(kFullMask, ma, o), __shfl_xor_sync(kFullMask, sa, o)});
+            const MaxSum ta =
+                ms_merge({ma, sa}, {__shfl_xor_sync(kFullMask, ma, o), __shfl_xor_sync(kFullMask, sa, o)});
             ma = ta.m;
             sa = ta.s;
             if constexpr (TEACHER) {

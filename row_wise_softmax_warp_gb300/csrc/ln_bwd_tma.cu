@@ -23,8 +23,10 @@ namespace {
 // rows), so the slots warp w touches are w / slot_rows + j * period and it
 // waits on every use of each of them, in order: a parity wait never meets a
 // phase two uses old.  (Making every warp visit every slot instead measured
-// slower on GB300: 4096 x 768, 22.1 us against 18.1.)  A row is swept twice in shared memory (the sums of g' and
-// g'*xhat, then dx), and dx goes straight to global memory.  When the rows are
+// slower on GB300: 4096 x 768, 22.1 us against 18.1.)  A row is swept twice
+// in shared memory (the sums of g' and g'*xhat, then dx), and dx goes
+// straight to global memory; inv_std is loaded at the top of each row
+// (loading it one row ahead measured slower).  When the rows are
 // done, the 16 warps add their partials in warp order through shared memory
 // (the ring, free by then) and the CTA writes its partial to workspace slot
 // blockIdx.x; ln_params_reduce adds the slots in order.  HBM sees one read of
@@ -226,7 +228,8 @@ bool launch_ln_bwd_tma(const float* dy, const float* gamma, const float* xhat, c
     nslot -= nslot % period;
     // The ring also holds the 16 warps' partials at the end.
     if (nslot < 2 || size_t(nslot) * slot_bytes < size_t(kConsumerWarps) * 8 * size_t(cols)) return false;
-    const size_t smem = size_t(nslot) * slot_bytes + size_t(cols) * sizeof(float) + 2 * size_t(nslot) * sizeof(uint64_t);
+    const size_t smem =
+        size_t(nslot) * slot_bytes + size_t(cols) * sizeof(float) + 2 * size_t(nslot) * sizeof(uint64_t);
     if (smem > kMaxDynSmem) return false;
     const int64_t per_cta = (rows + grid - 1) / grid;
     auto launch = [&](auto kern) {
