@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import oracle
-from parity_util import check_abs, check_rel, gpu, host
+from parity_util import check_abs, check_bound, check_rel, gpu, host, softmax_bwd_bound
 from row_wise_softmax_warp_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
@@ -161,4 +161,34 @@ def test_long_rows_not_on_16_byte_boundaries(ro, cols, off):
     check_abs(host(y)[idx], ref, 2e-6, "softmax")
     ro.rowops_softmax_fwd(xg, xg)  # in place
     check_abs(host(xg)[idx], ref, 2e-6, "softmax in place")
+    assert ro.library().rowops_pipeline_timeouts() == 0
+
+
+@pytest.mark.parametrize("cols,off", [(1000003, 0), (1000003, 1), (2 ** 20, 0)])
+def test_very_long_rows(ro, cols, off):
+    # rows of a million floats: dozens of chunks per pass in the two-pass
+    # kernels (each CTA of a cluster taking half a row), the streaming
+    # logsumexp and the two-input softmax backward
+    rows = 3
+    c = inputs.cross_entropy(cols + off, rows=rows, cols=cols, outlier_frac=1e-4)
+    x, t = c["logits"], c["targets"]
+    t[0] = cols - 1
+    xg = _at_offset(x, off)
+    check_rel(host(ro.rowops_logsumexp(xg)), oracle.logsumexp_rows(x), f"lse {rows}x{cols}+{off}")
+    g = _at_offset(np.zeros_like(x), off)
+    rl = torch.empty(rows, device="cuda")
+    ml = torch.empty(1, dtype=torch.float64, device="cuda")
+    ro.rowops_softmax_ce(xg, gpu(t), g, rl, ml, grad_scale=c["grad_scale"])
+    gr, rlr, mlr = oracle.softmax_cross_entropy(x, t, c["grad_scale"])
+    check_abs(host(g), gr, 2e-6 * c["grad_scale"], "ce grad")
+    check_rel(host(rl), rlr, "ce row loss")
+    ref = oracle.softmax_rows(x)
+    y = _at_offset(np.zeros_like(x), off)
+    ro.rowops_softmax_fwd(xg, y)
+    check_abs(host(y), ref, 2e-6, "softmax")
+    y32 = ref.astype(np.float32)
+    dy = np.random.default_rng(cols).normal(0, 1, x.shape).astype(np.float32)
+    dx = _at_offset(np.zeros_like(x), off)
+    ro.rowops_softmax_bwd(_at_offset(y32, off), _at_offset(dy, off), dx)
+    check_bound(host(dx), oracle.softmax_rows_backward(y32, dy), softmax_bwd_bound(y32, dy), "softmax bwd")
     assert ro.library().rowops_pipeline_timeouts() == 0
