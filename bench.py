@@ -799,11 +799,14 @@ def reference_leg(args):
     import oracle
     oracle.build()
     data = make_inputs()
+    # Per-step sample budget, smaller for long runs so that --steps K --warmup W
+    # stays within a few minutes of CPU work.
+    budget = min(args.ref_step_seconds, 120.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
-        cpu_leg(data, budget_s=1.0)
+        cpu_leg(data, budget_s=min(1.0, budget))
     vals, secs, last = [], 0.0, None
     for _ in range(args.steps):
-        last = cpu_leg(data, budget_s=args.ref_step_seconds)
+        last = cpu_leg(data, budget_s=budget)
         vals.append(last["value"])
         secs += last["seconds"]
     value = statistics.mean(vals)
