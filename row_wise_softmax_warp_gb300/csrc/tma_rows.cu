@@ -26,9 +26,9 @@
 // base): the row's first boundary splits off a head of h < 4 floats, the body
 // (a multiple of 4 floats) goes through the bulk copies, and the tail of
 // t < 4 floats after it is read with plain loads by consumer lanes, which also
-// write the head and tail outputs.  The output row must have the same
-// alignment modulo 16 bytes as the input row, so that the body's stores stay
-// 128-bit.
+// write the head and tail outputs.  An output row with the input row's
+// alignment modulo 16 bytes takes 128-bit stores; one on another phase takes
+// scalar stores (the same kernels, built for either).
 //
 // exp(x - m) is evaluated as 2^((x - m)*log2(e)) with the ex2.approx
 // instruction.
@@ -43,7 +43,33 @@ namespace {
 
 enum class RowOp { kLse, kCe, kSoftmax };
 
-template <RowOp OP>
+// Output float4 i of a chunk whose first float is dk: one 128-bit store when
+// the output row shares the input row's 16-byte phase (VEC), else four.
+template <bool VEC>
+__device__ __forceinline__ void store4(float* dk, int i, const float4 p) {
+    if constexpr (VEC) {
+        reinterpret_cast<float4*>(dk)[i] = p;
+    } else {
+        dk[4 * i] = p.x;
+        dk[4 * i + 1] = p.y;
+        dk[4 * i + 2] = p.z;
+        dk[4 * i + 3] = p.w;
+    }
+}
+// The same with streaming (evict-first) stores.
+template <bool VEC>
+__device__ __forceinline__ void store4_cs(float* dk, int i, const float4 p) {
+    if constexpr (VEC) {
+        __stcs(reinterpret_cast<float4*>(dk) + i, p);
+    } else {
+        __stcs(dk + 4 * i, p.x);
+        __stcs(dk + 4 * i + 1, p.y);
+        __stcs(dk + 4 * i + 2, p.z);
+        __stcs(dk + 4 * i + 3, p.w);
+    }
+}
+
+template <RowOp OP, bool OUT_VEC>
 __global__ void __launch_bounds__(kTmaThreads, 1)
 tma_rows(const float* x, float* out, const int32_t* __restrict__ targets, float* __restrict__ aux,
          int64_t rows, int cols, int chunk, int nslot, float grad_scale) {
@@ -193,7 +219,7 @@ tma_rows(const float* x, float* out, const int32_t* __restrict__ targets, float*
                 const int slot = int((n + k) % nslot);
                 const int cnt4 = min(chunk, body - k * chunk) >> 2;
                 const float4* c4 = reinterpret_cast<const float4*>(buf + size_t(slot) * chunk);
-                float4* d4 = reinterpret_cast<float4*>(dst + size_t(k) * chunk);
+                float* dk = dst + size_t(k) * chunk;
                 for (int i = ct; i < cnt4; i += kConsumers) {
                     const float4 v = c4[i];
                     float4 p;
@@ -208,7 +234,7 @@ tma_rows(const float* x, float* out, const int32_t* __restrict__ targets, float*
                         p.z = grad_scale * (p.z - (j + 2 == t ? 1.f : 0.f));
                         p.w = grad_scale * (p.w - (j + 3 == t ? 1.f : 0.f));
                     }
-                    d4[i] = p;
+                    store4<OUT_VEC>(dk, i, p);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[slot]);
@@ -234,7 +260,7 @@ tma_rows(const float* x, float* out, const int32_t* __restrict__ targets, float*
 // place: every chunk of pass 1 is copied into shared memory before the
 // consumers overwrite it in global memory, and pass 0 of the row is over (in
 // both CTAs) before pass 1 writes anything.
-template <RowOp OP, int SPLIT>
+template <RowOp OP, int SPLIT, bool OUT_VEC>
 __global__ void __launch_bounds__(kTmaThreads, 1)
 tma_rows_2pass(const float* x, float* out, const int32_t* __restrict__ targets, float* __restrict__ aux,
                int64_t rows, int cols, int chunk, int nslot, float grad_scale) {
@@ -407,7 +433,7 @@ tma_rows_2pass(const float* x, float* out, const int32_t* __restrict__ targets, 
                 }
                 const int cnt4 = min(chunk, len - k * chunk) >> 2;
                 const float4* c4 = reinterpret_cast<const float4*>(buf + size_t(n % nslot) * chunk);
-                float4* d4 = reinterpret_cast<float4*>(dst + head + lo + size_t(k) * chunk);
+                float* dk = dst + head + lo + size_t(k) * chunk;
                 for (int i = ct; i < cnt4; i += kConsumers) {
                     const float4 v = c4[i];
                     float4 p;
@@ -422,7 +448,7 @@ tma_rows_2pass(const float* x, float* out, const int32_t* __restrict__ targets, 
                         p.z = grad_scale * (p.z - (j + 2 == t ? 1.f : 0.f));
                         p.w = grad_scale * (p.w - (j + 3 == t ? 1.f : 0.f));
                     }
-                    __stcs(&d4[i], p);  // written once, not read again: evict first
+                    store4_cs<OUT_VEC>(dk, i, p);  // written once, not read again: evict first
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[n % nslot]);
@@ -444,15 +470,11 @@ constexpr size_t kStreamRingBytes = 160 * 1024;
 constexpr int64_t kMaxChunk2p = 12288;
 constexpr size_t kRing2p = 200 * 1024;
 
-template <RowOp OP>
-bool launch_tma(const float* x, float* out, const int32_t* targets, float* aux, int64_t rows,
-                int64_t cols, float grad_scale, cudaStream_t stream, cudaError_t* err) {
-    // Long rows only; 4-byte aligned buffers; for the ops that write rows, the
-    // output row has the input row's alignment modulo 16 bytes.
-    if (cols < 1024 || cols > INT32_MAX / 2) return false;
-    const uintptr_t xa = reinterpret_cast<uintptr_t>(x);
-    if ((xa & 3) != 0) return false;
-    if (OP != RowOp::kLse && ((reinterpret_cast<uintptr_t>(out) & 15) != (xa & 15))) return false;
+// OUT_VEC: the output rows share the input rows' 16-byte phase (128-bit
+// stores); otherwise the kernels write them with scalar stores.
+template <RowOp OP, bool OUT_VEC>
+bool launch_tma_v(const float* x, float* out, const int32_t* targets, float* aux, int64_t rows,
+                  int64_t cols, float grad_scale, cudaStream_t stream, cudaError_t* err) {
     // A row is cut into equal chunks of at most kMaxChunk floats: every chunk
     // costs the pipeline a fixed ~0.5 us per SM, so chunks are kept large (on
     // GB300, 16 KB chunks left logsumexp at 0.70 of the HBM copy rate, 48-64 KB
@@ -474,7 +496,7 @@ bool launch_tma(const float* x, float* out, const int32_t* targets, float* aux, 
     if (sms <= 0) return false;
     const int64_t grid = rows < sms ? rows : sms;
     if (smem <= kMaxDynSmem && nslot <= kMaxSlots) {
-        auto kern = tma_rows<OP>;
+        auto kern = tma_rows<OP, OUT_VEC>;
         *err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
         if (*err != cudaSuccess) return true;
         kern<<<unsigned(grid), kTmaThreads, smem, stream>>>(x, out, targets, aux, rows, int(cols), chunk, nslot,
@@ -501,7 +523,7 @@ bool launch_tma(const float* x, float* out, const int32_t* targets, float* aux, 
         // Two CTAs per row in clusters of two, as many clusters as can be
         // resident at once (one CTA per SM); one CTA per row if the device
         // cannot place them.
-        auto kern2 = tma_rows_2pass<OP, 2>;
+        auto kern2 = tma_rows_2pass<OP, 2, OUT_VEC>;
         *err = cudaFuncSetAttribute(kern2, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
         if (*err != cudaSuccess) return true;
         cudaLaunchConfig_t cfg = {};
@@ -553,13 +575,29 @@ bool launch_tma(const float* x, float* out, const int32_t* targets, float* aux, 
             if (*err == cudaSuccess) *err = cudaGetLastError();
             return true;
         }
-        auto kern = tma_rows_2pass<OP, 1>;
+        auto kern = tma_rows_2pass<OP, 1, OUT_VEC>;
         *err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
         if (*err != cudaSuccess) return true;
         kern<<<unsigned(grid), kTmaThreads, smem, stream>>>(x, out, targets, aux, rows, int(cols), chunk, nslot,
                                                              grad_scale);
         *err = cudaGetLastError();
         return true;
+    }
+}
+
+// Long rows only, 4-byte aligned buffers.
+template <RowOp OP>
+bool launch_tma(const float* x, float* out, const int32_t* targets, float* aux, int64_t rows,
+                int64_t cols, float grad_scale, cudaStream_t stream, cudaError_t* err) {
+    if (cols < 1024 || cols > INT32_MAX / 2) return false;
+    const uintptr_t xa = reinterpret_cast<uintptr_t>(x);
+    if ((xa & 3) != 0) return false;
+    if constexpr (OP == RowOp::kLse) {
+        return launch_tma_v<OP, true>(x, out, targets, aux, rows, cols, grad_scale, stream, err);
+    } else {
+        if ((reinterpret_cast<uintptr_t>(out) & 15) == (xa & 15))
+            return launch_tma_v<OP, true>(x, out, targets, aux, rows, cols, grad_scale, stream, err);
+        return launch_tma_v<OP, false>(x, out, targets, aux, rows, cols, grad_scale, stream, err);
     }
 }
 

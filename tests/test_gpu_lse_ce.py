@@ -192,3 +192,26 @@ def test_very_long_rows(ro, cols, off):
     ro.rowops_softmax_bwd(_at_offset(y32, off), _at_offset(dy, off), dx)
     check_bound(host(dx), oracle.softmax_rows_backward(y32, dy), softmax_bwd_bound(y32, dy), "softmax bwd")
     assert ro.library().rowops_pipeline_timeouts() == 0
+
+
+@pytest.mark.parametrize("cols", [50304, 60001, 152064])
+@pytest.mark.parametrize("offs", [(0, 1), (1, 0), (2, 3)])
+def test_long_rows_output_on_another_phase(ro, cols, offs):
+    # logits and gradient (or probabilities) on different 16-byte phases: the
+    # bulk-copy kernels write the output rows with scalar stores
+    rows = 200
+    c = inputs.cross_entropy(cols + 3 * offs[0] + offs[1], rows=rows, cols=cols, outlier_frac=1e-3)
+    x, t = c["logits"], c["targets"]
+    xg = _at_offset(x, offs[0])
+    g = _at_offset(np.zeros_like(x), offs[1])
+    rl = torch.empty(rows, device="cuda")
+    ml = torch.empty(1, dtype=torch.float64, device="cuda")
+    ro.rowops_softmax_ce(xg, gpu(t), g, rl, ml, grad_scale=c["grad_scale"])
+    gr, rlr, mlr = oracle.softmax_cross_entropy(x, t, c["grad_scale"])
+    check_abs(host(g), gr, 2e-6 * c["grad_scale"], "ce grad")
+    check_rel(host(rl), rlr, "ce row loss")
+    check_rel(host(ml), [mlr], "ce mean loss")
+    y = _at_offset(np.zeros_like(x), offs[1])
+    ro.rowops_softmax_fwd(xg, y)
+    check_abs(host(y), oracle.softmax_rows(x), 2e-6, "softmax")
+    assert ro.library().rowops_pipeline_timeouts() == 0
