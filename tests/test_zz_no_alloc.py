@@ -58,3 +58,13 @@ def test_noalloc_refuses_oversize_and_keeps_common_checks(ro):
                                             4096, 4096, None) == 4  # ROWOPS_ERR_WORKSPACE
     assert lib.rowops_layernorm_bwd_noalloc(None, None, None, None, None, None, None, 0, 768, None) == 0
     assert lib.rowops_layernorm_bwd_noalloc(None, None, None, None, None, None, None, 8, 768, None) == 1
+
+
+def test_noalloc_fits_every_row_count_up_to_1024_columns(ro):
+    # The header's promise: with cols <= 1024 the partial sums of any row
+    # count fit the library's 1 MiB array (on the current device's SM count).
+    lib = binding.library()
+    cap = lib.rowops_layernorm_bwd_noalloc_max_bytes()
+    for cols in (1, 64, 383, 384, 512, 768, 1000, 1023, 1024):
+        for rows in (1, 151, 152, 4096, 65536, 10 ** 7):
+            assert lib.rowops_layernorm_bwd_workspace(rows, cols) <= cap, (rows, cols)
