@@ -321,36 +321,59 @@ def peaks():
     return 6800.0, "fallback"
 
 
-# Sources each recorded kernel is compiled from (its kernels, their launchers
-# and the shared device helpers); a change to any of them voids the record.
-KERNEL_SOURCES = {
-    "softmax_ce": ("common.cuh", "pipeline.cuh", "tma_rows.cu"),  # the kernel's device code
-}
+TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "dram_traffic.json")
 
 
-def kernel_fingerprint(op="softmax_ce"):
+def _traffic_records():
+    if not os.path.exists(TRAFFIC_RECORD):
+        return {}
+    with open(TRAFFIC_RECORD) as f:
+        return json.load(f)
+
+
+def kernel_fingerprint(sources):
+    """First 16 hex digits of the SHA-256 of the named csrc files (sorted by name)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "row_wise_softmax_warp_gb300", "csrc")
-    for name in sorted(KERNEL_SOURCES[op]):
+    for name in sorted(sources):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(op):
-    """DRAM bytes per launch from the committed ncu summary (profiles/tma_rows_ce_8192x50304_dram.md),
-    if it was taken on the current kernel sources; else None."""
-    p = os.path.join(ROOT, "profiles", "tma_rows_ce_8192x50304_dram.md")
-    if not os.path.exists(p):
-        return None
-    if op not in KERNEL_SOURCES:
-        return None
-    fp = kernel_fingerprint(op)
-    for line in open(p):
-        cells = [c.strip() for c in line.strip().strip("|").split("|")]
-        if len(cells) == 3 and cells[0] == op and cells[1].isdigit():
-            return int(cells[1]) if cells[2] == fp else None
-    return None
+    """(DRAM read + write bytes per launch, the record) from the committed ncu
+    record profiles/dram_traffic.json, if it was taken on the current sources
+    of the op's kernel; else (None, the record or None)."""
+    rec = _traffic_records().get(op)
+    if not rec:
+        return None, None
+    if kernel_fingerprint(rec["sources"]) != rec["kernel_fingerprint"]:
+        return None, rec
+    return int(rec["per_launch_bytes"]), rec
+
+
+def link_rates(dev, nbytes, reps=3):
+    """Pinned host <-> device copy rates (GB/s) of one plain copy_ of nbytes
+    (capped at 1 GiB), best of reps, CUDA events on the current stream."""
+    import torch
+    n = int(min(nbytes, 1 << 30))
+    host = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+    devb = torch.empty(n, dtype=torch.uint8, device=dev)
+    out = {}
+    for name, dst, src in (("h2d", devb, host), ("d2h", host, devb)):
+        best = None
+        for _ in range(reps + 1):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            dst.copy_(src, non_blocking=True)
+            b.record()
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(b)
+            best = ms if best is None else min(best, ms)
+        out[name] = n / (best * 1e-3) / 1e9
+    del host, devb
+    return out, n
 
 
 def dist_setup():
@@ -625,6 +648,9 @@ def gpu_leg(args):
     ops2 = Ops(data, dev)
     e2e_ms_local, h2d, d2h = e2e_step_inputs(ops2, dev, stream, ke, dist)
     all_ms_local, all_h2d, all_d2h = e2e_every_buffer(ops2, dev, stream, ke, dist)
+    del ops2
+    torch.cuda.empty_cache()
+    link, link_n = link_rates(dev, h2d)
     clocks.mark = False
     clocks.stop()
 
@@ -650,6 +676,22 @@ def gpu_leg(args):
                         "alg_bytes": b}
     top = max(per_op, key=per_op.get)
     top_gbs = abytes[top][0] / (per_op[top] * 1e-3) / 1e9
+    traffic, rec = recorded_traffic(top)
+    roofline = {"bound": "hbm", "kernel": top, "achieved": round(top_gbs, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(top_gbs / peak, 4), "peak_kind": peak_kind, "traffic": traffic,
+                "traffic_source": "profiles/dram_traffic.json (ncu dram__bytes_read.sum + dram__bytes_write.sum)"
+                if rec else None}
+    if rec and traffic is None:
+        roofline["traffic_note"] = "null: the kernel's sources changed since the recorded capture"
+    if rec:
+        unwritten = rec["algorithmic_bytes"] - rec["per_launch_bytes"]
+        if unwritten > 0:
+            roofline["traffic_note"] = (
+                f"the capture's DRAM writes fall {unwritten / 1e6:.0f} MB short of the algorithmic bytes: that much "
+                "output is still dirty in the L2 when the isolated launch ends and is written back after its "
+                "events; the back-to-back fraction pays for it")
+    if top in b2b_ms:
+        roofline["frac_back_to_back"] = round(abytes[top][0] / (b2b_ms[top] * 1e-3) / 1e9 / peak, 4)
     line = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -665,9 +707,7 @@ def gpu_leg(args):
         "data": "synthetic (seeded numpy PCG64, the five workloads' distributions)",
         "config": {"workload": WORKLOAD, "l2": "flushed before every op (512 MiB device write), outside the op's events",
                    "ms_per_step_incl_flushes": round(wall_ms, 4), "parallelism": f"replicas x{world} (rows independent)"},
-        "roofline": {"bound": "hbm", "kernel": top, "achieved": round(top_gbs, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(top_gbs / peak, 4), "peak_kind": peak_kind,
-                     "traffic": recorded_traffic(top)},
+        "roofline": roofline,
         "ops": breakdown,
         "gpu_launches": int(launches),
         "next_ops": {n: {"ms": round(next_ms[n], 5), "alg_bytes": next_bytes()[n][0],
@@ -679,11 +719,16 @@ def gpu_leg(args):
                 "ms_per_step": round(e2e_ms, 3), "steps": ke,
                 "note": "each step uploads the step's inputs (each once), keeps the intermediates on the "
                         "device (softmax y, LayerNorm xhat/inv_std, attention P, router P) and reads back "
-                        "the mean cross-entropy loss"},
+                        "the mean cross-entropy loss",
+                **link_share(h2d, d2h, e2e_ms, link)},
+        "host_link": {"h2d_GB/s": round(link["h2d"], 1), "d2h_GB/s": round(link["d2h"], 1), "bytes": link_n,
+                      "note": "one plain pinned copy_ each way (best of 3); link_ms below is the step's copies "
+                              "at these rates, frac_of_link = link_ms / ms_per_step"},
         "e2e_every_buffer": {"value": round(world * total_bytes / (all_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                              "h2d_bytes_per_step": int(all_h2d), "d2h_bytes_per_step": int(all_d2h),
                              "ms_per_step": round(all_ms, 3), "steps": ke,
-                             "note": "every op's inputs uploaded and every output read back, per op"},
+                             "note": "every op's inputs uploaded and every output read back, per op",
+                             **link_share(all_h2d, all_d2h, all_ms, link)},
         "clocks": clocks.summary(),
     }
     if graph_step is not None and "ms" in graph_step:
@@ -713,6 +758,12 @@ def gpu_leg(args):
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def link_share(h2d, d2h, ms, link):
+    """The time a step's copies take at the measured link rates, and its share of the step."""
+    link_ms = (h2d / link["h2d"] + d2h / link["d2h"]) / 1e6
+    return {"link_ms": round(link_ms, 3), "frac_of_link": round(link_ms / ms, 4)}
 
 
 # ----------------------------------------------------------------- CPU leg

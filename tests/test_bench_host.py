@@ -66,3 +66,23 @@ def test_reference_arm_only_rank0_prints():
 
 def test_max_over_ranks_single_process_is_identity():
     assert bench.max_over_ranks(3.0, None, torch.device("cpu")) == 3.0
+
+
+def test_recorded_traffic_follows_the_kernel_sources(tmp_path, monkeypatch):
+    # The committed record is reported while the kernel's sources hash to its
+    # fingerprint, and is withheld (None) once any of them changes.
+    traffic, rec = bench.recorded_traffic("softmax_ce")
+    assert rec is not None and set(rec["sources"]) == {"common.cuh", "pipeline.cuh", "tma_rows.cu"}
+    fp_now = bench.kernel_fingerprint(rec["sources"])
+    assert (traffic == rec["per_launch_bytes"]) == (fp_now == rec["kernel_fingerprint"])
+    stale = dict(rec, kernel_fingerprint="0" * 16)
+    p = tmp_path / "dram_traffic.json"
+    p.write_text(__import__("json").dumps({"softmax_ce": stale}))
+    monkeypatch.setattr(bench, "TRAFFIC_RECORD", str(p))
+    assert bench.recorded_traffic("softmax_ce") == (None, stale)
+    assert bench.recorded_traffic("logsumexp") == (None, None)
+
+
+def test_link_share():
+    got = bench.link_share(2e9, 8, 20.0, {"h2d": 200.0, "d2h": 100.0})
+    assert got["link_ms"] == 10.0 and got["frac_of_link"] == 0.5
