@@ -187,13 +187,18 @@ size_t rowops_layernorm_bwd_workspace(int64_t rows, int64_t cols);
  * column sums are deterministic: fixed blocks of rows write partial sums into
  * `workspace` (at least rowops_layernorm_bwd_workspace(rows, cols) bytes of
  * 16-byte aligned device memory; its contents need not be initialised and are
- * garbage afterwards), then a second kernel adds the partials in a fixed order.
- * The workspace size depends on rows, cols and the current device's SM count
- * (the partials are per cluster or per CTA of a grid sized to one wave);
- * query it with the device current that will run the call.
- * Concurrent calls need separate workspaces.  cols == 0 is ROWOPS_ERR_SHAPE; a
- * short, NULL or misaligned workspace is ROWOPS_ERR_WORKSPACE.  No output may
- * overlap another buffer.
+ * garbage afterwards), then a second kernel, a programmatic dependent of the
+ * first, adds the partials in a fixed order.  The workspace size depends on
+ * rows, cols and the current device's SM count (the partials are per CTA or
+ * per cluster of a grid sized to one wave); query it with the device current
+ * that will run the call.  Concurrent calls need separate workspaces.
+ * cols == 0 is ROWOPS_ERR_SHAPE; a short, NULL or misaligned workspace is
+ * ROWOPS_ERR_WORKSPACE.  No output may overlap another buffer.  Rows of
+ * 384..1024 floats whose CTA blocks are too large for shared memory stream
+ * through a bulk-copy ring whose waits are bounded: a wait that runs out (a
+ * defect) leaves dx, dgamma and dbeta incomplete and counts one timeout, so
+ * callers that must know check rowops_pipeline_timeouts() after
+ * synchronizing.
  */
 int rowops_layernorm_bwd(const float *dy, const float *gamma, const float *xhat,
                          const float *inv_std, float *dx, float *dgamma, float *dbeta,
@@ -209,24 +214,35 @@ int rowops_layernorm_bwd(const float *dy, const float *gamma, const float *xhat,
  * host framework owns every allocation and offers no scratch space, or code
  * that must not enter an allocator at all (inside an allocator's own
  * out-of-memory path, for instance).  For them this entry point computes
- * exactly what rowops_layernorm_bwd computes, with the same argument rules,
- * using a workspace that lives inside the library: a fixed array of
+ * what rowops_layernorm_bwd computes (bit for bit wherever both run the same
+ * CTA count; see below), with the same argument rules, using a workspace that
+ * lives inside the library: a fixed array of
  * rowops_layernorm_bwd_noalloc_max_bytes() bytes (1 MiB) of device memory,
  * which every GPU that loads the library holds until the process exits.
  *
  *   - The first call on each device looks up that array's device address
  *     (with the device current); make that first call before any stream
- *     capture.  Later calls reuse the address.
- *   - Shapes whose workspace, rowops_layernorm_bwd_workspace(rows, cols), is
- *     larger than the array are refused with ROWOPS_ERR_WORKSPACE.  With
- *     cols <= 1024 every row count fits; wider rows fit while rows is small
- *     enough.
+ *     capture.  Later calls reuse the address for the life of the process, so
+ *     a device reset (cudaDeviceReset) after the first call on that device is
+ *     not supported.
+ *   - Errors are reported in this order: the argument checks of
+ *     rowops_layernorm_bwd (shape, NULL, alignment, overlap), then the size
+ *     check below, then a failed address lookup (ROWOPS_ERR_CUDA).
+ *   - Each CTA's partial sums take 8 * cols bytes.  Rows of up to 1024 floats
+ *     fit for every row count: the launch uses only as many CTAs as the array
+ *     holds partials for (rows of 863..1024 floats then run on fewer CTAs
+ *     than rowops_layernorm_bwd uses, so dgamma and dbeta are added in another
+ *     order; dx is the same).  Wider rows fit while rows is small enough
+ *     (e.g. 64 rows of 2048 floats, 8 rows of 16384); larger shapes are
+ *     refused with ROWOPS_ERR_WORKSPACE.
  *   - All calls on a device share the one array, and it keeps the contents of
  *     the last call.  Nothing in it needs to start at zero: each call writes
  *     every partial sum it later reads.  Calls that can overlap on the GPU
  *     (different streams, no ordering between them) race on the array and may
  *     return wrong dgamma/dbeta; order them, or use rowops_layernorm_bwd with
  *     separate workspaces.
+ *   - Bounded waits that run out are counted as for rowops_layernorm_bwd:
+ *     check rowops_pipeline_timeouts() after synchronizing.
  *   - It never calls cudaMalloc, cudaFree or any other allocating routine.
  */
 int rowops_layernorm_bwd_noalloc(const float *dy, const float *gamma, const float *xhat,

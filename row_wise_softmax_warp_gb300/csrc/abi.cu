@@ -77,6 +77,31 @@ cudaStream_t st(rowops_stream s) { return reinterpret_cast<cudaStream_t>(s); }
 
 }  // namespace
 
+namespace rowops {
+
+int layernorm_bwd_checks(const float* dy, const float* gamma, const float* xhat, const float* inv_std, float* dx,
+                         float* dgamma, float* dbeta, int64_t rows, int64_t cols, bool* vec4) {
+    if (int e = check_dims(rows, cols)) return e;
+    if (cols == 0) return ROWOPS_ERR_SHAPE;
+    if (rows == 0) return ROWOPS_OK;
+    if (!dy || !gamma || !xhat || !inv_std || !dx || !dgamma || !dbeta) return ROWOPS_ERR_NULL;
+    if (!elems_aligned({{dy, 4}, {gamma, 4}, {xhat, 4}, {inv_std, 4}, {dx, 4}, {dgamma, 4}, {dbeta, 4}}))
+        return ROWOPS_ERR_ALIGN;
+    const int64_t n = rows * cols * 4;
+    const Buf in[4] = {{dy, n}, {gamma, cols * 4}, {xhat, n}, {inv_std, rows * 4}};
+    const Buf o[3] = {{dx, n}, {dgamma, cols * 4}, {dbeta, cols * 4}};
+    for (int a = 0; a < 3; ++a) {
+        for (int b = 0; b < 4; ++b)
+            if (overlap(o[a], in[b])) return ROWOPS_ERR_ALIAS;
+        for (int b = 0; b < 3; ++b)
+            if (a != b && overlap(o[a], o[b])) return ROWOPS_ERR_ALIAS;
+    }
+    *vec4 = cols % 4 == 0 && aligned(dy, 16) && aligned(gamma, 16) && aligned(xhat, 16) && aligned(dx, 16);
+    return ROWOPS_OK;
+}
+
+}  // namespace rowops
+
 extern "C" {
 
 const char* rowops_status_string(int status) {
@@ -224,23 +249,18 @@ int rowops_layernorm_bwd(const float* dy, const float* gamma, const float* xhat,
                          const float* inv_std, float* dx, float* dgamma, float* dbeta,
                          int64_t rows, int64_t cols, void* workspace, size_t workspace_bytes,
                          rowops_stream stream) {
-    if (int e = check_dims(rows, cols)) return e;
-    if (cols == 0) return ROWOPS_ERR_SHAPE;
+    bool vec4 = false;
+    if (int e = rowops::layernorm_bwd_checks(dy, gamma, xhat, inv_std, dx, dgamma, dbeta, rows, cols, &vec4))
+        return e;
     if (rows == 0) return ROWOPS_OK;
-    if (!dy || !gamma || !xhat || !inv_std || !dx || !dgamma || !dbeta) return ROWOPS_ERR_NULL;
-    if (!elems_aligned({{dy, 4}, {gamma, 4}, {xhat, 4}, {inv_std, 4}, {dx, 4}, {dgamma, 4}, {dbeta, 4}}))
-        return ROWOPS_ERR_ALIGN;
     const size_t need = rowops::layernorm_bwd_workspace(rows, cols);
     if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return ROWOPS_ERR_WORKSPACE;
     const int64_t n = rows * cols * 4;
-    const Buf in[4] = {{dy, n}, {gamma, cols * 4}, {xhat, n}, {inv_std, rows * 4}};
-    const Buf o[4] = {{dx, n}, {dgamma, cols * 4}, {dbeta, cols * 4}, {workspace, int64_t(need)}};
-    for (int a = 0; a < 4; ++a) {
-        for (int b = 0; b < 4; ++b)
-            if (overlap(o[a], in[b]) || (a != b && overlap(o[a], o[b]))) return ROWOPS_ERR_ALIAS;
-    }
-    const bool vec4 = cols % 4 == 0 && aligned(dy, 16) && aligned(gamma, 16) && aligned(xhat, 16) &&
-                      aligned(dx, 16);
+    const Buf w{workspace, int64_t(need)};
+    const Buf all[7] = {{dy, n}, {gamma, cols * 4}, {xhat, n}, {inv_std, rows * 4},
+                        {dx, n}, {dgamma, cols * 4}, {dbeta, cols * 4}};
+    for (const Buf& b : all)
+        if (overlap(w, b)) return ROWOPS_ERR_ALIAS;
     return to_status(rowops::launch_layernorm_bwd(dy, gamma, xhat, inv_std, dx, dgamma, dbeta, rows,
                                                   cols, static_cast<float*>(workspace), vec4,
                                                   st(stream)));

@@ -115,12 +115,13 @@ uint32_t pipeline_timeouts_rows();
 uint32_t pipeline_timeouts_pairs();
 uint32_t pipeline_timeouts_ln();
 // LayerNorm backward stage 1 on rows of 384..1024 floats on 16-byte
-// boundaries (one CTA per SM, row blocks through the bulk-copy ring); writes
-// ln_bwd_tma_ctas(rows, cols) partials to ws.  ln_bwd_tma_ctas is 0 for
-// shapes it does not take.
-int64_t ln_bwd_tma_ctas(int64_t rows, int64_t cols);
+// boundaries through the bulk-copy ring (one CTA per SM, at most max_ctas,
+// 0: no limit); writes ln_bwd_tma_ctas(rows, cols, max_ctas) partials to ws.
+// ln_bwd_tma_ctas is 0 for shapes it does not take.
+int64_t ln_bwd_tma_ctas(int64_t rows, int64_t cols, int64_t max_ctas);
 bool launch_ln_bwd_tma(const float* dy, const float* gamma, const float* xhat, const float* inv_std, float* dx,
-                       float* ws, int64_t rows, int64_t cols, cudaStream_t stream, cudaError_t* err);
+                       float* ws, int64_t rows, int64_t cols, int64_t max_ctas, cudaStream_t stream,
+                       cudaError_t* err);
 // Softmax backward on long rows (two passes through the ring); y and dy must
 // share their alignment modulo 16 bytes.
 bool launch_softmax_bwd_tma(const float* y, const float* dy, float* dx, int64_t rows, int64_t cols,
@@ -142,11 +143,18 @@ cudaError_t launch_softmax_ce(const float* logits, const int32_t* targets, float
 cudaError_t launch_layernorm_fwd(const float* x, const float* gamma, const float* beta,
                                  float* out, float* xhat, float* inv_std, int64_t rows,
                                  int64_t cols, float eps, bool vec4, cudaStream_t stream);
-size_t layernorm_bwd_workspace(int64_t rows, int64_t cols);
+// The argument checks of rowops_layernorm_bwd other than the workspace's
+// (dimensions, null and misaligned pointers, overlaps of the inputs and
+// outputs), in the order that entry point reports them; sets *vec4.
+int layernorm_bwd_checks(const float* dy, const float* gamma, const float* xhat, const float* inv_std, float* dx,
+                         float* dgamma, float* dbeta, int64_t rows, int64_t cols, bool* vec4);
+// budget (bytes, 0: none) caps the workspace the launch may use: the
+// allocation-free entry point passes the size of its fixed array.
+size_t layernorm_bwd_workspace(int64_t rows, int64_t cols, size_t budget = 0);
 cudaError_t launch_layernorm_bwd(const float* dy, const float* gamma, const float* xhat,
                                  const float* inv_std, float* dx, float* dgamma, float* dbeta,
                                  int64_t rows, int64_t cols, float* workspace, bool vec4,
-                                 cudaStream_t stream);
+                                 cudaStream_t stream, size_t budget = 0);
 cudaError_t launch_router(const float* x, const uint8_t* mask, float* p, float* kept, int64_t rows,
                           int64_t cols, int64_t k, bool vec4, cudaStream_t stream);
 cudaError_t launch_top_k_rows(const float* x, float* values, float* indices, int64_t rows, int64_t cols,

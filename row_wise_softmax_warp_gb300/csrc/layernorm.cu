@@ -7,19 +7,22 @@
 //
 // Backward writes dx per row and the column sums dgamma_j = sum_i dy*xhat,
 // dbeta_j = sum_i dy in two deterministic stages:
-//   stage 1 (ln_bwd_group, clusters of 8 CTAs): each CTA owns a fixed block of
-//     rows; groups accumulate their columns in registers, CTAs add their warps
-//     in warp order through shared memory, and the 8 CTAs of a cluster add their
-//     partials in rank order through distributed shared memory, writing one
-//     partial per cluster to the workspace;
-//   stage 2 (ln_params_reduce): one thread per output column adds the
-//     cluster partials in increasing order.
-// Rows of 1025..8192 floats take a block-row stage 1 instead (ln_bwd_brow):
-// one CTA per row at a time, each thread keeping its columns' partials in
-// registers across the CTA's block of rows, one workspace slot per CTA.
-// Longer rows take ln_bwd_long: one 1024-thread CTA per SM, two passes over
-// each row, each thread's column partials in shared memory (or, past 25600
-// floats, in the CTA's workspace slot), one slot per CTA.
+//   stage 1 writes one partial of the column sums per CTA (or cluster) to the
+//     workspace: rows of 384..1024 floats on 16-byte boundaries take
+//     ln_bwd_cols (column owners, the CTA's whole block of rows staged in
+//     shared memory with cp.async) or, when the block does not fit,
+//     ln_bwd_tma (ln_bwd_tma.cu: row blocks through the bulk-copy ring);
+//     other rows of up to 1024 floats take ln_bwd_group (clusters of 8 CTAs:
+//     groups accumulate their columns in registers, CTAs add their warps in
+//     warp order through shared memory, the cluster adds its CTAs in rank
+//     order through distributed shared memory); rows of 1025..8192 floats
+//     take ln_bwd_brow (one CTA per row at a time, each thread keeping its
+//     columns' partials in registers across the CTA's rows); longer rows take
+//     ln_bwd_long (one 1024-thread CTA per SM, two passes over each row, each
+//     thread's column partials in shared memory or, past 25600 floats, in
+//     the CTA's workspace slot);
+//   stage 2 (ln_params_reduce, a programmatic dependent of stage 1) adds the
+//     partials per column in increasing order.
 #include "block_rows.cuh"
 #include "common.cuh"
 #include "launch.h"
@@ -32,12 +35,16 @@ constexpr int kLnClusterCtas = 8;
 // -------------------------------------------------------------- forward
 // pulsatrix HIPBackend::layer_norm_forward / TorchLean layer normalisation.
 
+// Blocks of any whole number of warps up to 1024 threads: a balanced launch
+// gives every SM one block of ceil(rows / SMs) groups, so no SM carries a
+// block more than another (with 256-thread blocks, 4096 rows of 768 floats put
+// 4 blocks on some SMs and 3 on the others).
 template <int LANES, int NV, int VEC>
-__global__ void __launch_bounds__(kBlockThreads)
+__global__ void __launch_bounds__(1024)
 ln_fwd_group(const float* __restrict__ x, const float* __restrict__ gamma,
              const float* __restrict__ beta, float* __restrict__ out, float* __restrict__ xhat,
              float* __restrict__ inv_std, int64_t rows, int cols, float eps) {
-    constexpr int GPB = kBlockThreads / LANES;
+    const int GPB = int(blockDim.x) / LANES;
     const int g = threadIdx.x % LANES;
     const int grp = threadIdx.x / LANES;
     const int lane = threadIdx.x & 31;
@@ -562,6 +569,197 @@ ln_bwd_brow(const float* __restrict__ dy, const float* __restrict__ gamma, const
     }
 }
 
+// Backward stage 1 with column owners (rows of 384..1024 floats on 16-byte
+// boundaries whose CTA block fits in shared memory whole).  A CTA of up to
+// 768 threads owns a contiguous block of rows, split into `sets` row sets of
+// tp threads (tp = cols/4 rounded up to whole warps): thread (h, t) owns the
+// float4 column chunk t of rows h, h + sets, ... of the block.  At the start
+// every thread issues cp.async copies of exactly those chunks of dy and xhat
+// (the whole block is requested at once, by all threads in parallel), in
+// kLnColsPhases commit groups, and later reads only its own data, so it
+// waits for its own copies and no other thread's.  Per phase: pass A adds the
+// thread's dgamma/dbeta partials for its columns in registers and reduces
+// each row's sums of g' and g'*xhat over the warp (shuffles), one value per
+// warp into shared memory; a CTA barrier; pass B adds the warps' values in
+// warp order and writes dx (the writes of a phase overlap the loads of the
+// next).  The column partials need no reduction across warps (each column
+// chunk has one owner per set): the sets add theirs in set order and the CTA
+// writes one workspace slot; ln_params_reduce adds the slots in order.  (A
+// single launch that finishes the column sums itself needs a rendezvous of
+// all CTAs, which measured slower on GB300 than this programmatic-dependent
+// second kernel.)
+constexpr int kLnColsThreads = 768;
+// Commit groups per thread (on GB300 at 4096 x 768, back to back: one 13.0 us,
+// two 12.7, three 13.4).
+constexpr int kLnColsPhases = 2;
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(smem))),
+                 "l"(gmem)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+// Waits until at most n of this thread's commit groups are pending (n <= 3).
+__device__ __forceinline__ void cp_async_wait_pending(int n) {
+    switch (n) {
+        case 0: asm volatile("cp.async.wait_group 0;\n" ::: "memory"); break;
+        case 1: asm volatile("cp.async.wait_group 1;\n" ::: "memory"); break;
+        case 2: asm volatile("cp.async.wait_group 2;\n" ::: "memory"); break;
+        default: asm volatile("cp.async.wait_group 3;\n" ::: "memory"); break;
+    }
+}
+
+__global__ void __launch_bounds__(kLnColsThreads, 1)
+ln_bwd_cols(const float* __restrict__ dy, const float* __restrict__ gamma, const float* __restrict__ xhat,
+            const float* __restrict__ inv_std, float* __restrict__ dx, float* __restrict__ ws, int64_t rows,
+            int cols, int64_t rows_per_cta, int sets, int tp) {
+    // Let the dependent stage-2 kernel be scheduled now; it waits for this
+    // grid's completion before reading the workspace.
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    constexpr int P = kLnColsPhases;
+    extern __shared__ __align__(16) float sm[];
+    const int nc = cols >> 2;
+    const int wps = tp >> 5;  // warps per set
+    const int64_t r_begin = int64_t(blockIdx.x) * rows_per_cta;
+    const int64_t r_end = r_begin + rows_per_cta < rows ? r_begin + rows_per_cta : rows;
+    const int n_rows = r_end > r_begin ? int(r_end - r_begin) : 0;
+    float4* sdy = reinterpret_cast<float4*>(sm);                              // [rows_per_cta][tp]
+    float4* sxh = sdy + size_t(rows_per_cta) * tp;                             // [rows_per_cta][tp]
+    float* red = reinterpret_cast<float*>(sxh + size_t(rows_per_cta) * tp);   // [rows_per_cta][wps][2]
+    float* inv_s = red + size_t(rows_per_cta) * wps * 2;                       // [rows_per_cta]
+    const int h = int(threadIdx.x) / tp;
+    const int t = int(threadIdx.x) % tp;
+    const int lane = threadIdx.x & 31;
+    const int wi = t >> 5;
+    const bool own = t < nc;
+    const int K = n_rows > h ? (n_rows - h + sets - 1) / sets : 0;  // rows of this thread's set
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+        if (own)
+            for (int k = p * K / P; k < (p + 1) * K / P; ++k) {
+                const int j = h + k * sets;
+                cp_async16(sdy + size_t(j) * tp + t, dy + (r_begin + j) * cols + 4 * t);
+                cp_async16(sxh + size_t(j) * tp + t, xhat + (r_begin + j) * cols + 4 * t);
+            }
+        cp_async_commit();
+    }
+    for (int j = int(threadIdx.x); j < n_rows; j += int(blockDim.x)) inv_s[j] = __ldg(inv_std + r_begin + j);
+    const float4 g = own ? __ldg(reinterpret_cast<const float4*>(gamma) + t) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float inv_cols = 1.0f / float(cols);
+    float4 pg = make_float4(0.f, 0.f, 0.f, 0.f), pb = pg;
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+        cp_async_wait_pending(P - 1 - p);  // this phase's rows have landed
+        const int k0 = p * K / P, k1 = (p + 1) * K / P;
+        for (int k = k0; k < k1; ++k) {  // pass A
+            const int j = h + k * sets;
+            float s1 = 0.f, s2 = 0.f;
+            if (own) {
+                const float4 a = sdy[size_t(j) * tp + t], x = sxh[size_t(j) * tp + t];
+                pg.x = fmaf(a.x, x.x, pg.x);
+                pg.y = fmaf(a.y, x.y, pg.y);
+                pg.z = fmaf(a.z, x.z, pg.z);
+                pg.w = fmaf(a.w, x.w, pg.w);
+                pb.x += a.x;
+                pb.y += a.y;
+                pb.z += a.z;
+                pb.w += a.w;
+                const float gx = a.x * g.x, gy = a.y * g.y, gz = a.z * g.z, gw = a.w * g.w;
+                s1 = (gx + gy) + (gz + gw);
+                s2 = fmaf(gx, x.x, s2);
+                s2 = fmaf(gy, x.y, s2);
+                s2 = fmaf(gz, x.z, s2);
+                s2 = fmaf(gw, x.w, s2);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                s1 += __shfl_xor_sync(kFullMask, s1, o);
+                s2 += __shfl_xor_sync(kFullMask, s2, o);
+            }
+            if (lane == 0) {
+                red[(size_t(j) * wps + wi) * 2] = s1;
+                red[(size_t(j) * wps + wi) * 2 + 1] = s2;
+            }
+        }
+        __syncthreads();  // the warps' row sums (and, the first time, inv_std) are in shared memory
+        for (int k = k0; k < k1; ++k) {  // pass B
+            const int j = h + k * sets;
+            float s1 = 0.f, s2 = 0.f;
+            for (int w = 0; w < wps; ++w) {
+                s1 += red[(size_t(j) * wps + w) * 2];
+                s2 += red[(size_t(j) * wps + w) * 2 + 1];
+            }
+            s1 *= inv_cols;
+            s2 *= inv_cols;
+            if (own) {
+                const float r = inv_s[j];
+                const float4 a = sdy[size_t(j) * tp + t], x = sxh[size_t(j) * tp + t];
+                float4 o;
+                o.x = r * (a.x * g.x - s1 - x.x * s2);
+                o.y = r * (a.y * g.y - s1 - x.y * s2);
+                o.z = r * (a.z * g.z - s1 - x.z * s2);
+                o.w = r * (a.w * g.w - s1 - x.w * s2);
+                reinterpret_cast<float4*>(dx + (r_begin + j) * cols)[t] = o;
+            }
+        }
+    }
+    __syncthreads();  // the staged rows are no longer read: the space holds the sets' partials
+    float4* cr = sdy;  // [sets][2][tp]
+    cr[(size_t(h) * 2) * tp + t] = pg;
+    cr[(size_t(h) * 2 + 1) * tp + t] = pb;
+    __syncthreads();
+    if (h == 0 && own) {
+        for (int q = 1; q < sets; ++q) {
+            const float4 u = cr[(size_t(q) * 2) * tp + t], v = cr[(size_t(q) * 2 + 1) * tp + t];
+            pg.x += u.x;
+            pg.y += u.y;
+            pg.z += u.z;
+            pg.w += u.w;
+            pb.x += v.x;
+            pb.y += v.y;
+            pb.z += v.z;
+            pb.w += v.w;
+        }
+        float4* slot = reinterpret_cast<float4*>(ws + int64_t(blockIdx.x) * 2 * cols);
+        slot[t] = pg;
+        slot[nc + t] = pb;
+    }
+}
+
+// Launch shape of ln_bwd_cols with at most max_ctas CTAs (0: one per SM):
+// grid, rows per CTA, row sets, threads per set and dynamic shared memory;
+// grid = 0 when the shape is not taken (the block does not fit).
+struct LnColsPlan {
+    int64_t grid = 0, per_cta = 0;
+    int sets = 0, tp = 0;
+    size_t smem = 0;
+};
+
+LnColsPlan ln_cols_plan(int64_t rows, int64_t cols, int64_t max_ctas) {
+    LnColsPlan pl;
+    if (cols < 384 || cols > 1024 || cols % 4 != 0 || rows <= 0) return pl;
+    const int sms = sm_count();
+    if (sms <= 0) return pl;
+    int64_t g = rows < sms ? rows : sms;
+    if (max_ctas > 0 && g > max_ctas) g = max_ctas;
+    if (g <= 0) return pl;
+    const int64_t per_cta = (rows + g - 1) / g;
+    g = (rows + per_cta - 1) / per_cta;
+    const int tp = int((cols / 4 + 31) / 32 * 32);
+    const int sets = kLnColsThreads / tp;
+    const size_t rows_bytes = size_t(per_cta) * (size_t(2) * tp * 16 + size_t(tp / 32) * 2 * 4 + 4);
+    const size_t parts_bytes = size_t(sets) * 2 * tp * 16;  // the sets' column partials at the end
+    const size_t smem = rows_bytes > parts_bytes ? rows_bytes : parts_bytes;
+    if (smem > 226 * 1024) return pl;
+    pl.grid = g;
+    pl.per_cta = per_cta;
+    pl.sets = sets;
+    pl.tp = tp;
+    pl.smem = smem;
+    return pl;
+}
+
 // Stage 2: out[i] = sum_p ws[p][i] for i in [0, 2*cols).  A block covers 32
 // outputs with 8 warps: warp j adds partials j, j+8, j+16, ... in order (loads
 // coalesced across the 32 outputs), then thread i adds the 8 warp sums in warp
@@ -614,8 +812,16 @@ cudaError_t launch_layernorm_fwd(const float* x, const float* gamma, const float
                                  int64_t cols, float eps, bool vec4, cudaStream_t stream) {
     const bool done = with_geometry(vec4, cols, [&](auto geo) {
         using G = decltype(geo);
-        ln_fwd_group<G::LANES, G::NV, G::VEC><<<group_grid(rows, G::LANES), kBlockThreads, 0, stream>>>(
-            x, gamma, beta, out, xhat, inv_std, rows, int(cols), eps);
+        const int sms = sm_count();
+        const int64_t per_sm = sms > 0 ? (rows + sms - 1) / sms : 0;  // groups per SM, balanced
+        const int64_t nt = (per_sm * G::LANES + 31) / 32 * 32;
+        if (nt >= kBlockThreads && nt <= 1024)
+            ln_fwd_group<G::LANES, G::NV, G::VEC><<<unsigned((rows + per_sm - 1) / per_sm), unsigned(nt), 0,
+                                                    stream>>>(x, gamma, beta, out, xhat, inv_std, rows,
+                                                              int(cols), eps);
+        else
+            ln_fwd_group<G::LANES, G::NV, G::VEC><<<group_grid(rows, G::LANES), kBlockThreads, 0, stream>>>(
+                x, gamma, beta, out, xhat, inv_std, rows, int(cols), eps);
     });
     if (!done) {
         if (with_block_geometry(vec4, cols, kBlockRowMax, [&](auto geo) {
@@ -634,9 +840,8 @@ cudaError_t launch_layernorm_fwd(const float* x, const float* gamma, const float
     return cudaGetLastError();
 }
 
-// Column partials of the backward: one per CTA of the row-block kernel or
-// one per cluster of the group kernel (rows of up to 1024 floats; the
-// workspace takes the larger count, so that it does not depend on alignment),
+// Column partials of the two-kernel backward: one per cluster of the group
+// kernel (rows of up to 1024 floats that the fused kernel does not take),
 // one per resident CTA of the block-row kernel (1024 threads per SM), one per
 // CTA of the long-row kernel.
 int64_t ln_bwd_slots(int64_t rows, int64_t cols) {
@@ -646,25 +851,48 @@ int64_t ln_bwd_slots(int64_t rows, int64_t cols) {
         const int64_t p = int64_t(sms > 0 ? sms : 1) * per_sm;
         return rows < p ? rows : p;
     }
-    const int64_t g = ln_bwd_partials(rows, cols), t = ln_bwd_tma_ctas(rows, cols);
-    return g > t ? g : t;
+    return ln_bwd_partials(rows, cols);
 }
 
-size_t layernorm_bwd_workspace(int64_t rows, int64_t cols) {
+// Stage-1 partials for rows of up to 1024 floats: the larger of the lane-group
+// kernel's cluster count and the column-owner / ring kernels' CTA count, so
+// the size does not depend on alignment.  With a byte budget the CTA count is
+// capped to fit it.
+int64_t ln_bwd_cap(int64_t cols, size_t budget) {
+    return budget ? int64_t(budget / (size_t(8) * size_t(cols))) : 0;
+}
+
+size_t layernorm_bwd_workspace(int64_t rows, int64_t cols, size_t budget) {
     if (rows <= 0 || cols <= 0) return 0;
-    return size_t(ln_bwd_slots(rows, cols)) * 2 * size_t(cols) * sizeof(float);
+    int64_t slots = ln_bwd_slots(rows, cols);
+    if (cols <= 1024) {
+        const int64_t c = ln_bwd_tma_ctas(rows, cols, ln_bwd_cap(cols, budget));
+        if (c > slots) slots = c;
+    }
+    return size_t(slots) * 2 * size_t(cols) * sizeof(float);
 }
 
 cudaError_t launch_layernorm_bwd(const float* dy, const float* gamma, const float* xhat,
                                  const float* inv_std, float* dx, float* dgamma, float* dbeta,
                                  int64_t rows, int64_t cols, float* ws, bool vec4,
-                                 cudaStream_t stream) {
-    int64_t partials = ln_bwd_slots(rows, cols);
+                                 cudaStream_t stream, size_t budget) {
     cudaError_t err = cudaSuccess;
+    int64_t partials = ln_bwd_slots(rows, cols);
     bool done = false;
-    if (vec4 && launch_ln_bwd_tma(dy, gamma, xhat, inv_std, dx, ws, rows, cols, stream, &err)) {
-        done = true;
-        partials = ln_bwd_tma_ctas(rows, cols);
+    const int64_t cap = ln_bwd_cap(cols, budget);
+    if (vec4) {
+        const LnColsPlan pl = ln_cols_plan(rows, cols, cap);
+        if (pl.grid > 0) {
+            err = cudaFuncSetAttribute(ln_bwd_cols, cudaFuncAttributeMaxDynamicSharedMemorySize, int(pl.smem));
+            if (err != cudaSuccess) return err;
+            ln_bwd_cols<<<unsigned(pl.grid), pl.sets * pl.tp, pl.smem, stream>>>(
+                dy, gamma, xhat, inv_std, dx, ws, rows, int(cols), pl.per_cta, pl.sets, pl.tp);
+            partials = pl.grid;
+            done = true;
+        } else if (launch_ln_bwd_tma(dy, gamma, xhat, inv_std, dx, ws, rows, cols, cap, stream, &err)) {
+            partials = ln_bwd_tma_ctas(rows, cols, cap);
+            done = true;
+        }
     }
     if (!done) done = with_ln_bwd_brow_geometry(vec4, cols, [&](auto geo) {
         using G = decltype(geo);
@@ -784,15 +1012,18 @@ extern "C" int rowops_layernorm_bwd_noalloc(const float* dy, const float* gamma,
                                             const float* inv_std, float* dx, float* dgamma,
                                             float* dbeta, int64_t rows, int64_t cols,
                                             rowops_stream stream) {
-    // Same argument rules as rowops_layernorm_bwd, checked there; only the
-    // workspace is ours.  Sizes whose workspace exceeds the array are refused.
-    if (rows > 0 && cols > 0 && rowops_layernorm_bwd_workspace(rows, cols) > kNoAllocScratchBytes)
+    // The argument rules of rowops_layernorm_bwd, in its order; then the size
+    // check against the array; the array's address is looked up last.
+    bool vec4 = false;
+    if (int e = rowops::layernorm_bwd_checks(dy, gamma, xhat, inv_std, dx, dgamma, dbeta, rows, cols, &vec4))
+        return e;
+    if (rows == 0) return ROWOPS_OK;
+    if (rowops::layernorm_bwd_workspace(rows, cols, kNoAllocScratchBytes) > kNoAllocScratchBytes)
         return ROWOPS_ERR_WORKSPACE;
-    if (rows <= 0 || cols <= 0)  // nothing to set up; let the common checks answer
-        return rowops_layernorm_bwd(dy, gamma, xhat, inv_std, dx, dgamma, dbeta, rows, cols, nullptr,
-                                    0, stream);
     float* ws = nullptr;
     if (int e = scratch_for_current_device(&ws)) return e;
-    return rowops_layernorm_bwd(dy, gamma, xhat, inv_std, dx, dgamma, dbeta, rows, cols, ws,
-                                kNoAllocScratchBytes, stream);
+    const cudaError_t err = rowops::launch_layernorm_bwd(dy, gamma, xhat, inv_std, dx, dgamma, dbeta, rows, cols,
+                                                         ws, vec4, reinterpret_cast<cudaStream_t>(stream),
+                                                         kNoAllocScratchBytes);
+    return err == cudaSuccess ? ROWOPS_OK : ROWOPS_ERR_CUDA;
 }

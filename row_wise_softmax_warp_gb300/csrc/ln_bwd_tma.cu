@@ -1,6 +1,8 @@
 // ln_bwd_tma.cu - LayerNorm backward stage 1 on rows of 384..1024 floats on
-// 16-byte boundaries, blocks of rows streamed through the bulk-copy ring
-// (pipeline.cuh); stage 2 (ln_params_reduce) is in layernorm.cu.
+// 16-byte boundaries whose CTA blocks do not fit in shared memory whole
+// (ln_bwd_cols in layernorm.cu takes those that do): blocks of rows streamed
+// through the bulk-copy ring (pipeline.cuh); stage 2 (ln_params_reduce) is in
+// layernorm.cu.
 #include "launch.h"
 #include "pipeline.cuh"
 
@@ -201,22 +203,21 @@ ln_bwd_tma(const float* __restrict__ dy, const float* __restrict__ gamma, const 
 
 }  // namespace
 
-int64_t ln_bwd_tma_ctas(int64_t rows, int64_t cols) {
+int64_t ln_bwd_tma_ctas(int64_t rows, int64_t cols, int64_t max_ctas) {
     // Below 384 floats the lane-group kernel is faster (on GB300, 65536 x 256:
     // 45.7 us against 50.8; 16384 x 512: 35.5 against 32.4).
     if (cols < 384 || cols > 128 * kLnTmaMaxNV || rows <= 0) return 0;
     const int sms = sm_count();
     if (sms <= 0) return 0;
-    // At most 2^17 / cols CTAs: the partials (8 * cols bytes each) of any row
-    // count then stay within 1 MiB.
     int64_t g = rows < sms ? rows : sms;
-    const int64_t cap = (int64_t(1) << 17) / cols;
-    return g < cap ? g : cap;
+    if (max_ctas > 0 && g > max_ctas) g = max_ctas;
+    return g;
 }
 
 bool launch_ln_bwd_tma(const float* dy, const float* gamma, const float* xhat, const float* inv_std, float* dx,
-                       float* ws, int64_t rows, int64_t cols, cudaStream_t stream, cudaError_t* err) {
-    const int64_t grid = ln_bwd_tma_ctas(rows, cols);
+                       float* ws, int64_t rows, int64_t cols, int64_t max_ctas, cudaStream_t stream,
+                       cudaError_t* err) {
+    const int64_t grid = ln_bwd_tma_ctas(rows, cols, max_ctas);
     if (grid <= 0 || cols % 4 != 0) return false;
     // slot_rows: a power of two; nslot: a multiple of 16 / slot_rows (see the kernel).
     int64_t slot_rows = 64;
