@@ -579,10 +579,11 @@ ln_bwd_brow(const float* __restrict__ dy, const float* __restrict__ gamma, const
 // kLnColsPhases commit groups, and later reads only its own data, so it
 // waits for its own copies and no other thread's.  Per phase: pass A adds the
 // thread's dgamma/dbeta partials for its columns in registers and reduces
-// each row's sums of g' and g'*xhat over the warp (shuffles), one value per
-// warp into shared memory; a CTA barrier; pass B adds the warps' values in
-// warp order and writes dx (the writes of a phase overlap the loads of the
-// next).  The column partials need no reduction across warps (each column
+// each row's sums of g' and g'*xhat over the warp, one value per warp into
+// shared memory (with two or more rows a thread, one reduce-scatter of all
+// the rows' sums: 16 shuffles where per-row butterflies take 10 a row); a CTA
+// barrier; pass B adds the warps' values in warp order and writes dx (the
+// writes of a phase overlap the loads of the next).  The column partials need no reduction across warps (each column
 // chunk has one owner per set): the sets add theirs in set order and the CTA
 // writes one workspace slot; ln_params_reduce adds the slots in order.  (A
 // single launch that finishes the column sums itself needs a rendezvous of
@@ -652,34 +653,83 @@ ln_bwd_cols(const float* __restrict__ dy, const float* __restrict__ gamma, const
     for (int p = 0; p < P; ++p) {
         cp_async_wait_pending(P - 1 - p);  // this phase's rows have landed
         const int k0 = p * K / P, k1 = (p + 1) * K / P;
-        for (int k = k0; k < k1; ++k) {  // pass A
-            const int j = h + k * sets;
-            float s1 = 0.f, s2 = 0.f;
-            if (own) {
-                const float4 a = sdy[size_t(j) * tp + t], x = sxh[size_t(j) * tp + t];
-                pg.x = fmaf(a.x, x.x, pg.x);
-                pg.y = fmaf(a.y, x.y, pg.y);
-                pg.z = fmaf(a.z, x.z, pg.z);
-                pg.w = fmaf(a.w, x.w, pg.w);
-                pb.x += a.x;
-                pb.y += a.y;
-                pb.z += a.z;
-                pb.w += a.w;
-                const float gx = a.x * g.x, gy = a.y * g.y, gz = a.z * g.z, gw = a.w * g.w;
-                s1 = (gx + gy) + (gz + gw);
-                s2 = fmaf(gx, x.x, s2);
-                s2 = fmaf(gy, x.y, s2);
-                s2 = fmaf(gz, x.z, s2);
-                s2 = fmaf(gw, x.w, s2);
-            }
+        if (k1 - k0 >= 2) {  // warp-uniform (a warp lies in one set)
+            // Pass A over up to 8 rows of this thread: their 16 sums are
+            // reduce-scattered over the warp (16 shuffles in all, the same
+            // addition tree as a butterfly per sum).
+            float v[16];
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                s1 += __shfl_xor_sync(kFullMask, s1, o);
-                s2 += __shfl_xor_sync(kFullMask, s2, o);
+            for (int i = 0; i < 16; ++i) v[i] = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int k = k0 + i;
+                if (own && k < k1) {
+                    const int j = h + k * sets;
+                    const float4 a = sdy[size_t(j) * tp + t], x = sxh[size_t(j) * tp + t];
+                    pg.x = fmaf(a.x, x.x, pg.x);
+                    pg.y = fmaf(a.y, x.y, pg.y);
+                    pg.z = fmaf(a.z, x.z, pg.z);
+                    pg.w = fmaf(a.w, x.w, pg.w);
+                    pb.x += a.x;
+                    pb.y += a.y;
+                    pb.z += a.z;
+                    pb.w += a.w;
+                    const float gx = a.x * g.x, gy = a.y * g.y, gz = a.z * g.z, gw = a.w * g.w;
+                    float s2 = 0.f;
+                    s2 = fmaf(gx, x.x, s2);
+                    s2 = fmaf(gy, x.y, s2);
+                    s2 = fmaf(gz, x.z, s2);
+                    s2 = fmaf(gw, x.w, s2);
+                    v[2 * i] = (gx + gy) + (gz + gw);
+                    v[2 * i + 1] = s2;
+                }
             }
-            if (lane == 0) {
-                red[(size_t(j) * wps + wi) * 2] = s1;
-                red[(size_t(j) * wps + wi) * 2 + 1] = s2;
+            // Each round halves the values a lane holds; lanes 2m and 2m + 1
+            // end with the warp's total of value m (row m / 2, sum m % 2).
+#pragma unroll
+            for (int half = 8, o = 16; half >= 1; half >>= 1, o >>= 1) {
+                const bool up = (lane & o) != 0;
+#pragma unroll
+                for (int i = 0; i < half; ++i) {
+                    const float send = up ? v[i] : v[i + half];
+                    const float keep = up ? v[i + half] : v[i];
+                    v[i] = keep + __shfl_xor_sync(kFullMask, send, o);
+                }
+            }
+            v[0] += __shfl_xor_sync(kFullMask, v[0], 1);
+            const int m = (lane >> 1) & 15;
+            if ((lane & 1) == 0 && (m >> 1) < k1 - k0)
+                red[(size_t(h + (k0 + (m >> 1)) * sets) * wps + wi) * 2 + (m & 1)] = v[0];
+        } else {  // one row or none: a butterfly per sum
+            for (int k = k0; k < k1; ++k) {  // pass A
+                const int j = h + k * sets;
+                float s1 = 0.f, s2 = 0.f;
+                if (own) {
+                    const float4 a = sdy[size_t(j) * tp + t], x = sxh[size_t(j) * tp + t];
+                    pg.x = fmaf(a.x, x.x, pg.x);
+                    pg.y = fmaf(a.y, x.y, pg.y);
+                    pg.z = fmaf(a.z, x.z, pg.z);
+                    pg.w = fmaf(a.w, x.w, pg.w);
+                    pb.x += a.x;
+                    pb.y += a.y;
+                    pb.z += a.z;
+                    pb.w += a.w;
+                    const float gx = a.x * g.x, gy = a.y * g.y, gz = a.z * g.z, gw = a.w * g.w;
+                    s1 = (gx + gy) + (gz + gw);
+                    s2 = fmaf(gx, x.x, s2);
+                    s2 = fmaf(gy, x.y, s2);
+                    s2 = fmaf(gz, x.z, s2);
+                    s2 = fmaf(gw, x.w, s2);
+                }
+    #pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    s1 += __shfl_xor_sync(kFullMask, s1, o);
+                    s2 += __shfl_xor_sync(kFullMask, s2, o);
+                }
+                if (lane == 0) {
+                    red[(size_t(j) * wps + wi) * 2] = s1;
+                    red[(size_t(j) * wps + wi) * 2 + 1] = s2;
+                }
             }
         }
         __syncthreads();  // the warps' row sums (and, the first time, inv_std) are in shared memory
@@ -748,6 +798,8 @@ LnColsPlan ln_cols_plan(int64_t rows, int64_t cols, int64_t max_ctas) {
     g = (rows + per_cta - 1) / per_cta;
     const int tp = int((cols / 4 + 31) / 32 * 32);
     const int sets = kLnColsThreads / tp;
+    const int64_t per_set = (per_cta + sets - 1) / sets;
+    if ((per_set + kLnColsPhases - 1) / kLnColsPhases > 8) return pl;  // pass A holds 8 rows
     const size_t rows_bytes = size_t(per_cta) * (size_t(2) * tp * 16 + size_t(tp / 32) * 2 * 4 + 4);
     const size_t parts_bytes = size_t(sets) * 2 * tp * 16;  // the sets' column partials at the end
     const size_t smem = rows_bytes > parts_bytes ? rows_bytes : parts_bytes;
