@@ -70,6 +70,27 @@ inline unsigned group_grid(int64_t rows, int lanes) {
     return static_cast<unsigned>(b < 1 ? 1 : b);
 }
 
+// Balanced launch for a group kernel whose block is any whole number of warps
+// (up to 1024 threads, GPB = blockDim.x / LANES): one block per SM holding
+// ceil(rows / SMs) groups, so no SM carries a block more than another (with
+// 256-thread blocks, 4096 rows of 768 floats put 4 blocks on 56 SMs and 3 on
+// the other 96).  threads = 0 when that block would be smaller than
+// kBlockThreads-equivalent work or larger than 1024 threads (use group_grid).
+struct BalancedLaunch {
+    unsigned grid = 0, threads = 0;
+};
+inline BalancedLaunch balanced_groups(int64_t rows, int lanes) {
+    BalancedLaunch b;
+    const int sms = sm_count();
+    if (sms <= 0 || rows <= 0) return b;
+    const int64_t per_sm = (rows + sms - 1) / sms;  // groups per block
+    const int64_t nt = (per_sm * lanes + 31) / 32 * 32;
+    if (nt < 256 || nt > 1024) return b;
+    b.grid = static_cast<unsigned>((rows + per_sm - 1) / per_sm);
+    b.threads = static_cast<unsigned>(nt);
+    return b;
+}
+
 // Blocks for a group kernel whose loop loads the next rows while it works on
 // the current ones: at most `per_sm` blocks per SM, so each group walks several
 // rows and its loads stay in flight across the selection work.

@@ -35,10 +35,8 @@ constexpr int kLnClusterCtas = 8;
 // -------------------------------------------------------------- forward
 // pulsatrix HIPBackend::layer_norm_forward / TorchLean layer normalisation.
 
-// Blocks of any whole number of warps up to 1024 threads: a balanced launch
-// gives every SM one block of ceil(rows / SMs) groups, so no SM carries a
-// block more than another (with 256-thread blocks, 4096 rows of 768 floats put
-// 4 blocks on some SMs and 3 on the others).
+// Blocks of any whole number of warps up to 1024 threads, for the balanced
+// launch (launch.h, balanced_groups).
 template <int LANES, int NV, int VEC>
 __global__ void __launch_bounds__(1024)
 ln_fwd_group(const float* __restrict__ x, const float* __restrict__ gamma,
@@ -864,13 +862,10 @@ cudaError_t launch_layernorm_fwd(const float* x, const float* gamma, const float
                                  int64_t cols, float eps, bool vec4, cudaStream_t stream) {
     const bool done = with_geometry(vec4, cols, [&](auto geo) {
         using G = decltype(geo);
-        const int sms = sm_count();
-        const int64_t per_sm = sms > 0 ? (rows + sms - 1) / sms : 0;  // groups per SM, balanced
-        const int64_t nt = (per_sm * G::LANES + 31) / 32 * 32;
-        if (nt >= kBlockThreads && nt <= 1024)
-            ln_fwd_group<G::LANES, G::NV, G::VEC><<<unsigned((rows + per_sm - 1) / per_sm), unsigned(nt), 0,
-                                                    stream>>>(x, gamma, beta, out, xhat, inv_std, rows,
-                                                              int(cols), eps);
+        const BalancedLaunch bl = balanced_groups(rows, G::LANES);
+        if (bl.threads)
+            ln_fwd_group<G::LANES, G::NV, G::VEC><<<bl.grid, bl.threads, 0, stream>>>(
+                x, gamma, beta, out, xhat, inv_std, rows, int(cols), eps);
         else
             ln_fwd_group<G::LANES, G::NV, G::VEC><<<group_grid(rows, G::LANES), kBlockThreads, 0, stream>>>(
                 x, gamma, beta, out, xhat, inv_std, rows, int(cols), eps);

@@ -21,11 +21,13 @@
 namespace rowops {
 namespace {
 
+// Blocks of any whole number of warps up to 1024 threads, for the balanced
+// launch (launch.h, balanced_groups).
 template <int LANES, int NV, int VEC>
-__global__ void __launch_bounds__(kBlockThreads)
+__global__ void __launch_bounds__(1024)
 rms_fwd_group(const float* __restrict__ x, const float* __restrict__ gamma, float* __restrict__ out,
               float* __restrict__ row_rms, int64_t rows, int cols, float eps) {
-    constexpr int GPB = kBlockThreads / LANES;
+    const int GPB = int(blockDim.x) / LANES;
     const int g = threadIdx.x % LANES;
     const int grp = threadIdx.x / LANES;
     const int nch = cols / VEC;
@@ -353,8 +355,13 @@ cudaError_t launch_rmsnorm_fwd(const float* x, const float* gamma, float* out, f
                                int64_t cols, float eps, bool vec4, cudaStream_t stream) {
     const bool done = with_geometry(vec4, cols, [&](auto geo) {
         using G = decltype(geo);
-        rms_fwd_group<G::LANES, G::NV, G::VEC><<<group_grid(rows, G::LANES), kBlockThreads, 0, stream>>>(
-            x, gamma, out, row_rms, rows, int(cols), eps);
+        const BalancedLaunch bl = balanced_groups(rows, G::LANES);
+        if (bl.threads)
+            rms_fwd_group<G::LANES, G::NV, G::VEC><<<bl.grid, bl.threads, 0, stream>>>(
+                x, gamma, out, row_rms, rows, int(cols), eps);
+        else
+            rms_fwd_group<G::LANES, G::NV, G::VEC><<<group_grid(rows, G::LANES), kBlockThreads, 0, stream>>>(
+                x, gamma, out, row_rms, rows, int(cols), eps);
     });
     if (!done) {
         if (with_block_geometry(vec4, cols, kBlockRowMax, [&](auto geo) {
