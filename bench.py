@@ -182,6 +182,19 @@ class Ops:
             ("top_k_rows", lambda: ro.rowops_top_k_rows(self.rx, self.k, True, self.tv, self.ti)),
         ]
 
+    def next_io(self):
+        """Per op beyond the step: (device inputs, device outputs) of its call."""
+        return {
+            "rmsnorm_fwd": ([self.lx, self.lg], [self.rms_out, self.rms_r]),
+            "rmsnorm_bwd": ([self.ldy, self.lg, self.lx, self.rms_r], [self.rms_dx, self.rms_t]),
+            "column_sums": ([self.rms_t], [self.rms_dg]),
+            "argmax_onehot": ([self.rx], [self.fk]),
+            "soft_ce": ([self.lx, self.ldy_soft], [self.rms_dx, self.rms_r, self.cml]),
+            "teacher_ce": ([self.lx, self.ldy], [self.rms_dx, self.rms_r, self.cml]),
+            "router_masked_topk": ([self.rx, self.rm], [self.fp, self.fk]),
+            "top_k_rows": ([self.rx], [self.tv, self.ti]),
+        }
+
     def e2e_io(self):
         """Per op: (device inputs, device outputs) that an end-to-end call moves."""
         return {
@@ -198,16 +211,16 @@ class Ops:
         }
 
 
-def back_to_back(ops, dev, stream, l2_bytes, calls_min=40):
-    """Per-call ms of each step op launched back to back, as in a training
-    step, with no flush and no events between the calls (the calls replayed as
-    one CUDA graph).  Each op cycles through copies of its own buffers whose
-    total exceeds twice the L2, so every call still finds its inputs outside
-    the L2.  Returns ({op: ms}, {op: sets})."""
+def back_to_back(ops, dev, stream, l2_bytes, calls_min=40, table="table", io_name="e2e_io"):
+    """Per-call ms of each op of ops.<table>() launched back to back, as in a
+    training step, with no flush and no events between the calls (the calls
+    replayed as one CUDA graph).  Each op cycles through copies of its own
+    buffers (ops.<io_name>()) whose total exceeds twice the L2, so every call
+    still finds its inputs outside the L2.  Returns ({op: ms}, {op: sets})."""
     import copy
     import torch
-    io = ops.e2e_io()
-    names = [n for n, _ in ops.table()]
+    io = getattr(ops, io_name)()
+    names = [n for n, _ in getattr(ops, table)()]
     per_call, sets_used = {}, {}
     for idx, name in enumerate(names):
         ins, outs = io[name]
@@ -223,7 +236,7 @@ def back_to_back(ops, dev, stream, l2_bytes, calls_min=40):
                         setattr(twin, attr, val.clone())
                     elif any(val is t for t in outs):
                         setattr(twin, attr, torch.empty_like(val))
-            fns.append(twin.table()[idx][1])
+            fns.append(getattr(twin, table)()[idx][1])
         calls = max(calls_min, n_sets)
         for f in fns:  # warm-up: every set once
             f()
@@ -606,10 +619,12 @@ def gpu_leg(args):
         next_ms[name] = sum(a.elapsed_time(b) for a, b in ts) / len(ts)
 
     # ------------------------------------------- the step ops back to back
-    b2b_ms, b2b_sets = {}, {}
+    b2b_ms, b2b_sets, next_b2b_ms = {}, {}, {}
     if not args.no_back_to_back:
         b2b_ms_local, b2b_sets = back_to_back(ops, dev, stream, L2_BYTES)
         b2b_ms = {n: max_over_ranks(b2b_ms_local[n], dist, dev) for n in b2b_ms_local}
+        nb_local, _ = back_to_back(ops, dev, stream, L2_BYTES, table="next_table", io_name="next_io")
+        next_b2b_ms = {n: max_over_ranks(nb_local[n], dist, dev) for n in nb_local}
 
     # ------------------------------------------------ the step as a CUDA graph
     # The ten calls captured once and replayed: no host work per launch and no
@@ -712,7 +727,11 @@ def gpu_leg(args):
         "gpu_launches": int(launches),
         "next_ops": {n: {"ms": round(next_ms[n], 5), "alg_bytes": next_bytes()[n][0],
                          "GB/s": round(next_bytes()[n][0] / (next_ms[n] * 1e-3) / 1e9, 1),
-                         "frac_of_measured": round(next_bytes()[n][0] / (next_ms[n] * 1e-3) / 1e9 / peak, 4)}
+                         "frac_of_measured": round(next_bytes()[n][0] / (next_ms[n] * 1e-3) / 1e9 / peak, 4),
+                         **({"back_to_back_ms": round(next_b2b_ms[n], 5),
+                             "back_to_back_frac_of_measured":
+                                 round(next_bytes()[n][0] / (next_b2b_ms[n] * 1e-3) / 1e9 / peak, 4)}
+                            if n in next_b2b_ms else {})}
                      for n in next_ms},
         "e2e": {"value": round(world * total_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
