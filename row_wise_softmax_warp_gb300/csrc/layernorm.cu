@@ -913,7 +913,12 @@ size_t layernorm_bwd_workspace(int64_t rows, int64_t cols, size_t budget) {
     if (rows <= 0 || cols <= 0) return 0;
     int64_t slots = ln_bwd_slots(rows, cols);
     if (cols <= 1024) {
-        const int64_t c = ln_bwd_tma_ctas(rows, cols, ln_bwd_cap(cols, budget));
+        // the column-owner kernel runs up to one CTA per SM; the ring kernel
+        // no more than that
+        const int sms = sm_count();
+        int64_t c = rows < sms ? rows : int64_t(sms);
+        const int64_t cap = ln_bwd_cap(cols, budget);
+        if (cap > 0 && c > cap) c = cap;
         if (c > slots) slots = c;
     }
     return size_t(slots) * 2 * size_t(cols) * sizeof(float);
