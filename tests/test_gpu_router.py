@@ -76,6 +76,40 @@ def test_kept_with_nan_and_infinities(ro, cols):
         assert np.array_equal(kept, oracle.topk_kept(x, k).astype(np.float32)), (cols, k)
 
 
+def _gpu_at(a: np.ndarray, offset_bytes: int) -> torch.Tensor:
+    """Device copy of `a` whose data pointer is `offset_bytes` past a 256-byte boundary."""
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    flat = torch.empty(t.numel() + 64, dtype=t.dtype, device="cuda")
+    off = offset_bytes // t.element_size()
+    view = flat[off:off + t.numel()].view(t.shape)
+    view.copy_(t.to("cuda"))
+    assert view.data_ptr() % 256 == offset_bytes
+    return view
+
+
+@pytest.mark.parametrize("cols", [34, 36, 40, 62, 64, 66, 96, 100, 128, 130])
+def test_kept_top2_every_alignment(ro, cols):
+    # Rows on 16-byte boundaries take the float4 lane groups, the others (8- or
+    # 4-byte boundaries, odd lengths) the scalar ones.  Ties, -0/+0,
+    # infinities and a NaN row, at every alignment of input and output.
+    rng = np.random.default_rng(cols)
+    rows = 203
+    x = (rng.integers(-6, 7, (rows, cols)) / 4.0).astype(np.float32)
+    x[x == 0] = np.where(rng.random(int((x == 0).sum())) < 0.5, 0.0, -0.0).astype(np.float32)
+    x[rng.random(x.shape) < 0.02] = np.inf
+    x[rng.random(x.shape) < 0.02] = -np.inf
+    x[7] = -np.inf
+    x[8] = 0.0
+    x[9, ::3] = np.nan
+    x[150] = -0.0
+    for k in (1, 2):
+        ref = oracle.topk_kept(x, k).astype(np.float32)
+        for xo, ko in ((0, 0), (8, 0), (0, 8), (8, 8), (4, 0), (12, 4)):
+            out = _gpu_at(np.zeros_like(x), ko)
+            ro.rowops_topk_kept(_gpu_at(x, xo), k, out)
+            assert np.array_equal(host(out), ref), (cols, k, xo, ko, np.argwhere(host(out) != ref)[:5])
+
+
 def test_kept_denormals(ro):
     tiny = np.float32(1e-45)
     x = np.array([[tiny, 0.0, -tiny, -0.0, 2 * tiny, tiny]], np.float32)
