@@ -6,8 +6,9 @@
 // and among equal values (-0 == +0 included) the lower column.  The entries
 // beating i are then exactly those ranked above it, so kept_i = [rank_i < k],
 // found exactly without counting:
-//   k <= 2      one pass keeping each lane's best two (value, column) pairs,
-//               then a butterfly merge of the pairs across the group;
+//   k <= 2      each lane's best two (value, column) pairs by a branch-free
+//               tournament over its entries in column order, then a
+//               butterfly merge of the pairs across the group;
 //   k <= LANES  (groups of 8 or more lanes, with per-warp shared scratch)
 //               candidates: each lane's largest value is an entry of the row,
 //               so at least k entries reach tau, the k-th largest of the
@@ -50,6 +51,44 @@ constexpr int kMaxRounds = 8;
 // or equal value (-0 == +0) and lower column.
 __device__ __forceinline__ bool beats(float xv, int xc, float yv, int yc) {
     return xv > yv || (xv == yv && xc < yc);
+}
+
+// The best two entries of a set: (v1, c1) before (v2, c2) in the rule's order.
+struct Top2 {
+    float v1, v2;
+    int c1, c2;
+};
+
+// Top2 of two entries, a's column below b's.
+__device__ __forceinline__ Top2 top2_pair(float av, int ac, float bv, int bc) {
+    const bool t = av >= bv;  // equal values: the lower column, a
+    return Top2{t ? av : bv, t ? bv : av, t ? ac : bc, t ? bc : ac};
+}
+
+// Top2 of the union of two disjoint sets; with `ordered` every column of a is
+// below every column of b, so equal values go to a without comparing columns.
+template <bool ordered>
+__device__ __forceinline__ Top2 top2_merge(const Top2& a, const Top2& b) {
+    const bool t = ordered ? a.v1 >= b.v1 : !beats(b.v1, b.c1, a.v1, a.c1);
+    // the runner-up is the better of the winner's second and the loser's first
+    const float av = t ? a.v2 : a.v1, bv = t ? b.v1 : b.v2;
+    const int ac = t ? a.c2 : a.c1, bc = t ? b.c1 : b.c2;
+    const bool u = ordered ? av >= bv : !beats(bv, bc, av, ac);
+    return Top2{t ? a.v1 : b.v1, u ? av : bv, t ? a.c1 : b.c1, u ? ac : bc};
+}
+
+// Top2 of entries [lo, lo + n) of a lane's list (columns increasing along
+// it): a tournament of adjacent blocks, so every merge is an ordered one.
+template <int N>
+__device__ __forceinline__ Top2 top2_range(const float* x, const int* c, int lo) {
+    if constexpr (N == 2) {
+        return top2_pair(x[lo], c[lo], x[lo + 1], c[lo + 1]);
+    } else if constexpr (N == 3) {
+        const Top2 a = top2_pair(x[lo], c[lo], x[lo + 1], c[lo + 1]);
+        return top2_merge<true>(a, Top2{x[lo + 2], -INFINITY, c[lo + 2], INT_MAX});
+    } else {
+        return top2_merge<true>(top2_range<N / 2>(x, c, lo), top2_range<N - N / 2>(x, c, lo + N / 2));
+    }
 }
 
 __device__ __forceinline__ uint64_t make_key(float x, int col, int cols) {
@@ -198,43 +237,35 @@ __device__ __forceinline__ void kept_select(const float (&v)[NV][VEC], const boo
 #pragma unroll
             for (int e = 0; e < VEC; ++e) keep[kk][e] = cnt[kk][e] < k;
     } else if (k <= 2) {
-        // Top two in one pass: each lane keeps its best two (value, column)
-        // pairs; its columns arrive in increasing order, so a later entry only
-        // displaces on a strictly larger value (or an empty place).  The group
-        // then merges the pairs with a butterfly under the full rule; every lane
-        // ends with the row's best two.
-        float m1 = -INFINITY, m2 = -INFINITY;
-        int i1 = INT_MAX, i2 = INT_MAX;
+        // Top two: each lane's best two by a tournament over its entries in
+        // column order (an entry outside the row counts as -inf at its own
+        // column, which is above every column of the row, so it loses every
+        // tie); then a butterfly merges the lanes' pairs under the full rule,
+        // and every lane ends with the row's best two.  A row has at least
+        // k entries, so no entry outside it is picked.
+        constexpr int E = NV * VEC;
+        float xs[E];
+        int cs[E];
 #pragma unroll
         for (int kk = 0; kk < NV; ++kk)
 #pragma unroll
             for (int e = 0; e < VEC; ++e) {
-                const float xv = v[kk][e];
-                const int c = (g + kk * LANES) * VEC + e;
-                if (valid[kk][e]) {
-                    if (xv > m1 || i1 == INT_MAX) {
-                        m2 = m1; i2 = i1; m1 = xv; i1 = c;
-                    } else if (xv > m2 || i2 == INT_MAX) {
-                        m2 = xv; i2 = c;
-                    }
-                }
+                xs[kk * VEC + e] = valid[kk][e] ? v[kk][e] : -INFINITY;
+                cs[kk * VEC + e] = (g + kk * LANES) * VEC + e;
             }
+        Top2 t;
+        if constexpr (E == 1) {
+            t = Top2{xs[0], -INFINITY, cs[0], INT_MAX};
+        } else {
+            t = top2_range<E>(xs, cs, 0);
+        }
 #pragma unroll
         for (int o = LANES / 2; o > 0; o >>= 1) {
-            const float om1 = __shfl_xor_sync(kFullMask, m1, o), om2 = __shfl_xor_sync(kFullMask, m2, o);
-            const int oi1 = __shfl_xor_sync(kFullMask, i1, o), oi2 = __shfl_xor_sync(kFullMask, i2, o);
-            if (beats(om1, oi1, m1, i1)) {
-                if (beats(om2, oi2, m1, i1)) {
-                    m2 = om2; i2 = oi2;
-                } else {
-                    m2 = m1; i2 = i1;
-                }
-                m1 = om1; i1 = oi1;
-            } else if (beats(om1, oi1, m2, i2)) {
-                m2 = om1; i2 = oi1;
-            }
+            const Top2 u{__shfl_xor_sync(kFullMask, t.v1, o), __shfl_xor_sync(kFullMask, t.v2, o),
+                         __shfl_xor_sync(kFullMask, t.c1, o), __shfl_xor_sync(kFullMask, t.c2, o)};
+            t = top2_merge<false>(t, u);
         }
-        if (k == 1) i2 = -1;
+        const int i1 = t.c1, i2 = k == 1 ? -1 : t.c2;
 #pragma unroll
         for (int kk = 0; kk < NV; ++kk)
 #pragma unroll
