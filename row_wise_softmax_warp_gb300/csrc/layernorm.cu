@@ -579,8 +579,9 @@ ln_bwd_brow(const float* __restrict__ dy, const float* __restrict__ gamma, const
 // thread's dgamma/dbeta partials for its columns in registers and reduces
 // each row's sums of g' and g'*xhat over the warp, one value per warp into
 // shared memory (with two or more rows a thread, one reduce-scatter of all
-// the rows' sums: 16 shuffles where per-row butterflies take 10 a row); a CTA
-// barrier; pass B adds the warps' values in warp order and writes dx (the
+// the rows' sums: 16 shuffles where per-row butterflies take 10 a row); a
+// barrier of the set's warps only (a named barrier per set: the sets share
+// no rows, so one set's late copies do not hold up another's); pass B adds the warps' values in warp order and writes dx (the
 // writes of a phase overlap the loads of the next).  The column partials need no reduction across warps (each column
 // chunk has one owner per set): the sets add theirs in set order and the CTA
 // writes one workspace slot; ln_params_reduce adds the slots in order.  (A
@@ -589,8 +590,14 @@ ln_bwd_brow(const float* __restrict__ dy, const float* __restrict__ gamma, const
 // second kernel.)
 constexpr int kLnColsThreads = 768;
 // Commit groups per thread (on GB300 at 4096 x 768, back to back: one 13.0 us,
-// two 12.7, three 13.4).
+// two 12.7, three 13.4; with the per-set barriers two 12.5-12.8, three 13.7,
+// four 14.2).
 constexpr int kLnColsPhases = 2;
+
+// Barrier of one row set's tp threads (named barrier 1 + h; sets <= 8).
+__device__ __forceinline__ void set_barrier(int h, int tp) {
+    asm volatile("bar.sync %0, %1;\n" ::"r"(1 + h), "r"(tp) : "memory");
+}
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(
@@ -643,7 +650,7 @@ ln_bwd_cols(const float* __restrict__ dy, const float* __restrict__ gamma, const
             }
         cp_async_commit();
     }
-    for (int j = int(threadIdx.x); j < n_rows; j += int(blockDim.x)) inv_s[j] = __ldg(inv_std + r_begin + j);
+    for (int k = t; k < K; k += tp) inv_s[h + k * sets] = __ldg(inv_std + r_begin + h + k * sets);  // own set's rows
     const float4 g = own ? __ldg(reinterpret_cast<const float4*>(gamma) + t) : make_float4(0.f, 0.f, 0.f, 0.f);
     const float inv_cols = 1.0f / float(cols);
     float4 pg = make_float4(0.f, 0.f, 0.f, 0.f), pb = pg;
@@ -730,7 +737,7 @@ ln_bwd_cols(const float* __restrict__ dy, const float* __restrict__ gamma, const
                 }
             }
         }
-        __syncthreads();  // the warps' row sums (and, the first time, inv_std) are in shared memory
+        set_barrier(h, tp);  // the set's warps' row sums (and, the first time, inv_std) are in shared memory
         for (int k = k0; k < k1; ++k) {  // pass B
             const int j = h + k * sets;
             float s1 = 0.f, s2 = 0.f;
