@@ -22,7 +22,7 @@ template <bool TEACHER, int LANES, int NV, int VEC>
 __global__ void __launch_bounds__(kBlockThreads)
 ce2_group(const float* __restrict__ x, const float* __restrict__ w, float* __restrict__ grad,
           float* __restrict__ row_loss, int64_t rows, int cols, float grad_scale) {
-    constexpr int GPB = kBlockThreads / LANES;
+    const int GPB = int(blockDim.x) / LANES;  // blocks of up to kBlockThreads
     const int g = threadIdx.x % LANES;
     const int grp = threadIdx.x / LANES;
     const int nch = cols / VEC;
@@ -318,8 +318,15 @@ cudaError_t launch_ce2(const float* x, const float* w, float* grad, float* row_l
                        int64_t rows, int64_t cols, float grad_scale, bool vec4, cudaStream_t stream) {
     const bool done = with_geometry(vec4, cols, [&](auto geo) {
         using G = decltype(geo);
-        ce2_group<TEACHER, G::LANES, G::NV, G::VEC><<<group_grid(rows, G::LANES), kBlockThreads, 0, stream>>>(
-            x, w, grad, row_loss, rows, int(cols), grad_scale);
+        // blocks of 128 threads: finer than 256 when a row takes a warp of
+        // ~90 registers and the rows do not fit one wave (on GB300, 4096 x 768
+        // back to back: soft 11.2 -> 10.9 us, teacher 12.6 -> 12.4)
+        constexpr int nt = 128;
+        const int64_t gpb = nt / G::LANES;
+        const int64_t blocks = (rows + gpb - 1) / gpb;
+        ce2_group<TEACHER, G::LANES, G::NV, G::VEC>
+            <<<unsigned(blocks < (1 << 20) ? blocks : (1 << 20)), nt, 0, stream>>>(x, w, grad, row_loss, rows,
+                                                                               int(cols), grad_scale);
     });
     cudaError_t err = cudaSuccess;
     if (!done && !with_block_geometry(vec4, cols, kBlockRowMax, [&](auto geo) {

@@ -53,42 +53,71 @@ __device__ __forceinline__ bool beats(float xv, int xc, float yv, int yc) {
     return xv > yv || (xv == yv && xc < yc);
 }
 
-// The best two entries of a set: (v1, c1) before (v2, c2) in the rule's order.
+// The best two entries of a set, (v1, c1) ahead of (v2, c2): larger key, or
+// equal keys and the lower column.  T is float (no NaN: -0 == +0 ties) or an
+// order-preserving uint32 key.
+template <class T>
 struct Top2 {
-    float v1, v2;
+    T v1, v2;
     int c1, c2;
 };
 
+template <class T>
+__device__ __forceinline__ bool ahead(T av, int ac, T bv, int bc) {
+    return av > bv || (av == bv && ac < bc);
+}
+
 // Top2 of two entries, a's column below b's.
-__device__ __forceinline__ Top2 top2_pair(float av, int ac, float bv, int bc) {
-    const bool t = av >= bv;  // equal values: the lower column, a
-    return Top2{t ? av : bv, t ? bv : av, t ? ac : bc, t ? bc : ac};
+template <class T>
+__device__ __forceinline__ Top2<T> top2_pair(T av, int ac, T bv, int bc) {
+    const bool t = av >= bv;  // equal keys: the lower column, a
+    return Top2<T>{t ? av : bv, t ? bv : av, t ? ac : bc, t ? bc : ac};
 }
 
 // Top2 of the union of two disjoint sets; with `ordered` every column of a is
-// below every column of b, so equal values go to a without comparing columns.
-template <bool ordered>
-__device__ __forceinline__ Top2 top2_merge(const Top2& a, const Top2& b) {
-    const bool t = ordered ? a.v1 >= b.v1 : !beats(b.v1, b.c1, a.v1, a.c1);
+// below every column of b, so equal keys go to a without comparing columns.
+template <bool ordered, class T>
+__device__ __forceinline__ Top2<T> top2_merge(const Top2<T>& a, const Top2<T>& b) {
+    const bool t = ordered ? a.v1 >= b.v1 : !ahead(b.v1, b.c1, a.v1, a.c1);
     // the runner-up is the better of the winner's second and the loser's first
-    const float av = t ? a.v2 : a.v1, bv = t ? b.v1 : b.v2;
+    const T av = t ? a.v2 : a.v1, bv = t ? b.v1 : b.v2;
     const int ac = t ? a.c2 : a.c1, bc = t ? b.c1 : b.c2;
-    const bool u = ordered ? av >= bv : !beats(bv, bc, av, ac);
-    return Top2{t ? a.v1 : b.v1, u ? av : bv, t ? a.c1 : b.c1, u ? ac : bc};
+    const bool u = ordered ? av >= bv : !ahead(bv, bc, av, ac);
+    return Top2<T>{t ? a.v1 : b.v1, u ? av : bv, t ? a.c1 : b.c1, u ? ac : bc};
 }
 
-// Top2 of entries [lo, lo + n) of a lane's list (columns increasing along
+// Top2 of entries [lo, lo + N) of a lane's list (columns increasing along
 // it): a tournament of adjacent blocks, so every merge is an ordered one.
-template <int N>
-__device__ __forceinline__ Top2 top2_range(const float* x, const int* c, int lo) {
-    if constexpr (N == 2) {
+// `lowest` is a key no entry is below: the empty runner-up place of a single
+// entry.  The left block takes the larger half, so a single entry is only
+// ever a right block, where a tie with the empty place goes to the real entry
+// on the left.
+template <int N, class T>
+__device__ __forceinline__ Top2<T> top2_range(const T* x, const int* c, int lo, T lowest) {
+    if constexpr (N == 1) {
+        return Top2<T>{x[lo], lowest, c[lo], INT_MAX};
+    } else if constexpr (N == 2) {
         return top2_pair(x[lo], c[lo], x[lo + 1], c[lo + 1]);
-    } else if constexpr (N == 3) {
-        const Top2 a = top2_pair(x[lo], c[lo], x[lo + 1], c[lo + 1]);
-        return top2_merge<true>(a, Top2{x[lo + 2], -INFINITY, c[lo + 2], INT_MAX});
     } else {
-        return top2_merge<true>(top2_range<N / 2>(x, c, lo), top2_range<N - N / 2>(x, c, lo + N / 2));
+        return top2_merge<true>(top2_range<N - N / 2>(x, c, lo, lowest),
+                                top2_range<N / 2>(x, c, lo + N - N / 2, lowest));
     }
+}
+
+// The group's best two: each lane's by the tournament over its E entries in
+// column order, then a butterfly merging the lanes' pairs (disjoint at every
+// round) under the full rule, where an empty place (column INT_MAX) loses
+// every tie; every lane of the group ends with the result.
+template <int LANES, int E, class T>
+__device__ __forceinline__ Top2<T> group_top2(const T (&x)[E], const int (&c)[E], T lowest) {
+    Top2<T> t = top2_range<E>(x, c, 0, lowest);
+#pragma unroll
+    for (int o = LANES / 2; o > 0; o >>= 1) {
+        const Top2<T> u{__shfl_xor_sync(kFullMask, t.v1, o), __shfl_xor_sync(kFullMask, t.v2, o),
+                        __shfl_xor_sync(kFullMask, t.c1, o), __shfl_xor_sync(kFullMask, t.c2, o)};
+        t = top2_merge<false>(t, u);
+    }
+    return t;
 }
 
 __device__ __forceinline__ uint64_t make_key(float x, int col, int cols) {
@@ -253,18 +282,7 @@ __device__ __forceinline__ void kept_select(const float (&v)[NV][VEC], const boo
                 xs[kk * VEC + e] = valid[kk][e] ? v[kk][e] : -INFINITY;
                 cs[kk * VEC + e] = (g + kk * LANES) * VEC + e;
             }
-        Top2 t;
-        if constexpr (E == 1) {
-            t = Top2{xs[0], -INFINITY, cs[0], INT_MAX};
-        } else {
-            t = top2_range<E>(xs, cs, 0);
-        }
-#pragma unroll
-        for (int o = LANES / 2; o > 0; o >>= 1) {
-            const Top2 u{__shfl_xor_sync(kFullMask, t.v1, o), __shfl_xor_sync(kFullMask, t.v2, o),
-                         __shfl_xor_sync(kFullMask, t.c1, o), __shfl_xor_sync(kFullMask, t.c2, o)};
-            t = top2_merge<false>(t, u);
-        }
+        const Top2<float> t = group_top2<LANES, E, float>(xs, cs, -INFINITY);
         const int i1 = t.c1, i2 = k == 1 ? -1 : t.c2;
 #pragma unroll
         for (int kk = 0; kk < NV; ++kk)

@@ -10,7 +10,8 @@
 //
 // top_k_rows: the order is a strict total order on (key, column) with key the
 // order-preserving uint32 of the value, NaN mapped above +inf and -0 onto +0;
-// k <= 2 takes one pass of per-lane best pairs and a butterfly merge, larger k
+// k <= 2 takes a tournament of each lane's entries and a butterfly merge of the
+// lanes' best pairs, larger k
 // takes k rounds that each pick the best remaining key (max for largest, min
 // for smallest) and the lowest column holding it.
 #include "common.cuh"
@@ -227,47 +228,57 @@ top_k_rows_group(const float* __restrict__ x, float* __restrict__ values, float*
             }
         }
         if (k <= 2) {
-            // One pass keeps each lane's best two (key, column) pairs, in the
-            // order "larger key first, then lower column" (keys complemented for
-            // smallest-first); a butterfly merge of the pairs leaves the row's
-            // best two in every lane of the group.  Columns are visited in
-            // increasing order, so a strict comparison keeps the lower column
-            // of equal keys.
+            // Without NaN or infinities in the warp's rows (a finite sum), the
+            // key order is the float order (-0 == +0) and the tournament runs
+            // on the values themselves, negated for smallest-first; the
+            // winners' values come back by negating again, bit for bit.
+            float probe = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) probe += v[kk][e];
+            if (!__any_sync(kFullMask, !(fabsf(probe) <= 3.402823466e38f))) {  // warp-uniform
+                const float sgn = largest ? 1.f : -1.f;
+                constexpr int E = NV * VEC;
+                float xs[E];
+                int cs[E];
+#pragma unroll
+                for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) {
+                        xs[kk * VEC + e] = avail[kk][e] ? sgn * v[kk][e] : -INFINITY;
+                        cs[kk * VEC + e] = (g + kk * LANES) * VEC + e;
+                    }
+                const kept_detail::Top2<float> t = kept_detail::group_top2<LANES, E, float>(xs, cs, -INFINITY);
+                if (live && g == 0) {
+                    values[row * int64_t(k)] = sgn * t.v1;
+                    indices[row * int64_t(k)] = float(t.c1);
+                    if (k == 2) {
+                        values[row * int64_t(k) + 1] = sgn * t.v2;
+                        indices[row * int64_t(k) + 1] = float(t.c2);
+                    }
+                }
+                continue;
+            }
+            // The group's best two (key, column) pairs in the order "larger
+            // key first, then lower column" (keys complemented for
+            // smallest-first): a tournament over each lane's entries in column
+            // order, then a butterfly (kept_core.cuh).  An entry outside the
+            // row counts as key 0 at its own column, above every column of
+            // the row, so it loses every tie and, as k <= cols, is not picked.
             const uint32_t flip = largest ? 0u : 0xffffffffu;
-            uint32_t m1 = 0, m2 = 0;
-            int i1 = INT_MAX, i2 = INT_MAX;  // INT_MAX: empty slot
+            constexpr int E = NV * VEC;
+            uint32_t ks[E];
+            int cs[E];
 #pragma unroll
             for (int kk = 0; kk < NV; ++kk)
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) {
-                    const uint32_t kx = key[kk][e] ^ flip;
-                    const int c = (g + kk * LANES) * VEC + e;
-                    if (avail[kk][e]) {
-                        if (kx > m1 || i1 == INT_MAX) {
-                            m2 = m1; i2 = i1; m1 = kx; i1 = c;
-                        } else if (kx > m2 || i2 == INT_MAX) {
-                            m2 = kx; i2 = c;
-                        }
-                    }
+                    ks[kk * VEC + e] = avail[kk][e] ? key[kk][e] ^ flip : 0u;
+                    cs[kk * VEC + e] = (g + kk * LANES) * VEC + e;
                 }
-            auto before = [](uint32_t ak, int ac, uint32_t bk, int bc) {
-                return ak > bk || (ak == bk && ac < bc);
-            };
-#pragma unroll
-            for (int o = LANES / 2; o > 0; o >>= 1) {
-                const uint32_t om1 = __shfl_xor_sync(kFullMask, m1, o), om2 = __shfl_xor_sync(kFullMask, m2, o);
-                const int oi1 = __shfl_xor_sync(kFullMask, i1, o), oi2 = __shfl_xor_sync(kFullMask, i2, o);
-                if (before(om1, oi1, m1, i1)) {
-                    if (before(om2, oi2, m1, i1)) {
-                        m2 = om2; i2 = oi2;
-                    } else {
-                        m2 = m1; i2 = i1;
-                    }
-                    m1 = om1; i1 = oi1;
-                } else if (before(om1, oi1, m2, i2)) {
-                    m2 = om1; i2 = oi1;
-                }
-            }
+            const kept_detail::Top2<uint32_t> t = kept_detail::group_top2<LANES, E, uint32_t>(ks, cs, 0u);
+            const int i1 = t.c1, i2 = t.c2;
             // The lanes holding the two columns pass their values to the group.
             float v1 = 0.f, v2 = 0.f;
 #pragma unroll

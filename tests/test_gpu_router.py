@@ -191,6 +191,31 @@ def test_top_k_rows_exact(ro, cols, misalign):
             assert _same_bits(host(v), vr.astype(np.float32)), (cols, k, largest)
 
 
+@pytest.mark.parametrize("cols", [1, 2, 3, 8, 33, 64, 100, 256, 1000])
+def test_top_k_rows_top2_ties_and_signed_zeros(ro, cols):
+    # k <= 2: warps whose rows hold no NaN or infinity run the tournament on
+    # the (negated, for smallest) values; the others on the rank keys.  Many
+    # ties and both zeros; then the same rows with a few NaN and infinite rows
+    # mixed in, so warps of both kinds meet.
+    rng = np.random.default_rng(cols + 101)
+    x = (rng.integers(-3, 4, (203, cols)) / 2.0).astype(np.float32)
+    x[x == 0] = np.where(rng.random(int((x == 0).sum())) < 0.5, 0.0, -0.0).astype(np.float32)
+    x[11] = -0.0
+    x[12] = 0.0
+    y = x.copy()
+    y[40, 0] = np.nan
+    y[90, -1] = np.inf
+    y[150, cols // 2] = -np.inf
+    for data in (x, y):
+        for k in sorted({1, min(2, cols)}):
+            for largest in (True, False):
+                for misalign in (False, True):
+                    v, i = ro.rowops_top_k_rows(gpu(data, misalign), k, largest)
+                    vr, ir = oracle.top_k_rows(data, k, largest)
+                    assert np.array_equal(host(i), ir.astype(np.float32)), (cols, k, largest, misalign)
+                    assert _same_bits(host(v), vr.astype(np.float32)), (cols, k, largest, misalign)
+
+
 def test_top_k_rows_router_logits(ro):
     r = inputs.router(1, rows=20000)
     v, i = ro.rowops_top_k_rows(gpu(r["x"]), 2, True)
