@@ -86,3 +86,6 @@ def test_recorded_traffic_follows_the_kernel_sources(tmp_path, monkeypatch):
 def test_link_share():
     got = bench.link_share(2e9, 8, 20.0, {"h2d": 200.0, "d2h": 100.0})
     assert got["link_ms"] == 10.0 and got["frac_of_link"] == 0.5
+    # both directions at once: the longer one
+    got = bench.link_share(2e9, 1.5e9, 20.0, {"h2d": 200.0, "d2h": 100.0})
+    assert got["link_ms"] == 15.0 and got["frac_of_link"] == 0.75
