@@ -575,19 +575,23 @@ ln_bwd_brow(const float* __restrict__ dy, const float* __restrict__ gamma, const
 // every thread issues cp.async copies of exactly those chunks of dy and xhat
 // (the whole block is requested at once, by all threads in parallel), in
 // kLnColsPhases commit groups, and later reads only its own data, so it
-// waits for its own copies and no other thread's.  Per phase: pass A adds the
-// thread's dgamma/dbeta partials for its columns in registers and reduces
-// each row's sums of g' and g'*xhat over the warp, one value per warp into
-// shared memory (with two or more rows a thread, one reduce-scatter of all
-// the rows' sums: 16 shuffles where per-row butterflies take 10 a row); a
-// barrier of the set's warps only (a named barrier per set: the sets share
-// no rows, so one set's late copies do not hold up another's); pass B adds the warps' values in warp order and writes dx (the
-// writes of a phase overlap the loads of the next).  The column partials need no reduction across warps (each column
-// chunk has one owner per set): the sets add theirs in set order and the CTA
-// writes one workspace slot; ln_params_reduce adds the slots in order.  (A
-// single launch that finishes the column sums itself needs a rendezvous of
-// all CTAs, which measured slower on GB300 than this programmatic-dependent
-// second kernel.)
+// waits for its own copies and no other thread's.  Per phase:
+//   pass A  adds the thread's dgamma/dbeta partials for its columns in
+//           registers and reduces each row's sums of g' and g'*xhat over the
+//           warp, one value per warp into shared memory (with two or more
+//           rows a thread, one reduce-scatter of all the rows' sums: 16
+//           shuffles where per-row butterflies take 10 a row);
+//   barrier of the set's warps only (a named barrier per set: the sets share
+//           no rows, so one set's late copies do not hold up another's);
+//   pass B  adds the warps' values of each row in warp order (once per row,
+//           by the set's first warp behind a second set barrier, when the
+//           phase gives a thread two or more rows) and writes dx; the writes
+//           of a phase overlap the loads of the next.
+// The column partials need no reduction across warps (each column chunk has
+// one owner per set): the sets add theirs in set order and the CTA writes one
+// workspace slot; ln_params_reduce adds the slots in order.  (A single launch
+// that finishes the column sums itself needs a rendezvous of all CTAs, which
+// measured slower on GB300 than this programmatic-dependent second kernel.)
 constexpr int kLnColsThreads = 768;
 // Commit groups per thread (on GB300 at 4096 x 768, back to back: one 13.0 us,
 // two 12.7, three 13.4; with the per-set barriers two 12.5-12.8, three 13.7,
@@ -738,15 +742,42 @@ ln_bwd_cols(const float* __restrict__ dy, const float* __restrict__ gamma, const
             }
         }
         set_barrier(h, tp);  // the set's warps' row sums (and, the first time, inv_std) are in shared memory
+        // With two or more rows a thread in the phase (the same for the whole
+        // set), the set's first warp adds the warps' sums of each row (lane
+        // l: row k0 + l) in warp order into the row's first slot, once,
+        // instead of every owner adding them (4096 x 768 on GB300, back to
+        // back: 12.9 -> 12.3 us); with one row the extra barrier costs more.
+        const bool once = k1 - k0 >= 2;
+        if (once) {
+            if (wi == 0 && lane < k1 - k0) {
+                const int j = h + (k0 + lane) * sets;
+                float s1 = 0.f, s2 = 0.f;
+                for (int w = 0; w < wps; ++w) {
+                    s1 += red[(size_t(j) * wps + w) * 2];
+                    s2 += red[(size_t(j) * wps + w) * 2 + 1];
+                }
+                red[size_t(j) * wps * 2] = s1 * inv_cols;
+                red[size_t(j) * wps * 2 + 1] = s2 * inv_cols;
+            }
+            set_barrier(h, tp);
+        }
         for (int k = k0; k < k1; ++k) {  // pass B
             const int j = h + k * sets;
-            float s1 = 0.f, s2 = 0.f;
-            for (int w = 0; w < wps; ++w) {
-                s1 += red[(size_t(j) * wps + w) * 2];
-                s2 += red[(size_t(j) * wps + w) * 2 + 1];
+            float s1, s2;
+            if (once) {
+                const float2 u = reinterpret_cast<const float2*>(red)[size_t(j) * wps];
+                s1 = u.x;
+                s2 = u.y;
+            } else {
+                s1 = 0.f;
+                s2 = 0.f;
+                for (int w = 0; w < wps; ++w) {
+                    s1 += red[(size_t(j) * wps + w) * 2];
+                    s2 += red[(size_t(j) * wps + w) * 2 + 1];
+                }
+                s1 *= inv_cols;
+                s2 *= inv_cols;
             }
-            s1 *= inv_cols;
-            s2 *= inv_cols;
             if (own) {
                 const float r = inv_s[j];
                 const float4 a = sdy[size_t(j) * tp + t], x = sxh[size_t(j) * tp + t];
