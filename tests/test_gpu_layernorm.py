@@ -54,6 +54,20 @@ def test_layernorm_bwd_row_blocks(ro, rows, cols):
     _run(ro, inputs.layernorm(rows * 7 + cols, rows=rows, cols=cols))
 
 
+@pytest.mark.parametrize("per_sm", [2, 3, 5, 9, 13, 16])
+@pytest.mark.parametrize("cols", [384, 512, 768, 1000])
+def test_layernorm_bwd_column_owner_phases(ro, per_sm, cols):
+    # rows of 384..1024 floats whose CTA block fits in shared memory: each row
+    # set's threads take one to eight rows a phase, so the phases alternate
+    # between the per-row butterfly and the reduce-scatter, and between the
+    # inline sum of the warps' row sums and the once-per-row sum (sets of one
+    # CTA differ by a row, so they differ there too); a ragged count leaves
+    # the last CTA short
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for rows in (sms * per_sm, sms * per_sm - 77):
+        _run(ro, inputs.layernorm(rows + cols, rows=rows, cols=cols))
+
+
 @pytest.mark.parametrize("rows,cols", [(2000, 2048), (700, 4100), (333, 8192), (400, 16384), (300, 30001)])
 @pytest.mark.parametrize("misalign", [False, True])
 def test_layernorm_block_rows_many_rows_per_cta(ro, rows, cols, misalign):
