@@ -579,8 +579,9 @@ ln_bwd_brow(const float* __restrict__ dy, const float* __restrict__ gamma, const
 //   pass A  adds the thread's dgamma/dbeta partials for its columns in
 //           registers and reduces each row's sums of g' and g'*xhat over the
 //           warp, one value per warp into shared memory (with two or more
-//           rows a thread, one reduce-scatter of all the rows' sums: 16
-//           shuffles where per-row butterflies take 10 a row);
+//           rows a thread, one reduce-scatter of all the rows' sums,
+//           ln_cols_pass_a: 6, 9 or 16 shuffles for 2, up to 4 or up to 8
+//           rows, where per-row butterflies take 10 a row);
 //   barrier of the set's warps only (a named barrier per set: the sets share
 //           no rows, so one set's late copies do not hold up another's);
 //   pass B  adds the warps' values of each row in warp order (once per row,
@@ -618,6 +619,63 @@ __device__ __forceinline__ void cp_async_wait_pending(int n) {
         case 2: asm volatile("cp.async.wait_group 2;\n" ::: "memory"); break;
         default: asm volatile("cp.async.wait_group 3;\n" ::: "memory"); break;
     }
+}
+
+// Pass A of ln_bwd_cols over 2..NR rows k0..k1-1 of this thread: the dgamma /
+// dbeta partials of its columns, and the rows' 2*NR sums of g' and g'*xhat
+// reduce-scattered over the warp.  Each round halves the values a lane holds
+// (rounds at lane distances 16, 8, ... while values remain, then a butterfly
+// over the rest), so every sum meets the same addition tree as a butterfly of
+// its own at distances 16, 8, 4, 2, 1, bit for bit, in 2*NR - 1 + log2(NR) + 1
+// shuffles instead of 10 a row.  Lanes 32/(2*NR)*m .. hold value m (row m / 2,
+// sum m % 2); the first of them stores it as the warp's value for the row.
+template <int NR>
+__device__ __forceinline__ void ln_cols_pass_a(const float4* sdy, const float4* sxh, float* red, float4 g,
+                                               float4& pg, float4& pb, int h, int t, int tp, int sets, int wps,
+                                               int wi, int lane, bool own, int k0, int k1) {
+    float v[2 * NR];
+#pragma unroll
+    for (int i = 0; i < 2 * NR; ++i) v[i] = 0.f;
+#pragma unroll
+    for (int i = 0; i < NR; ++i) {
+        const int k = k0 + i;
+        if (own && k < k1) {
+            const int j = h + k * sets;
+            const float4 a = sdy[size_t(j) * tp + t], x = sxh[size_t(j) * tp + t];
+            pg.x = fmaf(a.x, x.x, pg.x);
+            pg.y = fmaf(a.y, x.y, pg.y);
+            pg.z = fmaf(a.z, x.z, pg.z);
+            pg.w = fmaf(a.w, x.w, pg.w);
+            pb.x += a.x;
+            pb.y += a.y;
+            pb.z += a.z;
+            pb.w += a.w;
+            const float gx = a.x * g.x, gy = a.y * g.y, gz = a.z * g.z, gw = a.w * g.w;
+            float s2 = 0.f;
+            s2 = fmaf(gx, x.x, s2);
+            s2 = fmaf(gy, x.y, s2);
+            s2 = fmaf(gz, x.z, s2);
+            s2 = fmaf(gw, x.w, s2);
+            v[2 * i] = (gx + gy) + (gz + gw);
+            v[2 * i + 1] = s2;
+        }
+    }
+    int o = 16;
+#pragma unroll
+    for (int half = NR; half >= 1; half >>= 1, o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+            const float send = up ? v[i] : v[i + half];
+            const float keep = up ? v[i + half] : v[i];
+            v[i] = keep + __shfl_xor_sync(kFullMask, send, o);
+        }
+    }
+#pragma unroll
+    for (; o >= 1; o >>= 1) v[0] += __shfl_xor_sync(kFullMask, v[0], o);
+    constexpr int kSpan = 32 / (2 * NR);  // lanes holding each value
+    const int m = (lane / kSpan) & (2 * NR - 1);
+    if (lane % kSpan == 0 && (m >> 1) < k1 - k0) red[(size_t(h + (k0 + (m >> 1)) * sets) * wps + wi) * 2 + (m & 1)] = v[0];
 }
 
 __global__ void __launch_bounds__(kLnColsThreads, 1)
@@ -663,52 +721,12 @@ ln_bwd_cols(const float* __restrict__ dy, const float* __restrict__ gamma, const
         cp_async_wait_pending(P - 1 - p);  // this phase's rows have landed
         const int k0 = p * K / P, k1 = (p + 1) * K / P;
         if (k1 - k0 >= 2) {  // warp-uniform (a warp lies in one set)
-            // Pass A over up to 8 rows of this thread: their 16 sums are
-            // reduce-scattered over the warp (16 shuffles in all, the same
-            // addition tree as a butterfly per sum).
-            float v[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = 0.f;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int k = k0 + i;
-                if (own && k < k1) {
-                    const int j = h + k * sets;
-                    const float4 a = sdy[size_t(j) * tp + t], x = sxh[size_t(j) * tp + t];
-                    pg.x = fmaf(a.x, x.x, pg.x);
-                    pg.y = fmaf(a.y, x.y, pg.y);
-                    pg.z = fmaf(a.z, x.z, pg.z);
-                    pg.w = fmaf(a.w, x.w, pg.w);
-                    pb.x += a.x;
-                    pb.y += a.y;
-                    pb.z += a.z;
-                    pb.w += a.w;
-                    const float gx = a.x * g.x, gy = a.y * g.y, gz = a.z * g.z, gw = a.w * g.w;
-                    float s2 = 0.f;
-                    s2 = fmaf(gx, x.x, s2);
-                    s2 = fmaf(gy, x.y, s2);
-                    s2 = fmaf(gz, x.z, s2);
-                    s2 = fmaf(gw, x.w, s2);
-                    v[2 * i] = (gx + gy) + (gz + gw);
-                    v[2 * i + 1] = s2;
-                }
-            }
-            // Each round halves the values a lane holds; lanes 2m and 2m + 1
-            // end with the warp's total of value m (row m / 2, sum m % 2).
-#pragma unroll
-            for (int half = 8, o = 16; half >= 1; half >>= 1, o >>= 1) {
-                const bool up = (lane & o) != 0;
-#pragma unroll
-                for (int i = 0; i < half; ++i) {
-                    const float send = up ? v[i] : v[i + half];
-                    const float keep = up ? v[i + half] : v[i];
-                    v[i] = keep + __shfl_xor_sync(kFullMask, send, o);
-                }
-            }
-            v[0] += __shfl_xor_sync(kFullMask, v[0], 1);
-            const int m = (lane >> 1) & 15;
-            if ((lane & 1) == 0 && (m >> 1) < k1 - k0)
-                red[(size_t(h + (k0 + (m >> 1)) * sets) * wps + wi) * 2 + (m & 1)] = v[0];
+            if (k1 - k0 == 2)
+                ln_cols_pass_a<2>(sdy, sxh, red, g, pg, pb, h, t, tp, sets, wps, wi, lane, own, k0, k1);
+            else if (k1 - k0 <= 4)
+                ln_cols_pass_a<4>(sdy, sxh, red, g, pg, pb, h, t, tp, sets, wps, wi, lane, own, k0, k1);
+            else
+                ln_cols_pass_a<8>(sdy, sxh, red, g, pg, pb, h, t, tp, sets, wps, wi, lane, own, k0, k1);
         } else {  // one row or none: a butterfly per sum
             for (int k = k0; k < k1; ++k) {  // pass A
                 const int j = h + k * sets;
