@@ -231,8 +231,10 @@ int rowops_layernorm_bwd(const float *dy, const float *gamma, const float *xhat,
  *   - Each CTA's partial sums take 8 * cols bytes.  Rows of up to 1024 floats
  *     fit for every row count: the launch uses only as many CTAs as the array
  *     holds partials for (rows of 863..1024 floats then run on fewer CTAs
- *     than rowops_layernorm_bwd uses, so dgamma and dbeta are added in another
- *     order; dx is the same).  Wider rows fit while rows is small enough
+ *     than rowops_layernorm_bwd uses where a CTA's rows fit in shared memory,
+ *     so dgamma and dbeta are added in another order and dx may come from the
+ *     other stage-1 kernel; both agree with rowops_layernorm_bwd within the
+ *     parity bounds).  Wider rows fit while rows is small enough
  *     (e.g. 64 rows of 2048 floats, 8 rows of 16384); larger shapes are
  *     refused with ROWOPS_ERR_WORKSPACE.
  *   - All calls on a device share the one array, and it keeps the contents of

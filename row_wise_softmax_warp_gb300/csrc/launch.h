@@ -136,8 +136,9 @@ uint32_t pipeline_timeouts_rows();
 uint32_t pipeline_timeouts_pairs();
 uint32_t pipeline_timeouts_ln();
 // LayerNorm backward stage 1 on rows of 384..1024 floats on 16-byte
-// boundaries through the bulk-copy ring (one CTA per SM, at most max_ctas,
-// 0: no limit); writes ln_bwd_tma_ctas(rows, cols, max_ctas) partials to ws.
+// boundaries through the bulk-copy ring (one CTA per SM, at most 2^17 / cols
+// and at most max_ctas, 0: no further limit); writes
+// ln_bwd_tma_ctas(rows, cols, max_ctas) partials to ws.
 // ln_bwd_tma_ctas is 0 for shapes it does not take.
 int64_t ln_bwd_tma_ctas(int64_t rows, int64_t cols, int64_t max_ctas);
 bool launch_ln_bwd_tma(const float* dy, const float* gamma, const float* xhat, const float* inv_std, float* dx,
