@@ -272,17 +272,30 @@ __device__ __forceinline__ void kept_select(const float (&v)[NV][VEC], const boo
         // tie); then a butterfly merges the lanes' pairs under the full rule,
         // and every lane ends with the row's best two.  A row has at least
         // k entries, so no entry outside it is picked.
+        // (When the row fills every lane's entries, no entry lies outside it
+        // and the substitution is skipped: a row past the last one is not
+        // stored.)
         constexpr int E = NV * VEC;
         float xs[E];
         int cs[E];
 #pragma unroll
         for (int kk = 0; kk < NV; ++kk)
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                xs[kk * VEC + e] = valid[kk][e] ? v[kk][e] : -INFINITY;
-                cs[kk * VEC + e] = (g + kk * LANES) * VEC + e;
-            }
-        const Top2<float> t = group_top2<LANES, E, float>(xs, cs, -INFINITY);
+            for (int e = 0; e < VEC; ++e) cs[kk * VEC + e] = (g + kk * LANES) * VEC + e;
+        Top2<float> t;
+        if (cols == LANES * E) {  // warp-uniform
+#pragma unroll
+            for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) xs[kk * VEC + e] = v[kk][e];
+            t = group_top2<LANES, E, float>(xs, cs, -INFINITY);
+        } else {
+#pragma unroll
+            for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) xs[kk * VEC + e] = valid[kk][e] ? v[kk][e] : -INFINITY;
+            t = group_top2<LANES, E, float>(xs, cs, -INFINITY);
+        }
         const int i1 = t.c1, i2 = k == 1 ? -1 : t.c2;
 #pragma unroll
         for (int kk = 0; kk < NV; ++kk)

@@ -245,11 +245,21 @@ top_k_rows_group(const float* __restrict__ x, float* __restrict__ values, float*
 #pragma unroll
                 for (int kk = 0; kk < NV; ++kk)
 #pragma unroll
-                    for (int e = 0; e < VEC; ++e) {
-                        xs[kk * VEC + e] = avail[kk][e] ? sgn * v[kk][e] : -INFINITY;
-                        cs[kk * VEC + e] = (g + kk * LANES) * VEC + e;
-                    }
-                const kept_detail::Top2<float> t = kept_detail::group_top2<LANES, E, float>(xs, cs, -INFINITY);
+                    for (int e = 0; e < VEC; ++e) cs[kk * VEC + e] = (g + kk * LANES) * VEC + e;
+                kept_detail::Top2<float> t;
+                if (cols == LANES * E) {  // every entry in the row (warp-uniform; rows past the last are not stored)
+#pragma unroll
+                    for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e) xs[kk * VEC + e] = sgn * v[kk][e];
+                    t = kept_detail::group_top2<LANES, E, float>(xs, cs, -INFINITY);
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e) xs[kk * VEC + e] = avail[kk][e] ? sgn * v[kk][e] : -INFINITY;
+                    t = kept_detail::group_top2<LANES, E, float>(xs, cs, -INFINITY);
+                }
                 if (live && g == 0) {
                     values[row * int64_t(k)] = sgn * t.v1;
                     indices[row * int64_t(k)] = float(t.c1);
