@@ -579,7 +579,17 @@ def gpu_leg(args):
     table = ops.table()
     abytes = algorithmic_bytes()
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    clean = torch.ones(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    sink = torch.empty((), dtype=torch.int64, device=dev)
     stream = torch.cuda.current_stream(dev)
+
+    def flush_l2():
+        # A write larger than the L2 evicts the previous op's data (written
+        # back here); a read larger than the L2 then leaves it holding only
+        # clean lines, so the op's events do not include writing back the
+        # flush (on GB300 up to 126 MB: logsumexp 247.5 -> 232.4 us).
+        flush.zero_()
+        torch.sum(clean.view(torch.int64), 0, out=sink)
 
     uuid = None
     try:
@@ -592,7 +602,7 @@ def gpu_leg(args):
 
     for _ in range(args.warmup):
         for _, fn in table:
-            flush.zero_()
+            flush_l2()
             fn()
     torch.cuda.synchronize()
 
@@ -607,7 +617,7 @@ def gpu_leg(args):
     outer0.record(stream)
     for k in range(K):
         for name, fn in table:
-            flush.zero_()
+            flush_l2()
             starts[name][k].record(stream)
             fn()
             ends[name][k].record(stream)
@@ -619,17 +629,35 @@ def gpu_leg(args):
     step_ms_local = sum(per_op_ms.values())
     wall_ms_local = outer0.elapsed_time(outer1) / K
 
+    # The same ops after the write alone (the flush's dirty lines are then
+    # written back inside each op's events), for comparison.
+    kd = max(3, min(K, 20))
+    dirty_ev = []
+    for _ in range(kd):
+        for name, fn in table:
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            dirty_ev.append((name, a, b))
+    torch.cuda.synchronize()
+    dirty_ms = {n: 0.0 for n, _ in table}
+    for name, a, b in dirty_ev:
+        dirty_ms[name] += a.elapsed_time(b) / kd
+    dirty_step_ms_local = sum(dirty_ms.values())
+
     # ------------------------------------------- ops beyond the step
     nxt = ops.next_table()
     for _, fn in nxt:
         for _ in range(3):
-            flush.zero_()
+            flush_l2()
             fn()
     next_ms = {}
     for name, fn in nxt:
         ts = []
         for _ in range(max(5, min(K, 20))):
-            flush.zero_()
+            flush_l2()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             fn()
@@ -661,11 +689,11 @@ def gpu_leg(args):
                 fn()
         stream.wait_stream(cap)
         for _ in range(3):
-            flush.zero_()
+            flush_l2()
             graph.replay()
         ts = []
         for _ in range(max(5, min(K, 20))):
-            flush.zero_()
+            flush_l2()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             graph.replay()
@@ -690,6 +718,7 @@ def gpu_leg(args):
     clocks.stop()
 
     step_ms = max_over_ranks(step_ms_local, dist, dev)
+    dirty_step_ms = max_over_ranks(dirty_step_ms_local, dist, dev)
     e2e_ms = max_over_ranks(e2e_ms_local, dist, dev)
     all_ms = max_over_ranks(all_ms_local, dist, dev)
     wall_ms = max_over_ranks(wall_ms_local, dist, dev)
@@ -740,7 +769,9 @@ def gpu_leg(args):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic (seeded numpy PCG64, the five workloads' distributions)",
-        "config": {"workload": WORKLOAD, "l2": "flushed before every op (512 MiB device write), outside the op's events",
+        "config": {"workload": WORKLOAD,
+                   "l2": "flushed before every op, outside the op's events: a 512 MiB device write, then a "
+                         "512 MiB read, so the L2 holds only clean lines when the op starts",
                    "ms_per_step_incl_flushes": round(wall_ms, 4), "parallelism": f"replicas x{world} (rows independent)"},
         "roofline": roofline,
         "ops": breakdown,
@@ -770,6 +801,12 @@ def gpu_leg(args):
                              "note": "every op's inputs uploaded and every output read back, per op",
                              **link_share(all_h2d, all_d2h, all_ms, link)},
         "clocks": clocks.summary(),
+        "l2_write_only_flush": {
+            "ms_per_step": round(dirty_step_ms, 5),
+            "GB/s": round(world * total_bytes / (dirty_step_ms * 1e-3) / 1e9, 1),
+            "ops_ms": {n: round(v, 5) for n, v in dirty_ms.items()},
+            "note": "the same ops after the 512 MiB write alone: each op's events then also include "
+                    "writing back the dirty lines the flush left in the L2"},
     }
     if graph_step is not None and "ms" in graph_step:
         gms = graph_step["ms"]
