@@ -50,6 +50,26 @@ def test_teacher_ce(ro, cols, misalign):
     assert torch.equal(rl2, rl)
 
 
+@pytest.mark.parametrize("rows,cols", [(1, 132), (151, 260), (33, 512), (4096, 768), (5000, 768), (300, 772),
+                                       (153, 1020), (7000, 1024)])
+def test_ce_variants_warp_rows(ro, rows, cols):
+    # Rows of 129..1024 floats on 16-byte boundaries: a warp a row with the
+    # second input staged in shared memory; one wave, or warps that walk
+    # further rows (more than a CTA's warps per SM), ragged last CTAs.
+    x, w, t = _inputs(rows, cols, rows + cols)
+    g, rl, ml = ro.rowops_soft_ce(gpu(x), gpu(w), grad_scale=1.0 / rows)
+    gr, rlr, mlr = oracle.soft_ce(x, w, 1.0 / rows)
+    wsum = np.abs(w.astype(np.float64)).sum(axis=1, keepdims=True)
+    check_abs(host(g), gr, 2e-6 * (1.0 / rows) * np.maximum(1.0, wsum), f"soft ce grad {rows}x{cols}")
+    scale = np.maximum(1.0, np.abs(w.astype(np.float64)).sum(axis=1) * (np.abs(x).max(axis=1) + 10))
+    check_abs(host(rl), rlr, 1e-5 * scale, f"soft ce loss {rows}x{cols}")
+    g, rl, ml = ro.rowops_teacher_ce(gpu(x), gpu(t), grad_scale=1.0 / rows)
+    gr, rlr, mlr = oracle.teacher_ce(x, t, 1.0 / rows)
+    check_abs(host(g), gr, 4e-6 / rows, f"teacher grad {rows}x{cols}")
+    check_rel(host(rl), rlr, f"teacher loss {rows}x{cols}")
+    check_rel(host(ml), [mlr], "teacher mean")
+
+
 def test_soft_ce_one_hot_matches_integer_targets(ro):
     rng = np.random.default_rng(9)
     x = rng.normal(0, 2, (64, 50304)).astype(np.float32)
