@@ -9,14 +9,16 @@
 // never read back from HBM (13 bytes per element instead of 9 + 8).
 //
 // top_k_rows: the order is a strict total order on (key, column) with key the
-// order-preserving uint32 of the value, NaN mapped above +inf and -0 onto +0;
-// k <= 2 takes a tournament of each lane's entries and a butterfly merge of the
-// lanes' best pairs, larger k
-// takes k rounds that each pick the best remaining key (max for largest, min
-// for smallest) and the lowest column holding it.
+// order-preserving uint32 of the value, NaN mapped above +inf and -0 onto +0.
+// k <= 2 takes a tournament of each lane's (or, on rows of more than 1024
+// floats, each thread's) entries and butterfly merges of the best pairs; on
+// rows of up to 1024 floats larger k takes candidates or k rounds that each
+// pick the best remaining key (max for largest, min for smallest) and the
+// lowest column holding it; longer rows with larger k the select kernel.
 #include "common.cuh"
 #include "kept_core.cuh"
 #include "launch.h"
+
 
 namespace rowops {
 namespace {
@@ -442,6 +444,150 @@ top_k_rows_rowblock(const float* __restrict__ x, float* __restrict__ values, flo
     }
 }
 
+// Rows of more than 1024 floats with k <= 2: one pass.  One CTA per row
+// (rows blockIdx.x, + gridDim.x, ...); each thread keeps the best two of its
+// chunks (chunks c = tid, tid + NT, ...: a tournament inside each float4
+// chunk, then an ordered merge into the running pair, whose columns are all
+// lower), then a butterfly over the warp and one over the warps' pairs in
+// shared memory.  Without NaN or infinity in the row (a finite sum of its
+// values, block-wide) the ranking runs on the values themselves, negated for
+// smallest-first; otherwise the row is ranked again, from the L2, on the rank
+// keys (NaN above every number), and the winners' values re-read.
+template <class T, int VEC>
+__device__ __forceinline__ kept_detail::Top2<T> top2_chunk(const T (&v)[VEC], int col0, T lowest) {
+    int cs[VEC];
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) cs[e] = col0 + e;
+    return kept_detail::top2_range<VEC, T>(v, cs, 0, lowest);
+}
+
+// The block's best two of each thread's pair t (every thread calls it;
+// shared arrays of NT/32 pairs); returns it in every thread.
+template <int NT, class T>
+__device__ __forceinline__ kept_detail::Top2<T> block_top2(kept_detail::Top2<T> t, T lowest, T* sv, int* sc) {
+    using kept_detail::Top2;
+    constexpr int W = NT / 32;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const Top2<T> u{__shfl_xor_sync(kFullMask, t.v1, o), __shfl_xor_sync(kFullMask, t.v2, o),
+                        __shfl_xor_sync(kFullMask, t.c1, o), __shfl_xor_sync(kFullMask, t.c2, o)};
+        t = kept_detail::top2_merge<false>(t, u);
+    }
+    __syncthreads();  // the previous use of the shared pairs is over
+    if (lane == 0) {
+        sv[2 * wid] = t.v1;
+        sv[2 * wid + 1] = t.v2;
+        sc[2 * wid] = t.c1;
+        sc[2 * wid + 1] = t.c2;
+    }
+    __syncthreads();
+    t = lane < W ? Top2<T>{sv[2 * lane], sv[2 * lane + 1], sc[2 * lane], sc[2 * lane + 1]}
+                 : Top2<T>{lowest, lowest, INT_MAX, INT_MAX};
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const Top2<T> u{__shfl_xor_sync(kFullMask, t.v1, o), __shfl_xor_sync(kFullMask, t.v2, o),
+                        __shfl_xor_sync(kFullMask, t.c1, o), __shfl_xor_sync(kFullMask, t.c2, o)};
+        t = kept_detail::top2_merge<false>(t, u);
+    }
+    return t;
+}
+
+template <int NT, int VEC>
+__global__ void __launch_bounds__(NT)
+top_k_rows_top2(const float* __restrict__ x, float* __restrict__ values, float* __restrict__ indices,
+                int64_t rows, int cols, int k, int largest) {
+    using kept_detail::Top2;
+    constexpr int U = 4;  // chunks in flight per thread
+    __shared__ float fv[2 * (NT / 32)];
+    __shared__ uint32_t kv[2 * (NT / 32)];
+    __shared__ int cv[2 * (NT / 32)];
+    const int tid = threadIdx.x;
+    const float sgn = largest ? 1.f : -1.f;
+    const uint32_t flip = largest ? 0u : 0xffffffffu;
+    const int nch = cols / VEC;
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const float* xr = x + row * int64_t(cols);
+        Top2<float> t{-INFINITY, -INFINITY, INT_MAX, INT_MAX};  // no entry yet
+        bool first = true;
+        float probe = 0.f;
+        for (int c0 = 0; c0 < nch; c0 += U * NT) {  // block-uniform
+            float v[U][VEC];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int c = c0 + u * NT + tid;
+                if (c < nch) ld_chunk<VEC>(xr + c * VEC, v[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int c = c0 + u * NT + tid;
+                if (c < nch) {
+                    float xs[VEC];
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) {
+                        probe += v[u][e];
+                        xs[e] = sgn * v[u][e];
+                    }
+                    const Top2<float> ct = top2_chunk<float, VEC>(xs, c * VEC, -INFINITY);
+                    // a whole float4 chunk fills both places, so the running
+                    // pair is always complete and the merge can be ordered;
+                    // single entries merge under the full rule
+                    if constexpr (VEC >= 2) t = first ? ct : kept_detail::top2_merge<true>(t, ct);
+                    else t = first ? ct : kept_detail::top2_merge<false>(t, ct);
+                    first = false;
+                }
+            }
+        }
+        float* vr = values + row * int64_t(k);
+        float* ir = indices + row * int64_t(k);
+        if (!__syncthreads_or(!(fabsf(probe) <= 3.402823466e38f))) {  // block-uniform
+            t = block_top2<NT, float>(t, -INFINITY, fv, cv);
+            if (tid == 0) {
+                vr[0] = sgn * t.v1;
+                ir[0] = float(t.c1);
+                if (k == 2) {
+                    vr[1] = sgn * t.v2;
+                    ir[1] = float(t.c2);
+                }
+            }
+            continue;
+        }
+        // NaN or infinity in the row: rank keys, the row again from the L2
+        Top2<uint32_t> tk{0u, 0u, INT_MAX, INT_MAX};
+        first = true;
+        for (int c0 = 0; c0 < nch; c0 += U * NT) {
+            float v[U][VEC];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int c = c0 + u * NT + tid;
+                if (c < nch) ld_chunk<VEC>(xr + c * VEC, v[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int c = c0 + u * NT + tid;
+                if (c < nch) {
+                    uint32_t ks[VEC];
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) ks[e] = rank_key(v[u][e]) ^ flip;
+                    const Top2<uint32_t> ct = top2_chunk<uint32_t, VEC>(ks, c * VEC, 0u);
+                    if constexpr (VEC >= 2) tk = first ? ct : kept_detail::top2_merge<true>(tk, ct);
+                    else tk = first ? ct : kept_detail::top2_merge<false>(tk, ct);
+                    first = false;
+                }
+            }
+        }
+        tk = block_top2<NT, uint32_t>(tk, 0u, kv, cv);
+        if (tid == 0) {
+            vr[0] = xr[tk.c1];
+            ir[0] = float(tk.c1);
+            if (k == 2) {
+                vr[1] = xr[tk.c2];
+                ir[1] = float(tk.c2);
+            }
+        }
+    }
+}
+
 // Rows of more than 1024 floats with 2 <= k <= kSelectMaxK.  One CTA per row
 // (rows blockIdx.x, + gridDim.x, ...; NT = 256 threads and 4 CTAs per SM for
 // rows of up to 8192 floats, 512 threads and 2 CTAs per SM beyond, so that
@@ -744,7 +890,22 @@ cudaError_t launch_top_k_rows(const float* x, float* values, float* indices, int
     });
     cudaError_t err = cudaSuccess;
     const int sms = sm_count();
-    if (!done && k >= 2 && k <= kSelectMaxK && sms > 0) {
+    if (!done && k <= 2 && sms > 0) {
+        // as many CTAs of 256 threads as are resident (on GB300, 2048 x 50304,
+        // k = 2, back to back: 256 threads 69.6 us, 128 71.9, 512 82.4, 1024
+        // 101.6; the two-pass select took 183)
+        auto launch = [&](auto kern) {
+            int per_sm = 0;
+            constexpr int nt = 256;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, nt, 0) != cudaSuccess || per_sm < 1)
+                per_sm = 1;
+            const int64_t cap = int64_t(sms) * per_sm;
+            kern<<<unsigned(rows < cap ? rows : cap), nt, 0, stream>>>(x, values, indices, rows, int(cols),
+                                                                        int(k), largest ? 1 : 0);
+        };
+        if (vec4) launch(top_k_rows_top2<256, 4>);
+        else launch(top_k_rows_top2<256, 1>);
+    } else if (!done && k >= 2 && k <= kSelectMaxK && sms > 0) {
         auto launch = [&](auto kern, int nt, int per_sm) {
             const int64_t cap = int64_t(sms) * per_sm;
             const unsigned grid = unsigned(rows < cap ? rows : cap);

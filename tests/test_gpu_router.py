@@ -243,6 +243,32 @@ def test_top_k_rows_long_rows(ro, rows, cols, misalign):
             assert _same_bits(host(v), vr.astype(np.float32)), (cols, k, largest)
 
 
+@pytest.mark.parametrize("rows,cols", [(37, 1025), (5, 50304), (300, 3001), (2, 131072), (700, 4096)])
+@pytest.mark.parametrize("misalign", [False, True])
+def test_top_k_rows_long_rows_top2(ro, rows, cols, misalign):
+    # rows of more than 1024 floats with k <= 2: one pass on the values where a
+    # row holds no NaN or infinity, the rank keys again from the L2 where it
+    # does; ties and both zeros (values on a coarse grid), a few NaN and
+    # infinite rows among finite ones
+    rng = np.random.default_rng(rows * 7 + cols)
+    x = (rng.normal(0, 2, (rows, cols)) * 2).round().astype(np.float32) / 2
+    x[x == 0] = np.where(rng.random(int((x == 0).sum())) < 0.5, 0.0, -0.0).astype(np.float32)
+    y = x.copy()
+    y[0, cols // 3] = np.nan
+    y[-1, -1] = np.inf
+    if rows > 2:
+        y[1, 5] = -np.inf
+        y[1, 6] = np.nan
+    for data in (x, y):
+        xg = gpu(data, misalign)
+        for k in (1, 2):
+            for largest in (True, False):
+                v, i = ro.rowops_top_k_rows(xg, k, largest)
+                vr, ir = oracle.top_k_rows(data, k, largest)
+                assert np.array_equal(host(i), ir.astype(np.float32)), (rows, cols, k, largest, misalign)
+                assert _same_bits(host(v), vr.astype(np.float32)), (rows, cols, k, largest, misalign)
+
+
 @pytest.mark.parametrize("cols", [16, 64, 100, 128, 256, 512, 1000, 1024])
 @pytest.mark.parametrize("k", [3, 4, 8, 16, 32])
 def test_kept_candidates(ro, cols, k):
