@@ -202,6 +202,34 @@ __device__ __forceinline__ bool kept_by_candidates(const float (&v)[NV][VEC], co
 
 }  // namespace kept_detail
 
+// k <= 2 on a row that fills every lane's entries, with no NaN in the warp's
+// rows: the row's best two by group_top2, then zeros over the whole row and
+// 1.0 at the one or two winning columns, each stored by the lane that wrote
+// that column's chunk (in that order, so the 1.0 lands last): the same mask as
+// kept_select, without a comparison per entry.  kr is the row's mask, written
+// only when `live`.  Every lane of the warp must call it.
+template <int LANES, int NV, int VEC>
+__device__ __forceinline__ void kept_store_top2_full(const float (&v)[NV][VEC], int k, bool live, float* kr) {
+    const int g = threadIdx.x % LANES;
+    constexpr int E = NV * VEC;
+    float xs[E];
+    int cs[E];
+#pragma unroll
+    for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+            xs[kk * VEC + e] = v[kk][e];
+            cs[kk * VEC + e] = (g + kk * LANES) * VEC + e;
+        }
+    const kept_detail::Top2<float> t = kept_detail::group_top2<LANES, E, float>(xs, cs, -INFINITY);
+    if (live) {
+#pragma unroll
+        for (int kk = 0; kk < NV; ++kk) st_zero_chunk<VEC>(kr + (g + kk * LANES) * VEC);
+        if ((t.c1 / VEC) % LANES == g) kr[t.c1] = 1.f;
+        if (k == 2 && (t.c2 / VEC) % LANES == g) kr[t.c2] = 1.f;
+    }
+}
+
 // Loads row `row` into a group's registers (zeros outside the row or past the
 // last row); read-only input.
 template <int LANES, int NV, int VEC>

@@ -86,9 +86,13 @@ router_group(const float* x, const uint8_t* __restrict__ mask, float* p, float* 
             if (live && c < nch) st_chunk<VEC>(p + off + c * VEC, v[kk]);
         }
         // Top-k kept mask of those probabilities.
+        const bool any_nan = __any_sync(kFullMask, !(fabsf(probe) <= 3.402823466e38f));
+        if (k <= 2 && !any_nan && cols == LANES * NV * VEC) {  // warp-uniform
+            kept_store_top2_full<LANES, NV, VEC>(v, k, live, kept + off);
+            continue;
+        }
         bool keep[NV][VEC];
-        kept_select<LANES, NV, VEC>(v, valid, __any_sync(kFullMask, !(fabsf(probe) <= 3.402823466e38f)), cols,
-                                    k, keep, &kscratch[threadIdx.x >> 5]);
+        kept_select<LANES, NV, VEC>(v, valid, any_nan, cols, k, keep, &kscratch[threadIdx.x >> 5]);
 #pragma unroll
         for (int kk = 0; kk < NV; ++kk) {
             const int c = g + kk * LANES;

@@ -47,11 +47,15 @@ kept_group(const float* __restrict__ x, float* __restrict__ kept, int64_t rows, 
                 valid[kk][e] = live && g + kk * LANES < nch;
                 probe += v[kk][e];
             }
-        bool keep[NV][VEC];
         // A non-finite sum (NaN, or infinities / overflow) sends the warp to the
         // literal count, which is exact for every input.
-        kept_select<LANES, NV, VEC>(v, valid, __any_sync(kFullMask, !(fabsf(probe) <= 3.402823466e38f)), cols,
-                                    k, keep, &kscratch[threadIdx.x >> 5]);
+        const bool any_nan = __any_sync(kFullMask, !(fabsf(probe) <= 3.402823466e38f));
+        if (k <= 2 && !any_nan && cols == LANES * NV * VEC) {  // warp-uniform
+            kept_store_top2_full<LANES, NV, VEC>(v, k, live, kept + off);
+            continue;
+        }
+        bool keep[NV][VEC];
+        kept_select<LANES, NV, VEC>(v, valid, any_nan, cols, k, keep, &kscratch[threadIdx.x >> 5]);
 #pragma unroll
         for (int kk = 0; kk < NV; ++kk) {
             const int c = g + kk * LANES;
