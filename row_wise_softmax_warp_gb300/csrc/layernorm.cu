@@ -592,9 +592,9 @@ ln_bwd_brow(const float* __restrict__ dy, const float* __restrict__ gamma, const
 // one owner per set): the sets add theirs in set order (handed to set 0 as
 // soon as their last pass A is done, where shared memory has room for them
 // beside the rows) and the CTA writes one workspace slot; ln_params_reduce
-// adds the slots in order.  (A single launch
-// that finishes the column sums itself needs a rendezvous of all CTAs, which
-// measured slower on GB300 than this programmatic-dependent second kernel.)
+// adds the slots in order.  (A single launch that finishes the column sums
+// itself needs a rendezvous of all CTAs, which measured slower on GB300 than
+// this programmatic-dependent second kernel.)
 constexpr int kLnColsThreads = 768;
 // Commit groups per thread (on GB300 at 4096 x 768, back to back: one 13.0 us,
 // two 12.7, three 13.4; with the per-set barriers two 12.5-12.8, three 13.7,
@@ -640,8 +640,8 @@ __device__ __forceinline__ void cp_async_wait_pending(int n) {
 // reduce-scattered over the warp.  Each round halves the values a lane holds
 // (rounds at lane distances 16, 8, ... while values remain, then a butterfly
 // over the rest), so every sum meets the same addition tree as a butterfly of
-// its own at distances 16, 8, 4, 2, 1, bit for bit, in 2*NR - 1 + log2(NR) + 1
-// shuffles instead of 10 a row.  Lanes 32/(2*NR)*m .. hold value m (row m / 2,
+// its own at distances 16, 8, 4, 2, 1, bit for bit, in 2*NR - 1 + 4 - log2(NR)
+// shuffles (6, 9, 16 for NR = 2, 4, 8) instead of 10 a row.  Lanes 32/(2*NR)*m .. hold value m (row m / 2,
 // sum m % 2); the first of them stores it as the warp's value for the row.
 template <int NR>
 __device__ __forceinline__ void ln_cols_pass_a(const float4* sdy, const float4* sxh, float* red, float4 g,
@@ -689,7 +689,8 @@ __device__ __forceinline__ void ln_cols_pass_a(const float4* sdy, const float4* 
     for (; o >= 1; o >>= 1) v[0] += __shfl_xor_sync(kFullMask, v[0], o);
     constexpr int kSpan = 32 / (2 * NR);  // lanes holding each value
     const int m = (lane / kSpan) & (2 * NR - 1);
-    if (lane % kSpan == 0 && (m >> 1) < k1 - k0) red[(size_t(h + (k0 + (m >> 1)) * sets) * wps + wi) * 2 + (m & 1)] = v[0];
+    if (lane % kSpan == 0 && (m >> 1) < k1 - k0)
+        red[(size_t(h + (k0 + (m >> 1)) * sets) * wps + wi) * 2 + (m & 1)] = v[0];
 }
 
 __global__ void __launch_bounds__(kLnColsThreads, 1)
